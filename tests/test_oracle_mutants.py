@@ -1,0 +1,85 @@
+"""Plants plausible mistakes in a temporary copy of the CPU oracle and checks
+that the oracle's pins (tests/test_oracle_pins.py) catch every one.
+
+The mistakes are planted only in copies compiled into a temporary directory;
+the committed oracle is reloaded afterwards.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "sd_oracle.cpp")
+
+MUTANTS = {
+    "residual_sign": ("std::max(0.0, p[(size_t)m][(size_t)i] - q[(size_t)m][(size_t)i])",
+                      "std::max(0.0, q[(size_t)m][(size_t)i] - p[(size_t)m][(size_t)i])"),
+    "residual_unclamped": ("std::max(0.0, p[(size_t)m][(size_t)i] - q[(size_t)m][(size_t)i])",
+                           "std::fabs(p[(size_t)m][(size_t)i] - q[(size_t)m][(size_t)i])"),
+    "accept_inverted": ("if (!(u <= r[(size_t)j]))", "if (!(u >= r[(size_t)j]))"),
+    "ratio_inverted": ("r[(size_t)j] = qd > 0.0 ? pd / qd", "r[(size_t)j] = qd > 0.0 ? qd / pd"),
+    "bonus_wrong_row": ("w = p[(size_t)K];", "w = p[(size_t)K - 1];"),
+    "greedy_emits_draft": ("res.token = amax[(size_t)m];",
+                           "res.token = m < K ? tokens[m] : amax[(size_t)m];"),
+    "cdf_off_by_one": ("      return (int)i;\n    }\n  }\n  int last",
+                       "      return (int)std::min(i + 1, w.size() - 1);\n    }\n  }\n  int last"),
+    "philox_word_swap": ("const uint32_t n1 = lo1;", "const uint32_t n1 = hi1;"),
+    "no_temperature": ("e[i] = std::exp((l[i] - m) / T);", "e[i] = std::exp(l[i] - m);"),
+    "keys_keep_drafted": ("if (i == excl ||", "if (false ||"),
+    "offsets_inclusive": ("    offsets[b] = acc;\n", "    offsets[b] = acc + tau[b];\n"),
+    "tau_off_by_one": ("res.tau = res.n_acc + 1;", "res.tau = res.n_acc;"),
+    "argmax_last_tie": ("if (l[(size_t)i] > l[(size_t)best]) best = i;",
+                        "if (l[(size_t)i] >= l[(size_t)best]) best = i;"),
+    "accept_uses_sample_slot": ("uniform_from_philox(seed, row, (uint32_t)j, 0u)",
+                                "uniform_from_philox(seed, row, (uint32_t)j, 1u)"),
+}
+
+FAST_PINS = [
+    pins.test_worked_example_greedy,
+    pins.test_bonus_when_all_greedy_drafts_match,
+    pins.test_greedy_argmax_ties_match_torch_first_occurrence,
+    lambda o: pins.test_losslessness_exact_enumeration_V4_K2(o, 0.7),
+    pins.test_identical_models_accept_everything,
+    pins.test_probabilities_match_torch_softmax_float64,
+    pins.test_outcome_keys_match_stable_sort_brute_force,
+    pins.test_key_counts_from_d3d_preparation_table,
+    pins.test_hit_test_brute_force,
+    pins.test_compaction_brute_force,
+    pins.test_invalid_rows_and_degenerate_K0,
+    pins.test_philox_known_answers,
+]
+
+
+def _caught(lib_module):
+    for pin in FAST_PINS:
+        try:
+            pin(lib_module)
+        except AssertionError:
+            return True
+    # the Monte-Carlo pin is slower: only reached when every fast pin passed
+    try:
+        pins.test_chi_square_V8_one_million_rounds(lib_module)
+    except AssertionError:
+        return True
+    return False
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = tmp_path / "sd_oracle_mutant.cpp"
+    mutated.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-ffp-contract=off",
+                    str(mutated), "-o", str(so)], check=True)
+    try:
+        oracle.load_library(str(so))
+        assert _caught(oracle), f"planted mistake '{name}' passed every pin"
+    finally:
+        oracle.load_library(oracle.build())
