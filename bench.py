@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Benchmark of the speculative-decoding verify step on GB300.
+
+One step = one verify round of the whole hot path over one batch of
+synthetic logits: temperature softmax of the target and draft rows, the
+accept/reject scan, the correction / bonus draw, tau, the outcome-prediction
+keys (top-F of the draft rows and of the bonus draft row), the hit test and
+the compaction of all rows' tokens.  On the default workload ("saguaro",
+B=32, K=6, V=128256, bf16, T=0.7, fan-out 4,3,2,1,1,1,1) that is a single
+fused sd_verify launch per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference]
+
+Prints one JSON line (rank 0).  Timing: W untimed warm-up steps, then
+exactly K steps between barrier + synchronize on both sides, CUDA events on
+the launching stream, max over ranks.  Inputs rotate over a pool of input
+sets whose total exceeds 4x the L2 size, so no step reads logits a recent
+step left in L2.  ``--impl reference`` times the CPU oracle on the host
+cores instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import sd_workloads as W  # noqa: E402
+
+HEADLINE = "saguaro"
+METRIC = "verify rounds/s"
+UNIT = "rounds/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_logits_gb300", "csrc",
+                          "sd_verify.cu")
+
+
+def describe(name):
+    s = W.WORKLOADS[name]
+    d = f"{name}: B={s['B']} K={s['K']} V={s['V']} {s['dtype']} {s['kind']} T={s['temperature']}"
+    if s.get("fanout"):
+        d += f" fanout={','.join(map(str, s['fanout']))} + draft bonus row"
+    return d
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.15)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4)
+                          if r[i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "samples": len(rows),
+                "reasons": reasons}
+
+
+# ----------------------------------------------------------- helpers --------
+def peaks():
+    try:
+        return json.load(open(PEAKS_FILE)), "measured"
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def kernel_src_hash():
+    return hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the verify kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"sd_verify_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != kernel_src_hash():
+        return None
+    return float(m.group(1))
+
+
+def algorithmic_bytes(inp: W.Inputs) -> int:
+    return W.logit_bytes(inp, algorithmic=True, with_bonus=inp.fanout is not None)
+
+
+# ---------------------------------------------------------------- GPU arm ---
+def run_gpu(args):
+    import speculative_decoding_verification_logits_gb300 as sd
+
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sd.lib()
+    name = args.workload
+    spec = W.WORKLOADS[name]
+    fan = spec.get("fanout")
+
+    # pool of input sets totalling more than 4x L2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    one = W.workload(name, round_idx=0, device=dev)
+    set_bytes = W.logit_bytes(one, algorithmic=False, with_bonus=True)
+    n_sets = max(2, int(np.ceil(4 * l2 / set_bytes)) + 1)
+    pool = [one] + [W.workload(name, round_idx=i, device=dev) for i in range(1, n_sets)]
+    B, K, V = one.B, one.K, one.V
+    for p in pool:   # distinct uniforms per rank
+        p.meta["row_base"] = rank * B
+    outs = [sd.alloc_outputs(B, K, dev, hit=True, compact=True, n_keys=sum(fan) if fan else 0)
+            for _ in range(n_sets)]
+    stream = torch.cuda.Stream(dev)
+    wss = sd.workspace(B, K, dev, stream)
+
+    def step(i):
+        p = pool[i % n_sets]
+        sd.verify(p.target, p.draft, p.tokens, p.temperature, p.seed + i // n_sets,
+                  row_base=p.meta["row_base"], fanout=fan, draft_bonus=p.draft_bonus,
+                  compact=True, out=outs[i % n_sets], ws=wss, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize(dev)
+
+    # capture G steps per graph (launch-bound inner loop), replay to cover K
+    G = min(args.steps, max(n_sets, (256 // n_sets) * n_sets))
+    graphs = {}
+
+    def graph_for(n):
+        if n not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    step(i)
+            graphs[n] = g
+        return graphs[n]
+
+    full, rem = divmod(args.steps, G)
+    plan = [G] * full + ([rem] if rem else [])
+    with torch.cuda.stream(stream):
+        for n in set(plan):
+            graph_for(n).replay()
+    torch.cuda.synchronize(dev)
+
+    def timed(fn):
+        if ws_n > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1)
+        if ws_n > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    def replay_all():
+        with torch.cuda.stream(stream):   # replay on the stream the events are on
+            for n in plan:
+                graphs[n].replay()
+
+    with ClockSampler(local) as clk:
+        ms = timed(replay_all)
+    clocks = clk.summary()
+
+    # a verification pass on the last outputs of each set (cheap sanity)
+    hit_rate = float(np.mean([o.hit.float().mean().item() for o in outs]))
+    mean_tau = float(np.mean([o.tau.float().mean().item() for o in outs]))
+    st = int(sum(o.status.item() for o in outs))
+
+    # ---- end to end: inputs from pinned host memory, results back to host
+    e2e = None
+    if not args.no_e2e:
+        host = []
+        for p in pool[:2]:
+            hp = {}
+            for k in ("target", "draft", "tokens", "temperature", "draft_bonus"):
+                t = getattr(p, k)
+                if t is not None:
+                    hp[k] = t.cpu().pin_memory()
+            host.append(hp)
+        dbuf = {k: torch.empty_like(getattr(pool[0], k)) for k in host[0]}
+        r_host = {"out_tokens": torch.empty((B, K + 1), dtype=torch.int32).pin_memory(),
+                  "tau": torch.empty(B, dtype=torch.int32).pin_memory(),
+                  "hit": torch.empty(B, dtype=torch.uint8).pin_memory(),
+                  "offsets": torch.empty(B + 1, dtype=torch.int32).pin_memory(),
+                  "packed": torch.empty(B * (K + 1), dtype=torch.int32).pin_memory()}
+        h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+        d2h = sum(t.numel() * t.element_size() for t in r_host.values())
+        out0 = outs[0]
+        n_e2e = max(1, min(args.steps, args.e2e_steps))
+
+        def e2e_steps():
+            for i in range(n_e2e):
+                hp = host[i % 2]
+                for k, t in hp.items():
+                    dbuf[k].copy_(t, non_blocking=True)
+                sd.verify(dbuf["target"], dbuf["draft"], dbuf["tokens"], dbuf["temperature"],
+                          pool[0].seed + i, row_base=rank * B, fanout=fan,
+                          draft_bonus=dbuf.get("draft_bonus"), compact=True, out=out0, ws=wss,
+                          stream=stream)
+                for k, t in r_host.items():
+                    t.copy_(getattr(out0, k), non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            e2e_steps()
+            ms_e2e = timed(e2e_steps)
+        e2e = {"value": ws_n * n_e2e / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    if ws_n > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return None
+
+    steps = args.steps
+    per_launch_ms = ms / steps
+    alg = algorithmic_bytes(one)
+    formula = W.logit_bytes(one, algorithmic=False, with_bonus=fan is not None)
+    pk, pk_kind = peaks()
+    achieved = alg / (per_launch_ms / 1e3) / 1e9
+    traffic = profiled_traffic(name)
+    line = {
+        "metric": METRIC, "value": ws_n * steps / (ms / 1e3), "unit": UNIT, "n_gpus": ws_n,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": one.meta["dtype"],
+        "data": "synthetic (seeded logits shaped like the workload; draft tokens drawn from q)",
+        "config": {"workload": describe(name), "global_batch": B * ws_n, "seq_len": K + 1,
+                   "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU",
+                   "l2": f"rotating {n_sets} input sets ({n_sets * set_bytes / 1e6:.0f} MB, "
+                         f"> 4x L2 {l2 / 1e6:.0f} MB)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                     "peak_source": pk_kind, "kernel": "sd_verify_kernel",
+                     "algorithmic_bytes_per_launch": alg, "formula_bytes_per_launch": formula},
+        "gpu_launches": steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "hit_rate": hit_rate, "mean_tau": mean_tau, "status_bits": st,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(name, args.cpu_seconds)
+    return line
+
+
+# ------------------------------------------------------------- oracle arm ---
+def _oracle_round(inp: W.Inputs, rows, threads):
+    """The oracle on the given rows of one round: outcome prediction, verify
+    (one row per call, in parallel threads), then compaction of the rows."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+
+    t = W.to_numpy_logits(inp.target)
+    d = W.to_numpy_logits(inp.draft)
+    bonus = W.to_numpy_logits(inp.draft_bonus) if inp.draft_bonus is not None else None
+    tok = inp.tokens.cpu().numpy()
+    temps = inp.temperature.cpu().numpy()
+    fan = inp.fanout
+
+    def one(b):
+        keys = None
+        if fan is not None:
+            keys = oracle.outcome_predict(d[b:b + 1], tok[b:b + 1], fan,
+                                          None if bonus is None else bonus[b:b + 1])
+        return oracle.verify(t[b:b + 1], d[b:b + 1], tok[b:b + 1], temps[b:b + 1], inp.seed,
+                             row_base=int(b), keys=keys)
+
+    with ThreadPoolExecutor(threads) as ex:
+        res = list(ex.map(one, rows))
+    out = np.concatenate([r["out_tokens"] for r in res])
+    tau = np.concatenate([r["tau"] for r in res])
+    oracle.compact(out, tau)
+    return res
+
+
+def cpu_baseline(name, seconds):
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    inp = W.workload(name, round_idx=0, device="cpu")
+    B = inp.B
+    # calibrate on one row, then size the sample to ~`seconds` of wall time
+    t0 = time.perf_counter()
+    _oracle_round(inp, [0], 1)
+    per_row = time.perf_counter() - t0
+    n_rows = int(max(1, min(B * 50, seconds * cores / max(per_row, 1e-6))))
+    rows = [i % B for i in range(n_rows)]
+    t0 = time.perf_counter()
+    _oracle_round(inp, rows, cores)
+    dt = time.perf_counter() - t0
+    return {"value": (n_rows / B) / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n_rows} rows ({n_rows / B:.2f} rounds) of {name}, one row per oracle "
+                      f"call, {cores} threads; single-thread {per_row * 1e3:.1f} ms/row"}
+
+
+def run_reference(args):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    name = args.workload
+    cores = os.cpu_count() or 1
+    inp = W.workload(name, round_idx=0, device="cpu")
+    B = inp.B
+    t0 = time.perf_counter()
+    _oracle_round(inp, [0], 1)
+    per_row = time.perf_counter() - t0
+    # rows per step so that warm-up + steps end within ~3 minutes
+    budget_rows = 180.0 * cores / max(per_row, 1e-6)
+    rows_per_step = int(max(1, min(B, budget_rows / max(1, args.steps + args.warmup))))
+    for i in range(args.warmup):
+        _oracle_round(inp, [(i * rows_per_step + r) % B for r in range(rows_per_step)], cores)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        _oracle_round(inp, [(i * rows_per_step + r) % B for r in range(rows_per_step)], cores)
+    dt = time.perf_counter() - t0
+    rounds = args.steps * rows_per_step / B
+    v = rounds / dt
+    sample = (f"each step {rows_per_step} of {B} rows of {name} (one row per oracle call, "
+              f"{cores} threads), scaled to rounds")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws_n,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": describe(name), "global_batch": B},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=HEADLINE, choices=W.ORDER)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=400)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+/*
+ * sd_verify.h — C ABI of the GB300 speculative-decoding verify library.
+ *
+ * The library implements the verify step of speculative decoding and the
+ * outcome prediction of speculative speculative decoding as hand-written
+ * CUDA kernels for sm_103a.  Every entry point is stream-ordered and
+ * asynchronous: it validates its arguments on the host, enqueues kernels on
+ * the caller's stream and returns without synchronising.  All pointers that
+ * are not marked "host" are device pointers owned by the caller; the library
+ * allocates no memory and keeps no pointer after a call returns.
+ *
+ * Sources of the method (web pages):
+ *  - "What is speculative decoding" explainer (lotook.com), section on the
+ *    four-stage loop: draft K tokens recording each position's
+ *    distribution, score all positions in one target pass, accept/reject
+ *    left to right (greedy: match the target's top choice; sampling: keep a
+ *    token the target rates at least as high as the draft, else keep it
+ *    with the target/draft probability ratio), resample the first rejected
+ *    position from a residual of both distributions, or take a bonus token
+ *    from position K+1 when all K are accepted; FAQ on losslessness.
+ *  - "Speculative Speculative Decoding" blog (jiwasawa.github.io), section
+ *    "Saguaro 1. Outcome Prediction": predict the verify outcome
+ *    (accept length, bonus token) from the draft logits' top tokens with a
+ *    fan-out per position, cache pre-speculations under those keys.
+ *  - "LLMの生成を5倍速くする「D3D」を図で読む" (animemo.app), sections
+ *    検証のしくみ③ and 検証のまとめ (greedy worked example, accept length
+ *    tau), 答え:ありうる結果すべてに、先回りして下書きする (the drafter's own
+ *    next candidates for each rejection position plus one all-accepted
+ *    key), ヒット / ミス (hit test).
+ *
+ * Readings where the pages are silent (the exact formulas are not printed):
+ *  - temperature T enters as softmax(logits / T); T == 0 is greedy;
+ *  - accept d_j iff u_j <= p_j(d_j) / q_j(d_j), u_j in (0,1];
+ *  - residual w_i = max(0, p_i - q_i) sampled by inverse CDF in index order
+ *    (the smallest i whose running sum exceeds u * sum(w)); if the residual
+ *    is identically zero the draw falls back to p;
+ *  - uniforms: Philox4x32-10 keyed by the 64-bit seed, counter
+ *    (row, position, slot, 0), word 0 -> u = ((x >> 8) + 1) * 2^-24;
+ *    slot 0 = accept test, slot 1 = residual or bonus draw; the row number
+ *    is row_base + b so that a batch split over devices draws the same
+ *    uniforms;
+ *  - greedy ties go to the lowest index.
+ */
+#ifndef SD_VERIFY_H_
+#define SD_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host-side return codes. */
+typedef enum {
+  SD_OK = 0,
+  SD_ERR_INVALID_ARG = 1, /* a null pointer, a size out of range, a bad dtype */
+  SD_ERR_UNSUPPORTED = 2, /* a valid request the library does not implement  */
+  SD_ERR_CUDA = 3         /* the CUDA runtime reported an error at launch    */
+} sd_status_t;
+
+/* Device-side status bits, OR-ed into the optional *status word.  Kernels
+ * never trap: a data error marks the affected row invalid (tau = 0, all
+ * out_tokens = -1, num_accepted = 0, hit = 0) and sets a bit here. */
+#define SD_STATUS_BAD_TOKEN 0x1u /* a draft token outside [0, V)              */
+#define SD_STATUS_BAD_TEMP 0x2u  /* a temperature < 0, NaN or infinite        */
+#define SD_STATUS_TIMEOUT 0x8u   /* a bounded wait for a bulk copy gave up    */
+
+typedef enum { SD_F32 = 0, SD_BF16 = 1 } sd_dtype_t;
+
+/* Limits of this build. */
+#define SD_MAX_K 32         /* draft tokens per row                           */
+#define SD_MAX_V 262144     /* vocabulary size                                */
+#define SD_MAX_FANOUT 8     /* outcome-prediction candidates per position     */
+
+/* sd_verify flags */
+#define SD_FLAG_PREDICT 0x1u /* also build the outcome-prediction keys from
+                                the draft rows read by this pass (keys_out)  */
+#define SD_FLAG_COMPACT 0x2u /* also pack the emitted tokens of all rows
+                                (offsets, packed), as sd_compact does         */
+
+/*
+ * Arguments of sd_verify.  Logits are contiguous, row-major, last dimension V,
+ * in the dtype given; a row need not start on any particular alignment.
+ */
+typedef struct sd_verify_args {
+  int32_t B;            /* rows (sequences) in the batch, >= 0               */
+  int32_t K;            /* draft tokens per row, 0 <= K <= SD_MAX_K          */
+  int32_t V;            /* vocabulary size, 1 <= V <= SD_MAX_V               */
+  sd_dtype_t dtype;     /* SD_F32 or SD_BF16                                  */
+  uint32_t flags;       /* SD_FLAG_*                                          */
+  uint64_t seed;        /* key of the uniforms (one per verify round)        */
+  int64_t row_base;     /* global number of row 0 (uniform counters)         */
+
+  const void *target_logits;   /* [B][K+1][V]  required                      */
+  const void *draft_logits;    /* [B][K][V]    required when K > 0           */
+  const int32_t *draft_tokens; /* [B][K]       required when K > 0           */
+  const float *temperature;    /* [B]          required; 0 => greedy row     */
+
+  /* Outcome-prediction keys to test the outcome against (optional):
+   * [B][n_keys][2] pairs (position, token) as written by sd_outcome_predict;
+   * (-1,-1) marks an empty slot.  Ignored when SD_FLAG_PREDICT is set. */
+  const int32_t *cache_keys;
+  int32_t n_keys;
+
+  /* Fused outcome prediction (SD_FLAG_PREDICT): fanout_host [K+1] (host),
+   * each 0..SD_MAX_FANOUT; draft_bonus_logits [B][V] optional; keys_out
+   * [B][sum(fanout)][2].  The hit test then uses keys_out. */
+  const int32_t *fanout_host;
+  const void *draft_bonus_logits;
+  int32_t *keys_out;
+
+  /* Outputs (required). */
+  int32_t *num_accepted; /* [B]                                              */
+  int32_t *out_tokens;   /* [B][K+1]: accepted drafts, then the corrected or
+                            bonus token, then -1                              */
+  int32_t *tau;          /* [B]: num_accepted + 1 (0 for an invalid row)     */
+
+  /* Optional outputs (may be null). */
+  uint8_t *hit;          /* [B]: 1 if (num_accepted, emitted token) is a key */
+  int32_t *offsets;      /* [B+1] with SD_FLAG_COMPACT: exclusive scan of tau */
+  int32_t *packed;       /* [B*(K+1)] with SD_FLAG_COMPACT                    */
+  float *accept_ratio;   /* [B][K]: p_j(d_j) / q_j(d_j), sampled rows only    */
+  float *p_draft;        /* [B][K]: p_j(d_j), sampled rows only               */
+  float *q_draft;        /* [B][K]: q_j(d_j), sampled rows only               */
+  int32_t *target_argmax;/* [B][K+1]: top target token per position          */
+  int32_t *status;       /* one int32, SD_STATUS_* bits OR-ed in             */
+
+  /* Scratch: at least sd_verify_workspace_size(B, K) bytes, 16-byte
+   * aligned, filled with zeros before its first use.  It holds per-row
+   * completion counters and per-position results; every call that returns
+   * SD_OK and whose status has no SD_STATUS_TIMEOUT bit leaves it all zero
+   * again, so the same buffer serves the next call on the same stream (any
+   * B and K that fit) without being cleared.  Calls that overlap on the GPU
+   * need separate workspaces. */
+  void *workspace;
+  size_t workspace_bytes;
+} sd_verify_args;
+
+/* Bytes of scratch sd_verify needs for a batch of B rows of K drafts. */
+size_t sd_verify_workspace_size(int32_t B, int32_t K);
+
+/*
+ * The verify step: per-row temperature softmax of the K+1 target and K draft
+ * rows, the left-to-right accept/reject scan (argmax match for T == 0), the
+ * correction token from the residual at the first rejection or the bonus
+ * token from target row K, tau, the optional hit test, and optionally the
+ * outcome-prediction keys and the compaction of all rows' tokens.
+ * Each logit row is read from memory once.
+ */
+sd_status_t sd_verify(const sd_verify_args *args, void *stream);
+
+/*
+ * Outcome prediction: for each row b and position k < K, the fanout[k]
+ * tokens with the highest draft logit at k other than the drafted token
+ * d_k (ties to the lowest index, -inf logits never chosen), keyed (k, token):
+ * the corrections a rejection at k could produce.  For k == K the fanout[K]
+ * highest logits of draft_bonus_logits [B][V] (optional; without it those
+ * slots stay empty), keyed (K, token): the bonus token when all K are
+ * accepted.  keys: [B][n_keys][2], n_keys = sum(fanout); empty slots are
+ * (-1,-1).  fanout_host and n_keys_out are host pointers.
+ */
+sd_status_t sd_outcome_predict(int32_t B, int32_t K, int32_t V, sd_dtype_t dtype,
+                               const void *draft_logits, const int32_t *draft_tokens,
+                               const void *draft_bonus_logits, const int32_t *fanout_host,
+                               int32_t *keys, int32_t *n_keys_out, int32_t *status,
+                               void *stream);
+
+/*
+ * Compaction: offsets[b] = sum of tau over rows before b (B+1 entries) and
+ * packed[offsets[b] + i] = out_tokens[b][i] for i < tau[b].  packed needs
+ * room for B*(K+1) tokens.  Entries of tau outside [0, K+1] set
+ * SD_STATUS_BAD_TOKEN in *status (optional) and count as 0.
+ */
+sd_status_t sd_compact(int32_t B, int32_t K, const int32_t *out_tokens, const int32_t *tau,
+                       int32_t *offsets, int32_t *packed, int32_t *status, void *stream);
+
+/*
+ * The uniforms the verify step draws: out[i] = u(seed, row[i], pos[i],
+ * slot[i]) as defined above, for n entries (device arrays).  Lets callers
+ * reproduce or audit a round.
+ */
+sd_status_t sd_uniforms(uint64_t seed, int32_t n, const int32_t *row, const int32_t *pos,
+                        const int32_t *slot, double *out, void *stream);
+
+/* sizeof(sd_verify_args) as compiled into the library, so that bindings
+ * can check their mirror of the struct. */
+size_t sd_verify_args_size(void);
+
+/* Version string of the library (static storage). */
+const char *sd_version(void);
+
+/* Name of a host-side return code (static storage). */
+const char *sd_status_string(sd_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SD_VERIFY_H_ */

@@ -1,0 +1,318 @@
+"""GB300-native speculative-decoding verify step (Python binding).
+
+Thin ctypes binding of ``libsdverify.so`` (C ABI in ``include/sd_verify.h``).
+This module only marshals arguments: it checks tensor dtypes, devices and
+shapes, allocates outputs with torch, and passes raw device pointers and the
+current CUDA stream to the library.  Every step of the verify path runs in
+the library's CUDA kernels; there is no CPU fallback, and importing or calling
+without the built library raises.
+
+Entry points (same names as the C ABI):
+  verify(...)            sd_verify
+  outcome_predict(...)   sd_outcome_predict
+  compact(...)           sd_compact
+  uniforms(...)          sd_uniforms
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+from . import _build
+
+SD_OK, SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED, SD_ERR_CUDA = 0, 1, 2, 3
+SD_STATUS_BAD_TOKEN, SD_STATUS_BAD_TEMP, SD_STATUS_TIMEOUT = 0x1, 0x2, 0x8
+SD_F32, SD_BF16 = 0, 1
+SD_FLAG_PREDICT, SD_FLAG_COMPACT = 0x1, 0x2
+SD_MAX_K, SD_MAX_V, SD_MAX_FANOUT = 32, 262144, 8
+
+_P = ctypes.c_void_p
+
+
+class VerifyArgs(ctypes.Structure):
+    """Mirror of ``sd_verify_args`` in include/sd_verify.h."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("K", ctypes.c_int32), ("V", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32),
+        ("seed", ctypes.c_uint64), ("row_base", ctypes.c_int64),
+        ("target_logits", _P), ("draft_logits", _P), ("draft_tokens", _P),
+        ("temperature", _P), ("cache_keys", _P), ("n_keys", ctypes.c_int32),
+        ("fanout_host", _P), ("draft_bonus_logits", _P), ("keys_out", _P),
+        ("num_accepted", _P), ("out_tokens", _P), ("tau", _P),
+        ("hit", _P), ("offsets", _P), ("packed", _P),
+        ("accept_ratio", _P), ("p_draft", _P), ("q_draft", _P), ("target_argmax", _P),
+        ("status", _P), ("workspace", _P), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load (building first if the sources are newer) libsdverify.so."""
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            if _build.stale():
+                _build.build()
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError("libsdverify.so is missing; run __graft_entry__.build()")
+            L = ctypes.CDLL(_build.LIB)
+            i32, u64, sz = ctypes.c_int32, ctypes.c_uint64, ctypes.c_size_t
+            L.sd_verify_workspace_size.argtypes = [i32, i32]
+            L.sd_verify_workspace_size.restype = sz
+            L.sd_verify.argtypes = [ctypes.POINTER(VerifyArgs), _P]
+            L.sd_verify.restype = ctypes.c_int
+            L.sd_outcome_predict.argtypes = [i32, i32, i32, ctypes.c_int, _P, _P, _P, _P, _P, _P,
+                                             _P, _P]
+            L.sd_outcome_predict.restype = ctypes.c_int
+            L.sd_compact.argtypes = [i32, i32, _P, _P, _P, _P, _P, _P]
+            L.sd_compact.restype = ctypes.c_int
+            L.sd_uniforms.argtypes = [u64, i32, _P, _P, _P, _P, _P]
+            L.sd_uniforms.restype = ctypes.c_int
+            L.sd_verify_args_size.argtypes = []
+            L.sd_verify_args_size.restype = sz
+            if L.sd_verify_args_size() != ctypes.sizeof(VerifyArgs):
+                raise RuntimeError("sd_verify_args layout differs between library and binding")
+            L.sd_version.argtypes = []
+            L.sd_version.restype = ctypes.c_char_p
+            L.sd_status_string.argtypes = [ctypes.c_int]
+            L.sd_status_string.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+class SDError(RuntimeError):
+    pass
+
+
+def _check(rc: int, what: str):
+    if rc != SD_OK:
+        raise SDError(f"{what} failed: {lib().sd_status_string(rc).decode()}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device, stream):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SD_F32
+    if t.dtype == torch.bfloat16:
+        return SD_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _need(t, name, dtype=None, shape=None, device=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+_ws = {}
+_ws_lock = threading.Lock()
+
+
+def workspace_bytes(B: int, K: int) -> int:
+    return int(lib().sd_verify_workspace_size(B, K))
+
+
+def workspace(B: int, K: int, device=None, stream=None) -> torch.Tensor:
+    """A zero-filled scratch buffer for sd_verify, cached per (device,
+    stream).  The library leaves it zeroed after every successful call, so
+    it is cleared only once."""
+    device = torch.device(device if device is not None else torch.cuda.current_device())
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    need = workspace_bytes(B, K)
+    key = (device.index, s.cuda_stream)
+    with _ws_lock:
+        buf = _ws.get(key)
+        if buf is None or buf.numel() < need:
+            buf = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=device)
+            _ws[key] = buf
+    return buf
+
+
+@dataclass
+class VerifyResult:
+    num_accepted: torch.Tensor      # [B] int32
+    out_tokens: torch.Tensor        # [B][K+1] int32
+    tau: torch.Tensor               # [B] int32
+    hit: torch.Tensor | None = None           # [B] uint8
+    offsets: torch.Tensor | None = None       # [B+1] int32
+    packed: torch.Tensor | None = None        # [B*(K+1)] int32
+    keys: torch.Tensor | None = None          # [B][n_keys][2] int32
+    accept_ratio: torch.Tensor | None = None  # [B][K] float32
+    p_draft: torch.Tensor | None = None
+    q_draft: torch.Tensor | None = None
+    target_argmax: torch.Tensor | None = None  # [B][K+1] int32
+    status: torch.Tensor | None = None        # [1] int32
+
+
+def alloc_outputs(B, K, device, *, hit=False, compact=False, stats=False, n_keys=0,
+                  status=True) -> VerifyResult:
+    e = lambda *s, dt=torch.int32: torch.empty(s, dtype=dt, device=device)
+    r = VerifyResult(e(B), e(B, K + 1), e(B))
+    if hit or n_keys:
+        r.hit = e(B, dt=torch.uint8)
+    if compact:
+        r.offsets, r.packed = e(B + 1), e(max(B * (K + 1), 1))
+    if n_keys:
+        r.keys = e(B, n_keys, 2)
+    if stats:
+        r.accept_ratio = torch.full((B, K), float("nan"), device=device)
+        r.p_draft = torch.full((B, K), float("nan"), device=device)
+        r.q_draft = torch.full((B, K), float("nan"), device=device)
+        r.target_argmax = e(B, K + 1)
+    if status:
+        r.status = torch.zeros(1, dtype=torch.int32, device=device)
+    return r
+
+
+def verify(target, draft, tokens, temperature, seed: int, *, row_base: int = 0,
+           cache_keys=None, fanout=None, draft_bonus=None, compact: bool = False,
+           stats: bool = False, out: VerifyResult | None = None, ws=None,
+           stream=None) -> VerifyResult:
+    """Run sd_verify on the current (or given) stream.
+
+    target [B][K+1][V], draft [B][K][V] (float32 or bfloat16, CUDA,
+    contiguous), tokens [B][K] int32, temperature [B] float32.  cache_keys:
+    [B][n_keys][2] int32 keys to test the outcome against.  fanout ([K+1]
+    ints) asks for the outcome-prediction keys to be built in the same pass
+    (draft_bonus [B][V] optional).  compact=True also packs the tokens."""
+    _need(target, "target")
+    dev = target.device
+    B, K1, V = target.shape
+    K = K1 - 1
+    dt = _dtype_code(target)
+    if K > 0:
+        _need(draft, "draft", target.dtype, (B, K, V), dev)
+        _need(tokens, "tokens", torch.int32, (B, K), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    n_keys = 0
+    flags = 0
+    fan_arr = None
+    if fanout is not None:
+        fanout = [int(f) for f in fanout]
+        if len(fanout) != K + 1:
+            raise ValueError("fanout needs K+1 entries")
+        n_keys = sum(fanout)
+        fan_arr = (ctypes.c_int32 * (K + 1))(*fanout)
+        flags |= SD_FLAG_PREDICT
+        if draft_bonus is not None:
+            _need(draft_bonus, "draft_bonus", target.dtype, (B, V), dev)
+    if cache_keys is not None:
+        _need(cache_keys, "cache_keys", torch.int32, None, dev)
+        if cache_keys.dim() != 3 or cache_keys.shape[0] != B or cache_keys.shape[2] != 2:
+            raise ValueError("cache_keys must be [B][n_keys][2]")
+    if compact:
+        flags |= SD_FLAG_COMPACT
+    r = out or alloc_outputs(B, K, dev, hit=cache_keys is not None or n_keys > 0,
+                             compact=compact, stats=stats, n_keys=n_keys)
+    w = ws if ws is not None else workspace(B, K, dev, stream)
+    a = VerifyArgs()
+    a.B, a.K, a.V, a.dtype, a.flags = B, K, V, dt, flags
+    a.seed, a.row_base = int(seed) & (2 ** 64 - 1), int(row_base)
+    a.target_logits, a.draft_logits = target.data_ptr(), (draft.data_ptr() if K > 0 else None)
+    a.draft_tokens = tokens.data_ptr() if K > 0 else None
+    a.temperature = temperature.data_ptr()
+    if cache_keys is not None:
+        a.cache_keys, a.n_keys = cache_keys.data_ptr(), cache_keys.shape[1]
+    if fan_arr is not None:
+        a.fanout_host = ctypes.cast(fan_arr, ctypes.c_void_p)
+        a.draft_bonus_logits = draft_bonus.data_ptr() if draft_bonus is not None else None
+        a.keys_out = r.keys.data_ptr() if n_keys else None
+    a.num_accepted, a.out_tokens, a.tau = (r.num_accepted.data_ptr(), r.out_tokens.data_ptr(),
+                                          r.tau.data_ptr())
+    a.hit = r.hit.data_ptr() if r.hit is not None else None
+    if compact:
+        a.offsets, a.packed = r.offsets.data_ptr(), r.packed.data_ptr()
+    if r.accept_ratio is not None:
+        a.accept_ratio, a.p_draft, a.q_draft = (r.accept_ratio.data_ptr(), r.p_draft.data_ptr(),
+                                                r.q_draft.data_ptr())
+        a.target_argmax = r.target_argmax.data_ptr()
+    a.status = r.status.data_ptr() if r.status is not None else None
+    a.workspace, a.workspace_bytes = w.data_ptr(), w.numel()
+    _check(lib().sd_verify(ctypes.byref(a), _stream(dev, stream)), "sd_verify")
+    return r
+
+
+def outcome_predict(draft, tokens, fanout, draft_bonus=None, *, keys=None, status=None,
+                    stream=None) -> torch.Tensor:
+    """Speculation-cache keys [B][sum(fanout)][2] (position, token)."""
+    _need(draft, "draft")
+    B, K, V = draft.shape
+    dev = draft.device
+    dt = _dtype_code(draft)
+    _need(tokens, "tokens", torch.int32, (B, K), dev)
+    fanout = [int(f) for f in fanout]
+    if len(fanout) != K + 1:
+        raise ValueError("fanout needs K+1 entries")
+    if draft_bonus is not None:
+        _need(draft_bonus, "draft_bonus", draft.dtype, (B, V), dev)
+    n = sum(fanout)
+    if keys is None:
+        keys = torch.empty((B, n, 2), dtype=torch.int32, device=dev)
+    fan_arr = (ctypes.c_int32 * (K + 1))(*fanout)
+    n_out = ctypes.c_int32(0)
+    _check(lib().sd_outcome_predict(B, K, V, dt, _ptr(draft), _ptr(tokens), _ptr(draft_bonus),
+                                    ctypes.cast(fan_arr, ctypes.c_void_p), _ptr(keys),
+                                    ctypes.cast(ctypes.byref(n_out), ctypes.c_void_p),
+                                    _ptr(status), _stream(dev, stream)), "sd_outcome_predict")
+    assert n_out.value == n
+    return keys
+
+
+def compact(out_tokens, tau, *, offsets=None, packed=None, status=None, stream=None):
+    """(offsets [B+1], packed [B*(K+1)]) from out_tokens [B][K+1] and tau [B]."""
+    _need(out_tokens, "out_tokens", torch.int32)
+    B, K1 = out_tokens.shape
+    dev = out_tokens.device
+    _need(tau, "tau", torch.int32, (B,), dev)
+    if offsets is None:
+        offsets = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    if packed is None:
+        packed = torch.empty(max(B * K1, 1), dtype=torch.int32, device=dev)
+    _check(lib().sd_compact(B, K1 - 1, _ptr(out_tokens), _ptr(tau), _ptr(offsets), _ptr(packed),
+                            _ptr(status), _stream(dev, stream)), "sd_compact")
+    return offsets, packed
+
+
+def uniforms(seed: int, row, pos, slot, *, stream=None) -> torch.Tensor:
+    """The verify step's uniforms u(seed, row, pos, slot) (float64)."""
+    _need(row, "row", torch.int32)
+    dev = row.device
+    _need(pos, "pos", torch.int32, tuple(row.shape), dev)
+    _need(slot, "slot", torch.int32, tuple(row.shape), dev)
+    out = torch.empty(row.shape, dtype=torch.float64, device=dev)
+    _check(lib().sd_uniforms(int(seed) & (2 ** 64 - 1), row.numel(), _ptr(row), _ptr(pos),
+                             _ptr(slot), _ptr(out), _stream(dev, stream)), "sd_uniforms")
+    return out
+
+
+def version() -> str:
+    return lib().sd_version().decode()

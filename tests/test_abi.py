@@ -1,0 +1,69 @@
+"""The C-ABI library loads and exports every symbol the headers declare
+(host-side checks only: no CUDA compute is called here)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_logits_gb300 as sd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(sd_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    L = sd.lib()
+    names = _declared_functions()
+    assert "sd_verify" in names and "sd_outcome_predict" in names and "sd_compact" in names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_struct_layout_and_strings():
+    L = sd.lib()
+    assert L.sd_verify_args_size() == ctypes.sizeof(sd.VerifyArgs)
+    assert "sm_103a" in sd.version()
+    assert L.sd_status_string(sd.SD_ERR_INVALID_ARG) == b"SD_ERR_INVALID_ARG"
+
+
+def test_workspace_size_grows_with_batch():
+    a, b = sd.workspace_bytes(8, 5), sd.workspace_bytes(256, 5)
+    assert 0 < a < b and a % 256 == 0
+    assert sd.lib().sd_verify_workspace_size(4, sd.SD_MAX_K + 1) == 0
+
+
+def test_host_argument_checks_reject_bad_requests():
+    L = sd.lib()
+    assert L.sd_verify(None, None) == sd.SD_ERR_INVALID_ARG
+    a = sd.VerifyArgs()
+    a.B, a.K, a.V = 4, sd.SD_MAX_K + 1, 100
+    assert L.sd_verify(ctypes.byref(a), None) == sd.SD_ERR_INVALID_ARG
+    a.K, a.V = 4, 0
+    assert L.sd_verify(ctypes.byref(a), None) == sd.SD_ERR_INVALID_ARG
+    a.V, a.dtype = 100, 7
+    assert L.sd_verify(ctypes.byref(a), None) == sd.SD_ERR_INVALID_ARG
+    a.dtype = sd.SD_BF16
+    assert L.sd_verify(ctypes.byref(a), None) == sd.SD_ERR_INVALID_ARG   # null pointers
+    assert L.sd_compact(-1, 2, None, None, None, None, None, None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_uniforms(1, -1, None, None, None, None, None) == sd.SD_ERR_INVALID_ARG
+    fan = (ctypes.c_int32 * 3)(1, 9, 1)
+    assert L.sd_outcome_predict(2, 2, 10, sd.SD_BF16, None, None, None,
+                                ctypes.cast(fan, ctypes.c_void_p), None, None, None,
+                                None) == sd.SD_ERR_INVALID_ARG
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    t = torch.zeros(2, 3, 10)
+    with pytest.raises(ValueError):
+        sd.verify(t, t[:, :2], torch.zeros(2, 2, dtype=torch.int32), torch.zeros(2), 1)

@@ -1,0 +1,296 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small shapes that span several CTA slices and ragged tails are compared in
+full; the five workloads at full size are compared on sampled rows (rows
+are independent, so the oracle recomputes a row alone with its global row
+number), in the launch configuration the benchmark uses.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sd_workloads as W
+from tests.parity import compare_verify
+
+pytestmark = pytest.mark.gpu
+
+sd = pytest.importorskip("speculative_decoding_verification_logits_gb300")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    oracle.build()
+    return torch.device("cuda:0")
+
+
+def _np(t):
+    return W.to_numpy_logits(t)
+
+
+def _oracle_for(inp, rows=None, keys=None):
+    t, d = inp.target, inp.draft
+    tok, temps = inp.tokens, inp.temperature
+    if rows is None:
+        return oracle.verify(_np(t), _np(d), tok.cpu().numpy(), temps.cpu().numpy(), inp.seed,
+                             keys=keys, stats=True)
+    outs = []
+    for b in rows:
+        k = None if keys is None else keys[b:b + 1]
+        outs.append(oracle.verify(_np(t[b:b + 1]), _np(d[b:b + 1]), tok[b:b + 1].cpu().numpy(),
+                                  temps[b:b + 1].cpu().numpy(), inp.seed, row_base=int(b),
+                                  keys=k, stats=True))
+    return {k: np.concatenate([o[k] for o in outs]) if isinstance(outs[0][k], np.ndarray)
+            else sum(o[k] for o in outs) for k in outs[0]}
+
+
+def _check(stats, bad):
+    assert not bad, bad[:10]
+    assert stats["mismatch_outside_guard"] == 0
+
+
+# ----------------------------------------------------------------- uniforms --
+def test_uniforms_bit_exact_with_oracle(dev):
+    rng = np.random.default_rng(1)
+    n = 4096
+    row = torch.from_numpy(rng.integers(0, 2 ** 31 - 1, n).astype(np.int32)).to(dev)
+    pos = torch.from_numpy(rng.integers(0, 33, n).astype(np.int32)).to(dev)
+    slot = torch.from_numpy(rng.integers(0, 2, n).astype(np.int32)).to(dev)
+    for seed in (0, 1234, 2 ** 63 + 12345, 0xFFFFFFFFFFFFFFFF):
+        u = sd.uniforms(seed, row, pos, slot).cpu().numpy()
+        ro, po, so = row.cpu().numpy(), pos.cpu().numpy(), slot.cpu().numpy()
+        ref = np.array([oracle.uniform(seed, int(ro[i]), int(po[i]), int(so[i])) for i in range(n)])
+        np.testing.assert_array_equal(u, ref)
+
+
+# ----------------------------------------------------------- worked example --
+def test_worked_example_greedy(dev):
+    from tests.test_oracle_pins import _worked_example_inputs
+    g, ids, target, draftl, tokens = _worked_example_inputs()
+    K = tokens.size
+    r = sd.verify(torch.from_numpy(target[None]).to(dev), torch.from_numpy(draftl[None]).to(dev),
+                  torch.from_numpy(tokens[None]).to(dev), torch.zeros(1, device=dev), seed=1,
+                  compact=True)
+    assert int(r.num_accepted[0]) == int(g["expect_n_accepted"][0])
+    assert int(r.tau[0]) == int(g["expect_tau"][0])
+    assert r.packed[: int(r.offsets[1])].tolist() == [ids[w] for w in g["expect_packed"]]
+    assert r.out_tokens[0, K - 1].item() == -1
+
+
+# ------------------------------------------------- small shapes, full compare --
+SHAPES = [
+    # (B, K, V, dtype)
+    (3, 4, 1000, "f32"),
+    (4, 3, 4099, "bf16"),      # odd V: rows start off the 16-byte grid
+    (5, 5, 20000, "bf16"),
+    (2, 2, 32001, "f32"),
+    (3, 6, 1, "bf16"),         # one-token vocabulary
+    (4, 2, 17, "f32"),
+    (2, 0, 777, "bf16"),       # K = 0: a plain sampling step
+    (6, 8, 151936, "bf16"),    # largest vocabulary of the workloads
+]
+
+
+@pytest.mark.parametrize("B,K,V,dt", SHAPES)
+@pytest.mark.parametrize("kind", ["normal", "peaked"])
+def test_small_shapes_full_parity(dev, B, K, V, dt, kind):
+    temps = [0.0, 0.6, 1.0, 1.7, 0.3, 1.0][:B]
+    inp = W.synth(B, K, V, dt, kind=kind, sigma=2.0, draft_sigma=0.7, peaks=3 if V > 8 else 0,
+                  temperature=temps, seed=B * 1000 + K * 10 + V, device=dev)
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, stats=True,
+                  compact=True)
+    torch.cuda.synchronize()
+    o = _oracle_for(inp)
+    stats, bad = compare_verify(r, o, temps)
+    _check(stats, bad)
+    offs, packed = oracle.compact(r.out_tokens.cpu().numpy(), r.tau.cpu().numpy())
+    np.testing.assert_array_equal(r.offsets.cpu().numpy(), offs)
+    np.testing.assert_array_equal(r.packed.cpu().numpy()[: offs[-1]], packed)
+    assert int(r.status.item()) == 0
+
+
+def test_zipf_and_ties_and_neg_inf(dev):
+    B, K, V = 4, 3, 3001
+    inp = W.synth(B, K, V, "bf16", kind="zipf", temperature=[1.0, 0.0, 0.6, 1.0], seed=77,
+                  device=dev)
+    # ties and -inf logits: quantise some rows and knock out a block of tokens
+    t = inp.target.float()
+    t[1] = torch.round(t[1] * 2) / 2
+    t[2, :, 100:400] = float("-inf")
+    inp.target = t.to(torch.bfloat16).contiguous()
+    d = inp.draft.float()
+    d[2, :, 500:700] = float("-inf")
+    inp.draft = d.to(torch.bfloat16).contiguous()
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, stats=True)
+    o = _oracle_for(inp)
+    _check(*compare_verify(r, o, inp.temperature.cpu().numpy()))
+
+
+# ------------------------------------------------------ outcome prediction ----
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_outcome_keys_standalone_and_fused(dev, dt):
+    B, K, V = 5, 6, 12007
+    fan = [4, 3, 2, 1, 1, 1, 1]
+    inp = W.synth(B, K, V, dt, kind="peaked", sigma=3.0, draft_sigma=1.0, peaks=20,
+                  temperature=[0.7, 0.0, 1.0, 0.7, 0.7], seed=5, device=dev, bonus_row=True)
+    # ties in the draft logits of one row
+    d = inp.draft.float()
+    d[3] = torch.round(d[3])
+    inp.draft = d.to(inp.target.dtype).contiguous()
+    keys_ref = oracle.outcome_predict(_np(inp.draft), inp.tokens.cpu().numpy(), fan,
+                                      _np(inp.draft_bonus))
+    keys = sd.outcome_predict(inp.draft, inp.tokens, fan, inp.draft_bonus)
+    np.testing.assert_array_equal(keys.cpu().numpy(), keys_ref)
+    keys_nb = sd.outcome_predict(inp.draft, inp.tokens, fan, None)
+    np.testing.assert_array_equal(
+        keys_nb.cpu().numpy(), oracle.outcome_predict(_np(inp.draft), inp.tokens.cpu().numpy(), fan))
+    # fused into the verify pass, and the hit test on both paths
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, fanout=fan,
+                  draft_bonus=inp.draft_bonus, stats=True)
+    np.testing.assert_array_equal(r.keys.cpu().numpy(), keys_ref)
+    r2 = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, cache_keys=keys)
+    o = _oracle_for(inp, keys=keys_ref)
+    _check(*compare_verify(r, o, inp.temperature.cpu().numpy()))
+    _check(*compare_verify(r2, o, inp.temperature.cpu().numpy(), check_stats=False))
+
+
+def test_d3d_key_counts(dev):
+    B, K, V = 2, 15, 4096
+    inp = W.synth(B, K, V, "bf16", kind="normal", temperature=0.0, seed=9, device=dev,
+                  bonus_row=True)
+    for positions, cands, tokens_prepared in [(11, 2, 384), (15, 2, 512), (11, 5, 912)]:
+        fan = [cands] * positions + [0] * (K - positions) + [1]
+        keys = sd.outcome_predict(inp.draft, inp.tokens, fan, inp.draft_bonus)
+        assert (keys.shape[1] + 1) * 16 == tokens_prepared
+        ref = oracle.outcome_predict(_np(inp.draft), inp.tokens.cpu().numpy(), fan,
+                                     _np(inp.draft_bonus))
+        np.testing.assert_array_equal(keys.cpu().numpy(), ref)
+
+
+# --------------------------------------------------------------- edge cases ----
+def test_invalid_rows_set_status_and_empty_batch(dev):
+    B, K, V = 4, 3, 999
+    inp = W.synth(B, K, V, "f32", temperature=[1.0, 1.0, 1.0, 0.0], seed=3, device=dev)
+    inp.tokens[1, 2] = V
+    inp.temperature[2] = -1.0
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, compact=True)
+    st = int(r.status.item())
+    assert st & sd.SD_STATUS_BAD_TOKEN and st & sd.SD_STATUS_BAD_TEMP
+    assert r.tau[1].item() == 0 and r.tau[2].item() == 0
+    assert (r.out_tokens[1] == -1).all() and (r.out_tokens[2] == -1).all()
+    o = _oracle_for(inp)
+    _check(*compare_verify(r, o, inp.temperature.cpu().numpy(), check_stats=False))
+    # empty batch
+    e = torch.empty((0, K + 1, V), device=dev)
+    r0 = sd.verify(e, torch.empty((0, K, V), device=dev), torch.empty((0, K), dtype=torch.int32,
+                   device=dev), torch.empty(0, device=dev), 1, compact=True)
+    assert r0.offsets.tolist() == [0]
+
+
+def test_workspace_is_left_zeroed_and_reusable(dev):
+    B, K, V = 8, 5, 5000
+    inp = W.synth(B, K, V, "bf16", kind="peaked", peaks=4, temperature=0.8, seed=21, device=dev)
+    ws = torch.zeros(sd.workspace_bytes(B, K), dtype=torch.uint8, device=dev)
+    a = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, ws=ws,
+                  compact=True)
+    torch.cuda.synchronize()
+    b = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, ws=ws,
+                  compact=True)
+    n = int(a.offsets[-1])
+    assert torch.equal(a.out_tokens, b.out_tokens) and torch.equal(a.packed[:n], b.packed[:n])
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero().item()) == 0
+    # a smaller batch with another K reuses the same buffer
+    inp2 = W.synth(3, 2, 777, "f32", temperature=[0.0, 1.0, 0.5], seed=2, device=dev)
+    c = sd.verify(inp2.target, inp2.draft, inp2.tokens, inp2.temperature, inp2.seed, ws=ws)
+    o = _oracle_for(inp2)
+    _check(*compare_verify(c, o, inp2.temperature.cpu().numpy(), check_stats=False))
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero().item()) == 0
+
+
+def test_row_base_splits_batch_identically(dev):
+    B, K, V = 10, 4, 9000
+    inp = W.synth(B, K, V, "bf16", kind="normal", temperature=0.9, seed=31, device=dev)
+    full = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed)
+    h = B // 2
+    lo = sd.verify(inp.target[:h].contiguous(), inp.draft[:h].contiguous(),
+                   inp.tokens[:h].contiguous(), inp.temperature[:h].contiguous(), inp.seed)
+    hi = sd.verify(inp.target[h:].contiguous(), inp.draft[h:].contiguous(),
+                   inp.tokens[h:].contiguous(), inp.temperature[h:].contiguous(), inp.seed,
+                   row_base=h)
+    assert torch.equal(full.out_tokens, torch.cat([lo.out_tokens, hi.out_tokens]))
+
+
+def test_compact_standalone(dev):
+    rng = np.random.default_rng(4)
+    B, K = 3000, 5
+    tau = rng.integers(0, K + 2, B).astype(np.int32)
+    out = np.full((B, K + 1), -1, np.int32)
+    for b in range(B):
+        out[b, : tau[b]] = rng.integers(0, 10 ** 6, tau[b])
+    offs, packed = sd.compact(torch.from_numpy(out).to(dev), torch.from_numpy(tau).to(dev))
+    ro, rp = oracle.compact(out, tau)
+    np.testing.assert_array_equal(offs.cpu().numpy(), ro)
+    np.testing.assert_array_equal(packed.cpu().numpy()[: ro[-1]], rp)
+
+
+# ------------------------------------------- workloads at full size, sampled --
+@pytest.mark.parametrize("name", W.ORDER)
+def test_workload_full_size_sampled_rows(dev, name):
+    inp = W.workload(name, round_idx=3, device=dev)
+    spec = W.WORKLOADS[name]
+    fan = spec.get("fanout")
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, fanout=fan,
+                  draft_bonus=inp.draft_bonus, compact=True, stats=True)
+    torch.cuda.synchronize()
+    B = inp.B
+    rng = np.random.default_rng(hash(name) % 2 ** 32)
+    rows = sorted(set([0, B - 1] + list(rng.choice(B, size=min(B, 6), replace=False))))
+    keys_ref = None
+    if fan is not None:
+        keys_ref = oracle.outcome_predict(_np(inp.draft[rows]), inp.tokens[rows].cpu().numpy(),
+                                          fan, _np(inp.draft_bonus[rows]))
+        np.testing.assert_array_equal(r.keys.cpu().numpy()[rows], keys_ref)
+        full_keys = np.zeros((B,) + keys_ref.shape[1:], np.int32)
+        full_keys[rows] = keys_ref
+        keys_ref = full_keys
+    o = _oracle_for(inp, rows=rows, keys=keys_ref)
+    stats, bad = compare_verify(r, o, inp.temperature.cpu().numpy()[rows], rows=rows)
+    _check(stats, bad)
+    # compaction over every row (integer work: exact)
+    offs, packed = oracle.compact(r.out_tokens.cpu().numpy(), r.tau.cpu().numpy())
+    np.testing.assert_array_equal(r.offsets.cpu().numpy(), offs)
+    np.testing.assert_array_equal(r.packed.cpu().numpy()[: offs[-1]], packed)
+    # properties that hold for every row
+    tau = r.tau.cpu().numpy()
+    na = r.num_accepted.cpu().numpy()
+    assert ((tau >= 1) & (tau <= inp.K + 1)).all() and (tau == na + 1).all()
+    ot = r.out_tokens.cpu().numpy()
+    tok = inp.tokens.cpu().numpy()
+    for b in range(B):
+        assert (ot[b, : na[b]] == tok[b, : na[b]]).all()
+        assert 0 <= ot[b, na[b]] < inp.V and (ot[b, na[b] + 1:] == -1).all()
+        if na[b] < inp.K and inp.temperature[b].item() > 0:
+            assert ot[b, na[b]] != tok[b, na[b]]     # the residual excludes a rejected draft
+    assert int(r.status.item()) == 0
+
+
+@pytest.mark.parametrize("name,rounds", [("small", 200), ("peaked", 40)])
+def test_many_rounds_mismatch_count(dev, name, rounds):
+    """Every sampled row compared in full over many rounds: no difference
+    outside the guard band; guarded rows counted."""
+    tot = dict(rows=0, positions=0, guarded=0, guarded_mismatch=0, mismatch_outside_guard=0)
+    for rd in range(rounds):
+        inp = W.workload(name, round_idx=rd, device=dev)
+        r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, stats=True)
+        o = _oracle_for(inp)
+        stats, bad = compare_verify(r, o, inp.temperature.cpu().numpy())
+        assert not bad, (rd, bad[:5])
+        for k in tot:
+            tot[k] += stats[k]
+    print(f"{name}: {tot}")
+    assert tot["mismatch_outside_guard"] == 0
+    assert tot["guarded_mismatch"] <= max(1, 1e-4 * tot["positions"])
