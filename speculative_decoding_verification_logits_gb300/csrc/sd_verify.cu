@@ -1,27 +1,31 @@
 // GB300 (sm_103a) kernels of the speculative-decoding verify step.
 //
-// One thread-block cluster works on one (row b, position j) item at a time:
-// its CTAs split the vocabulary into contiguous slices, bring their slice of
-// target row j and draft row j into shared memory with 1-D TMA bulk copies
-// (each logit read from HBM exactly once), reduce max / argmax / sum of
-// exponentials per slice, and exchange the per-CTA partials over
-// distributed shared memory.  Every CTA of the cluster then holds the same
-// row statistics and takes the same decisions.  A position whose draft is
-// rejected, and the bonus position K, draw their token right there from
-// the slices still resident in shared memory (inverse CDF over the
-// residual max(0, p - q) or over p), so no logit is read twice.  The item's
-// owner CTA publishes its result to global scratch; the last item of a row
-// to finish (an atomic counter, no spin-waits) runs that row's
-// left-to-right accept scan, writes tau / the emitted tokens / the hit
-// test, and the last row to finish packs all rows' tokens.  The kernel is
-// persistent: clusters loop over items with a two-stage shared-memory
-// pipeline so that the bulk copies of the next item overlap the reductions
-// of the current one.
+// Layout of the work: one thread-block cluster per sequence (row b of the
+// batch).  The cluster's CTAs split the vocabulary into contiguous slices;
+// each CTA streams its slice of every logit row of the sequence -- target
+// rows K..0 and draft rows K-1..0, plus the optional draft row of the bonus
+// position.  Each thread copies its own 16-byte vectors a few steps ahead
+// into its own shared-memory slots (cp.async, so no block-wide barrier is
+// needed while streaming) and keeps only per-row statistics in registers:
+// max, lowest-index argmax, the sum of 2^(l s + c) (s = log2(e) / T, c a
+// per-thread offset carried exactly into the combine) and, for draft rows,
+// the few vectors that can hold the top-F keys.  One exchange over
+// distributed shared memory gives every CTA the statistics of all K+1
+// positions, so each CTA evaluates the left-to-right accept scan itself and
+// all of them agree on the first rejection m.  Only then is a single
+// inverse-CDF draw needed per sequence: over the residual max(0, p - q) at m,
+// or over p at the bonus position K.  The CTAs re-read their slices of those
+// one or two rows (rows are streamed in the order K..0, so the likely m ~ 0
+// rows were read last and are still in L2), exchange slice masses, and the
+// CTA holding the crossing point scans it.  The owning CTA writes the
+// sequence's tokens and tau, and the last sequence to finish (one atomic
+// counter) packs all sequences' tokens.  Nothing waits on another cluster
+// and there are no spin-waits.
 //
 // Method sources (web pages, stated in prose there):
-//  "What is speculative decoding" explainer (lotook.com): the four-stage
-//    loop (greedy match; keep a token the target rates at least as high as
-//    the draft, else keep it with the probability ratio; resample the first
+//  "What is speculative decoding" explainer (lotook.com): the four-stage loop
+//    (greedy match; keep a token the target rates at least as high as the
+//    draft, else keep it with the probability ratio; resample the first
 //    rejection from a residual of both distributions; bonus token at K+1).
 //  "Speculative Speculative Decoding" blog (jiwasawa.github.io), "Saguaro
 //    1. Outcome Prediction": keys from the draft logits' top tokens with a
@@ -36,28 +40,29 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
-#include <map>
-#include <tuple>
-#include <algorithm>
 
 namespace cg = cooperative_groups;
 
 namespace sdv {
 
-constexpr int kMaxF = SD_MAX_FANOUT;
-constexpr int kMaxK = SD_MAX_K;
-constexpr int kMaxCS = 16;
-constexpr int kCandCap = 512;           // top-F candidate buffer per CTA
-constexpr int kThreads = 512;     // threads per CTA
-constexpr unsigned kWaitSpins = 1u << 24;  // bounded mbarrier wait (~1 s with backoff)
+constexpr int kU = 4;                        // 16-byte vectors per thread per step
+constexpr int kDepth = 3;                    // steps in each thread's copy ring
+constexpr int kMaxWarps = 16;                // threads per CTA <= 512
+constexpr int kMaxCS = 16;                   // cluster size limit
+constexpr int kMaxRows = 2 * SD_MAX_K + 2;   // K+1 target, K draft, 1 bonus
+constexpr int kMaxSliceVec = 4096;           // vectors in one row slice
+constexpr float kRebase = 16.f;              // log2 headroom of the exp offset
 
 enum Mode : int { kVerify = 0, kPredict = 1 };
+enum RowKind : int { kTarget = 0, kDraft = 1, kBonus = 2 };
+enum RowFlag : int { kNeedExp = 1, kNeedArg = 2, kNeedKeys = 4 };
 
 struct Params {
   const uint8_t *target;   // [B][K+1][V]
@@ -73,21 +78,17 @@ struct Params {
   float *ratio_out, *p_out, *q_out;
   int32_t *argmax_out;
   int32_t *status;
-  int32_t *row_counter;    // [B]   workspace
-  int32_t *done_counter;   // [1]   workspace
-  int32_t *pos_token;      // [B][K+1] workspace
-  int8_t *pos_accept;      // [B][K+1] workspace
+  int32_t *done_counter;   // workspace
   uint64_t seed;
   int64_t row_base;
   int32_t B, K, V;
   int32_t mode;
   int32_t keys;            // build keys in this pass
-  int32_t compact;         // pack tokens at the end
+  int32_t compact;
   int32_t n_keys_in, n_keys_out;
-  int32_t cs, nstage, slice, region;
-  int32_t n_items;
-  int32_t fanout[kMaxK + 1];
-  int32_t fan_off[kMaxK + 2];
+  int32_t cs, slice;       // cluster size, vocabulary slice per CTA
+  int32_t fanout[SD_MAX_K + 1];
+  int32_t fan_off[SD_MAX_K + 2];
 };
 
 // ------------------------------------------------------------------ Philox --
@@ -122,59 +123,41 @@ __device__ __forceinline__ double uniform_u(uint64_t seed, int64_t row, int pos,
 }
 
 // ------------------------------------------------------------- primitives --
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0u;
-}
-
-// Bounded wait on one phase of an mbarrier; false if it gave up.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-  for (unsigned i = 0; i < kWaitSpins; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (i > 32) __nanosleep(64);
-  }
-  return false;
-}
-
-// 1-D TMA bulk copy global -> this CTA's shared memory, completion counted
-// in bytes on the mbarrier.  dst, src and bytes are multiples of 16.
-__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
-                                              uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
-// 2^x on the special-function unit (x <= 0 here; results below 2^-126 flush
-// to zero, far below anything that moves a sum of at least 1).
+// 2^x on the special-function unit.  Results below 2^-126 flush to zero, far
+// below anything that moves a sum of at least 1.
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^d for a double d without a double-precision transcendental: the integer
+// part goes into the float exponent, the fraction (exact in double) through
+// ex2 (relative error about 2^-22).  Results below the normal range are 0.
+__device__ __forceinline__ float exp2_split(double d) {
+  if (!(d > -126.0)) return 0.f;
+  if (d >= 128.0) return INFINITY;
+  const double n = floor(d);
+  const float y = ex2((float)(d - n));  // in [1, 2)
+  return __int_as_float(__float_as_int(y) + ((int)n << 23));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+// 16-byte asynchronous copy global -> shared (L2 only), per thread
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// 16-byte global load through L2 only (read-once data)
+__device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
+  return __ldcg(reinterpret_cast<const uint4 *>(p));
 }
 
 __device__ __forceinline__ void kahan_add(float &sum, float &comp, float v) {
@@ -189,6 +172,11 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
 __device__ __forceinline__ int warp_min_i(int v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -200,367 +188,22 @@ __device__ __forceinline__ double warp_sum_d(double v) {
   return v;
 }
 
-struct Red {
-  float f[32];
-  int i[32];
-  double d[32];
-};
-
-__device__ float block_max(float v, Red &r) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  v = warp_max(v);
-  if (lane == 0) r.f[w] = v;
-  __syncthreads();
-  float x = lane < nw ? r.f[lane] : -INFINITY;
-  x = warp_max(x);
-  __syncthreads();
-  return x;
-}
-__device__ int block_min_i(int v, Red &r) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  v = warp_min_i(v);
-  if (lane == 0) r.i[w] = v;
-  __syncthreads();
-  int x = lane < nw ? r.i[lane] : INT32_MAX;
-  x = warp_min_i(x);
-  __syncthreads();
-  return x;
-}
-// Sum in double, combined in a fixed order (warp tree, then warps in order).
-__device__ double block_sum_d(double v, Red &r) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  v = warp_sum_d(v);
-  if (lane == 0) r.d[w] = v;
-  __syncthreads();
-  double x = lane < nw ? r.d[lane] : 0.0;
-  x = warp_sum_d(x);
-  __syncthreads();
-  return x;
-}
-
-// --------------------------------------------------------- element types --
-template <typename E>
-struct Elt;
-template <>
-struct Elt<float> {
-  static constexpr int kSize = 4;
-  static constexpr int kPerVec = 4;
-  static __device__ __forceinline__ void unpack(const uint4 &v, float *f) {
-    f[0] = __uint_as_float(v.x);
-    f[1] = __uint_as_float(v.y);
-    f[2] = __uint_as_float(v.z);
-    f[3] = __uint_as_float(v.w);
-  }
-  static __device__ __forceinline__ float load(const uint8_t *p) {
-    return *reinterpret_cast<const float *>(p);
-  }
-  static __device__ __forceinline__ float load_global(const uint8_t *p) {
-    return __ldg(reinterpret_cast<const float *>(p));
-  }
-  static __device__ __forceinline__ void store_neg_inf(uint8_t *p) {
-    *reinterpret_cast<uint32_t *>(p) = 0xFF800000u;
-  }
-  static __device__ __forceinline__ void copy_elem(uint8_t *dst, const uint8_t *src) {
-    *reinterpret_cast<uint32_t *>(dst) = __ldg(reinterpret_cast<const unsigned int *>(src));
-  }
-};
-template <>
-struct Elt<__nv_bfloat16> {
-  static constexpr int kSize = 2;
-  static constexpr int kPerVec = 8;
-  static __device__ __forceinline__ void unpack(const uint4 &v, float *f) {
-    f[0] = __uint_as_float(v.x << 16);
-    f[1] = __uint_as_float(v.x & 0xffff0000u);
-    f[2] = __uint_as_float(v.y << 16);
-    f[3] = __uint_as_float(v.y & 0xffff0000u);
-    f[4] = __uint_as_float(v.z << 16);
-    f[5] = __uint_as_float(v.z & 0xffff0000u);
-    f[6] = __uint_as_float(v.w << 16);
-    f[7] = __uint_as_float(v.w & 0xffff0000u);
-  }
-  static __device__ __forceinline__ float load(const uint8_t *p) {
-    return __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t *>(p)) << 16);
-  }
-  static __device__ __forceinline__ float load_global(const uint8_t *p) {
-    return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(p)) << 16);
-  }
-  static __device__ __forceinline__ void store_neg_inf(uint8_t *p) {
-    *reinterpret_cast<uint16_t *>(p) = (uint16_t)0xFF80u;
-  }
-  static __device__ __forceinline__ void copy_elem(uint8_t *dst, const uint8_t *src) {
-    *reinterpret_cast<uint16_t *>(dst) = __ldg(reinterpret_cast<const unsigned short *>(src));
-  }
-};
-
-// Where one CTA's slice [v0, v1) of one logit row sits in shared memory.
-// The region mirrors the global 16-byte alignment of the slice: element
-// v0 is at byte `hp` and vector q covers global bytes [g_first + 16q, +16).
-// Bytes of the first/last vector outside the slice hold -inf.
-struct Slice {
-  int v0, v1;       // element range
-  int hp;           // head pad in bytes
-  int nvec;         // 16-byte vectors in the region
-  __device__ __forceinline__ int first_elem(int q, int sz) const {
-    return v0 + (q * 16 - hp) / sz;
-  }
-};
-
-__device__ __forceinline__ Slice make_slice(const uint8_t *row, int v0, int v1, int sz) {
-  Slice s;
-  s.v0 = v0;
-  s.v1 = v1;
-  const uintptr_t a0 = (uintptr_t)(row + (int64_t)v0 * sz);
-  const uintptr_t a1 = (uintptr_t)(row + (int64_t)v1 * sz);
-  const uintptr_t gf = a0 & ~(uintptr_t)15, gl = (a1 + 15) & ~(uintptr_t)15;
-  s.hp = (int)(a0 - gf);
-  s.nvec = v1 > v0 ? (int)((gl - gf) / 16) : 0;
-  return s;
-}
-
-// Issued by one thread: the bulk copy of the 16-byte-aligned interior of the
-// slice, plain loads for the ragged head and tail, -inf in the pad bytes.
-// Returns the bytes the bulk copy will deliver.
-template <typename E>
-__device__ uint32_t bulk_bytes(const uint8_t *row, const Slice &s) {
-  constexpr int sz = Elt<E>::kSize;
-  if (s.v1 <= s.v0) return 0;
-  const uintptr_t a0 = (uintptr_t)(row + (int64_t)s.v0 * sz);
-  const uintptr_t a1 = (uintptr_t)(row + (int64_t)s.v1 * sz);
-  const uintptr_t lo = (a0 + 15) & ~(uintptr_t)15, hi = a1 & ~(uintptr_t)15;
-  return hi > lo ? (uint32_t)(hi - lo) : 0u;
-}
-
-template <typename E>
-__device__ void issue_slice(uint8_t *region, const uint8_t *row, const Slice &s, uint64_t *bar) {
-  constexpr int sz = Elt<E>::kSize;
-  if (s.v1 <= s.v0) return;
-  const uintptr_t a0 = (uintptr_t)(row + (int64_t)s.v0 * sz);
-  const uintptr_t a1 = (uintptr_t)(row + (int64_t)s.v1 * sz);
-  const uintptr_t gf = a0 & ~(uintptr_t)15, gl = (a1 + 15) & ~(uintptr_t)15;
-  const uintptr_t lo = (a0 + 15) & ~(uintptr_t)15, hi = a1 & ~(uintptr_t)15;
-  uintptr_t plain_hi = a1;  // end of the head part loaded with plain loads
-  if (hi > lo) {
-    uint32_t off = (uint32_t)(lo - gf), bytes = (uint32_t)(hi - lo);
-    const uint8_t *src = reinterpret_cast<const uint8_t *>(lo);
-    // chunks of at most 64 KiB per instruction
-    while (bytes > 0) {
-      const uint32_t n = bytes > 65536u ? 65536u : bytes;
-      bulk_copy_g2s(region + off, src, n, bar);
-      off += n;
-      src += n;
-      bytes -= n;
-    }
-    plain_hi = lo;
-    for (uintptr_t a = hi; a < a1; a += sz)
-      Elt<E>::copy_elem(region + (a - gf), reinterpret_cast<const uint8_t *>(a));
-  }
-  for (uintptr_t a = a0; a < plain_hi; a += sz)
-    Elt<E>::copy_elem(region + (a - gf), reinterpret_cast<const uint8_t *>(a));
-  for (uintptr_t a = gf; a < a0; a += sz) Elt<E>::store_neg_inf(region + (a - gf));
-  for (uintptr_t a = a1; a < gl; a += sz) Elt<E>::store_neg_inf(region + (a - gf));
-}
-
-// ------------------------------------------------------------ item layout --
-struct Item {
-  int b, j;
-  float T;
-  bool tvalid, sampled;   // temperature valid / T > 0
-  int d;                  // drafted token at j (-1 at j == K)
-  bool dvalid;
-  bool need_t, need_1;    // target row j / second row (draft j or bonus)
-  const uint8_t *trow, *row1;
-  int fan;                // keys to build at this position (0 if none)
-};
-
-template <typename E>
-__device__ __forceinline__ Item describe(const Params &P, int it) {
-  constexpr int sz = Elt<E>::kSize;
-  Item I;
-  I.b = it / (P.K + 1);
-  I.j = it - I.b * (P.K + 1);
-  const float T = P.temps ? P.temps[I.b] : 0.f;
-  I.T = T;
-  I.tvalid = (T >= 0.f) && (T <= 3.4e38f);  // rejects NaN, negative, inf
-  I.sampled = I.tvalid && T > 0.f;
-  I.d = I.j < P.K ? P.tokens[(int64_t)I.b * P.K + I.j] : -1;
-  I.dvalid = I.j < P.K ? (I.d >= 0 && I.d < P.V) : true;
-  I.fan = P.keys ? P.fanout[I.j] : 0;
-  const int64_t V = P.V;
-  if (P.mode == kPredict) {
-    I.need_t = false;
-    I.trow = nullptr;
-    if (I.j < P.K) {
-      I.row1 = P.draft + ((int64_t)I.b * P.K + I.j) * V * sz;
-      I.need_1 = I.fan > 0;
-    } else {
-      I.row1 = P.bonus ? P.bonus + (int64_t)I.b * V * sz : nullptr;
-      I.need_1 = I.fan > 0 && P.bonus != nullptr;
-    }
-  } else {
-    I.need_t = true;
-    I.trow = P.target + ((int64_t)I.b * (P.K + 1) + I.j) * V * sz;
-    if (I.j < P.K) {
-      I.row1 = P.draft + ((int64_t)I.b * P.K + I.j) * V * sz;
-      I.need_1 = I.sampled || I.fan > 0;
-    } else {
-      I.row1 = P.bonus ? P.bonus + (int64_t)I.b * V * sz : nullptr;
-      I.need_1 = I.fan > 0 && P.bonus != nullptr;
-    }
-    if (!I.need_1) I.row1 = nullptr;
-  }
-  return I;
-}
-
-// ------------------------------------------------------- per-CTA partials --
-struct alignas(16) Part {
-  float mt;       // target slice max
-  int at;         // first index of mt in the slice (INT32_MAX if none)
-  double zt;      // sum 2^((l - mt) s) over the slice
-  float ld;       // target logit of the drafted token (if in slice)
-  int has_ld;
-  float m1;       // second row: slice max
-  double z1;      // second row: sum 2^((l - m1) s)
-  float l1d;      // second row logit of the drafted token (if in slice)
-  int has_l1d;
-  int nc;         // top-F candidates found in the slice
-  float cv[kMaxF];
-  int ci[kMaxF];
-  double s;       // mass of the sampling pass over the slice
-};
-static_assert(sizeof(Part) % 16 == 0, "Part is copied in 16-byte units");
-
-// Decisions every CTA of a cluster derives identically from the partials.
-struct Decision {
-  float M, M1;
-  double Zt, Z1;
-  int amax;
-  int accept;
-  int sample;     // 0 none, 1 residual, 2 from p (bonus / empty residual)
-  float s_hi, s_lo;
-  float A, Bq;    // 1/Zt and 1/Z1 as floats (sampling pass weights)
-  double t;       // u * S of the sampling pass
-  int cstar;      // CTA that owns the sampled token
-  double t_loc;   // target within the owning CTA's slice
-  float ratio, p_d, q_d;
-  int token;
-  int owner;
-};
-
-struct Smem {
-  uint64_t bar[2];
-  Part part[2];
-  Part peer[kMaxCS];      // local copies of the cluster's partials
-  double zterm[kMaxCS], z1term[kMaxCS], sterm[kMaxCS];
-  Red red;
-  Decision dec;
-  int cand_n;
-  int found_thread;
-  int tok;
-  int flag_compact;
-  int found_q;
-};
-
-// ----------------------------------------------------- slice reductions --
-template <typename E>
-__device__ __forceinline__ float slice_max(const uint8_t *reg, const Slice &s) {
-  float m = -INFINITY;
-  for (int q = threadIdx.x; q < s.nvec; q += blockDim.x) {
-    float f[Elt<E>::kPerVec];
-    Elt<E>::unpack(*reinterpret_cast<const uint4 *>(reg + 16 * q), f);
-#pragma unroll
-    for (int k = 0; k < Elt<E>::kPerVec; ++k) m = fmaxf(m, f[k]);
-  }
-  return m;
-}
-
-// first index (in [v0, v1)) of a value equal to target among this thread's vectors
-template <typename E>
-__device__ __forceinline__ int slice_first_eq(const uint8_t *reg, const Slice &s, float target) {
-  constexpr int sz = Elt<E>::kSize;
-  for (int q = threadIdx.x; q < s.nvec; q += blockDim.x) {
-    float f[Elt<E>::kPerVec];
-    Elt<E>::unpack(*reinterpret_cast<const uint4 *>(reg + 16 * q), f);
-    const int e0 = s.first_elem(q, sz);
-#pragma unroll
-    for (int k = 0; k < Elt<E>::kPerVec; ++k) {
-      const int e = e0 + k;
-      if (f[k] == target && e >= s.v0 && e < s.v1) return e;
-    }
-  }
-  return INT32_MAX;
-}
-
-// sum over the slice of 2^((l - m) s), s = s_hi + s_lo (s_lo >= 0 so that
-// -inf logits give 2^-inf = 0 without inf - inf)
-template <typename E>
-__device__ __forceinline__ float slice_expsum(const uint8_t *reg, const Slice &s, float m,
-                                              float s_hi, float s_lo) {
-  float sum = 0.f, comp = 0.f;
-  for (int q = threadIdx.x; q < s.nvec; q += blockDim.x) {
-    float f[Elt<E>::kPerVec];
-    Elt<E>::unpack(*reinterpret_cast<const uint4 *>(reg + 16 * q), f);
-    float e[Elt<E>::kPerVec];
-#pragma unroll
-    for (int k = 0; k < Elt<E>::kPerVec; ++k) {
-      const float dl = f[k] - m;
-      e[k] = ex2(fmaf(dl, s_hi, dl * s_lo));
-    }
-#pragma unroll
-    for (int w = Elt<E>::kPerVec / 2; w > 0; w >>= 1)
-#pragma unroll
-      for (int k = 0; k < w; ++k) e[k] += e[k + w];
-    kahan_add(sum, comp, e[0]);
-  }
-  return sum;
-}
-
-// Weights of the sampling pass for the Elt::kPerVec elements of target
-// vector q: residual max(0, 2^x A - 2^y Bq) (mode 1) or 2^x A (mode 2),
-// x = (l - M) s, y = (l' - M1) s.  Elements outside the slice weigh 0.
-template <typename E>
-__device__ __forceinline__ void sample_weights(const uint8_t *rt, const Slice &st,
-                                               const uint8_t *r1, const Slice &s1, int q,
-                                               const Decision &D, float *w) {
-  constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec;
-  float f[N];
-  Elt<E>::unpack(*reinterpret_cast<const uint4 *>(rt + 16 * q), f);
-#pragma unroll
-  for (int k = 0; k < N; ++k) {
-    const float dl = f[k] - D.M;
-    w[k] = ex2(fmaf(dl, D.s_hi, dl * D.s_lo)) * D.A;
-  }
-  if (D.sample == 1) {
-    float g[N];
-    if (s1.hp == st.hp) {
-      Elt<E>::unpack(*reinterpret_cast<const uint4 *>(r1 + 16 * q), g);
-    } else {
-      const int e0 = st.first_elem(q, sz);
-#pragma unroll
-      for (int k = 0; k < N; ++k) {
-        const int e = e0 + k;
-        g[k] = (e >= s1.v0 && e < s1.v1) ? Elt<E>::load(r1 + s1.hp + (e - s1.v0) * sz)
-                                         : -INFINITY;
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < N; ++k) {
-      const float dl = g[k] - D.M1;
-      const float qv = ex2(fmaf(dl, D.s_hi, dl * D.s_lo)) * D.Bq;
-      w[k] = fmaxf(0.f, w[k] - qv);
-    }
-  }
-  const int e0 = st.first_elem(q, sz);
-#pragma unroll
-  for (int k = 0; k < N; ++k) {
-    const int e = e0 + k;
-    if (e < st.v0 || e >= st.v1) w[k] = 0.f;
-  }
-}
-
-// ------------------------------------------------------------- top-F keys --
-// Ordered key of (value, index): larger value first, then lower index.
+// Order of (value, index) candidates: larger value first, then lower index.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
+}
+
+// Warp-wide best (value desc, index asc) of one candidate per lane.
+__device__ __forceinline__ void warp_best(float &v, int &i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
 }
 
 // Bitonic sort of one value per lane, descending; returns this lane's value.
@@ -571,7 +214,7 @@ __device__ __forceinline__ float warp_sort_desc(float v) {
 #pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
       const float o = __shfl_xor_sync(0xffffffffu, v, j);
-      const bool up = ((lane & k) == 0);         // block sorted descending
+      const bool up = ((lane & k) == 0);
       const bool lower = ((lane & j) == 0);
       v = (lower == up) ? fmaxf(v, o) : fminf(v, o);
     }
@@ -579,184 +222,252 @@ __device__ __forceinline__ float warp_sort_desc(float v) {
   return v;
 }
 
-// Top-`fan` (value desc, index asc) of the slice excluding index `excl` and
-// -inf values.  m_thread: this thread's slice max.  Result left in
-// sm.part[par].cv/ci/nc by thread 0.
+// --------------------------------------------------------- element types --
 template <typename E>
-__device__ void slice_topf(const uint8_t *reg, const Slice &s, float m_thread, int fan, int excl,
-                           float *cand_v, int *cand_i, Smem &sm, Part &out) {
+struct Elt;
+template <>
+struct Elt<float> {
+  static constexpr int kSize = 4;
+  static constexpr int kPerVec = 4;
+  static constexpr uint32_t kNegInfWord = 0xFF800000u;
+  static __device__ __forceinline__ void unpack(const uint4 &v, float *f) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  static __device__ __forceinline__ float vmax(const uint4 &v) {
+    return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                 fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
+  static __device__ __forceinline__ float load_global(const uint8_t *p) {
+    return __ldg(reinterpret_cast<const float *>(p));
+  }
+};
+template <>
+struct Elt<__nv_bfloat16> {
+  static constexpr int kSize = 2;
+  static constexpr int kPerVec = 8;
+  static constexpr uint32_t kNegInfWord = 0xFF80FF80u;
+  static __device__ __forceinline__ void unpack(const uint4 &v, float *f) {
+    f[0] = __uint_as_float(v.x << 16);
+    f[1] = __uint_as_float(v.x & 0xffff0000u);
+    f[2] = __uint_as_float(v.y << 16);
+    f[3] = __uint_as_float(v.y & 0xffff0000u);
+    f[4] = __uint_as_float(v.z << 16);
+    f[5] = __uint_as_float(v.z & 0xffff0000u);
+    f[6] = __uint_as_float(v.w << 16);
+    f[7] = __uint_as_float(v.w & 0xffff0000u);
+  }
+  // max of the 8 values with packed bf16x2 maxima (exact), then widened
+  static __device__ __forceinline__ float vmax(const uint4 &v) {
+    const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x),
+                                     *reinterpret_cast<const __nv_bfloat162 *>(&v.y));
+    const __nv_bfloat162 c = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&v.z),
+                                     *reinterpret_cast<const __nv_bfloat162 *>(&v.w));
+    const __nv_bfloat162 m = __hmax2(a, c);
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(&m);
+    return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+  static __device__ __forceinline__ float load_global(const uint8_t *p) {
+    return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(p)) << 16);
+  }
+};
+
+// ---------------------------------------------------------------- rows ----
+// One logit row as this CTA sees it: the slice [v0, v1) occupies `nvec`
+// 16-byte vectors starting at `gbase`, the 16-byte boundary at or below
+// element v0 (element v0 sits `hp` bytes into vector 0).  Vectors in
+// [qlo, qhi) lie wholly inside the slice and are copied with cp.async; the
+// (at most two) others are assembled from element loads with -inf in the
+// bytes outside the slice, so every vector a thread sees is a plain list of
+// logits with -inf padding.  `qd` is the vector holding the token excluded
+// from this row's keys (-1 if it is not in this slice).
+struct RowInfo {
+  const uint8_t *g;      // element 0 of the row
+  const uint8_t *gbase;  // 16-byte boundary at or below element v0
+  int kind, j;           // RowKind, position
+  int flags;             // RowFlag bits
+  int excl;              // token excluded from the keys (-1: none)
+  int fan;               // keys wanted from this row
+  int hp, nvec, nsteps, qlo, qhi, qd;
+};
+
+// Element index of element i of slice vector q.
+__device__ __forceinline__ int elem_index(int v0, int hp, int q, int i, int sz) {
+  return v0 + (q * 16 - hp) / sz + i;
+}
+
+template <int NT>
+__device__ __forceinline__ void row_geometry(RowInfo &R, int v0, int v1, int sz) {
+  constexpr int kStepVec = NT * kU;
+  R.gbase = R.g;
+  R.hp = R.nvec = R.nsteps = R.qlo = R.qhi = 0;
+  R.qd = -1;
+  if (v1 <= v0) return;
+  const uintptr_t a0 = (uintptr_t)(R.g + (int64_t)v0 * sz);
+  const uintptr_t a1 = (uintptr_t)(R.g + (int64_t)v1 * sz);
+  const uintptr_t gf = a0 & ~(uintptr_t)15, gl = (a1 + 15) & ~(uintptr_t)15;
+  R.gbase = reinterpret_cast<const uint8_t *>(gf);
+  R.hp = (int)(a0 - gf);
+  R.nvec = (int)((gl - gf) / 16);
+  R.nsteps = (R.nvec + kStepVec - 1) / kStepVec;
+  R.qlo = R.hp == 0 ? 0 : 1;
+  R.qhi = (a1 & 15) == 0 ? R.nvec : R.nvec - 1;
+  if (R.excl >= v0 && R.excl < v1) R.qd = ((R.excl - v0) * sz + R.hp) / 16;
+}
+
+// Vector q of row R's slice assembled from element loads (ragged ends, or
+// -inf past the slice).
+template <typename E>
+__device__ __noinline__ uint4 load_vec_slow(const RowInfo &R, int q, int v0, int v1) {
   constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec;
-  const int lane = threadIdx.x & 31;
-  // threshold: the (fan+1)-th largest thread maximum of the best warp is a
-  // lower bound of the (fan+1)-th largest value of the slice, so every
-  // top-fan element other than `excl` is >= theta.
-  const float sorted = warp_sort_desc(m_thread);
-  float th = __shfl_sync(0xffffffffu, sorted, fan);  // fan <= kMaxF < 32
-  th = block_max(th, sm.red);
-  if (threadIdx.x == 0) sm.cand_n = 0;
-  __syncthreads();
-  for (int q = threadIdx.x; q < s.nvec; q += blockDim.x) {
-    float f[N];
-    Elt<E>::unpack(*reinterpret_cast<const uint4 *>(reg + 16 * q), f);
-    const int e0 = s.first_elem(q, sz);
+  const uint32_t ninf = Elt<E>::kNegInfWord;
+  uint32_t w[4] = {ninf, ninf, ninf, ninf};
+  if (q < R.nvec) {
 #pragma unroll
-    for (int k = 0; k < N; ++k) {
-      if (f[k] >= th && f[k] > -INFINITY) {
-        const int e = e0 + k;
-        if (e != excl && e >= s.v0 && e < s.v1) {
-          const int slot = atomicAdd(&sm.cand_n, 1);
-          if (slot < kCandCap) {
-            cand_v[slot] = f[k];
-            cand_i[slot] = e;
-          }
+    for (int i = 0; i < N; ++i) {
+      const int e = elem_index(v0, R.hp, q, i, sz);
+      if (e >= v0 && e < v1) {
+        if (sz == 4) {
+          w[i] = __ldg(reinterpret_cast<const unsigned int *>(R.g + (int64_t)e * 4));
+        } else {
+          const uint32_t h = __ldg(reinterpret_cast<const unsigned short *>(R.g + (int64_t)e * 2));
+          w[i >> 1] = (i & 1) ? ((w[i >> 1] & 0x0000ffffu) | (h << 16))
+                              : ((w[i >> 1] & 0xffff0000u) | h);
         }
       }
     }
   }
-  __syncthreads();
-  const int n = sm.cand_n;
-  if (n > kCandCap) {
-    // many ties at the threshold: exact selection by repeated block argmax
-    float last_v = INFINITY;
-    int last_i = -1;
-    for (int r = 0; r < fan; ++r) {
-      float bv = -INFINITY;
-      int bi = INT32_MAX;
-      for (int q = threadIdx.x; q < s.nvec; q += blockDim.x) {
-        float f[N];
-        Elt<E>::unpack(*reinterpret_cast<const uint4 *>(reg + 16 * q), f);
-        const int e0 = s.first_elem(q, sz);
-#pragma unroll
-        for (int k = 0; k < N; ++k) {
-          const int e = e0 + k;
-          if (e == excl || e < s.v0 || e >= s.v1 || !(f[k] > -INFINITY)) continue;
-          if (!better(last_v, last_i, f[k], e) || (f[k] == last_v && e == last_i)) continue;
-          if (better(f[k], e, bv, bi)) {
-            bv = f[k];
-            bi = e;
-          }
-        }
-      }
-      const float mv = block_max(bv, sm.red);
-      const int mi = block_min_i(bv == mv ? bi : INT32_MAX, sm.red);
-      if (threadIdx.x == 0) {
-        if (mv > -INFINITY && mi != INT32_MAX) {
-          out.cv[r] = mv;
-          out.ci[r] = mi;
-          out.nc = r + 1;
-        }
-      }
-      last_v = mv;
-      last_i = mi;
-      if (!(mv > -INFINITY) || mi == INT32_MAX) break;
-    }
-    __syncthreads();
-    return;
-  }
-  // warp 0 selects the best `fan` candidates
-  if (threadIdx.x < 32) {
-    int taken = 0;  // bit r set: this lane's r-th candidate already chosen
-    int nc = 0;
-    for (int r = 0; r < fan; ++r) {
-      float bv = -INFINITY;
-      int bi = INT32_MAX, bslot = -1;
-      for (int c = lane, t = 0; c < n; c += 32, ++t) {
-        if (taken & (1 << t)) continue;
-        if (better(cand_v[c], cand_i[c], bv, bi)) {
-          bv = cand_v[c];
-          bi = cand_i[c];
-          bslot = t;
-        }
-      }
-      float wv = bv;
-      int wi = bi;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
-        if (better(ov, oi, wv, wi)) {
-          wv = ov;
-          wi = oi;
-        }
-      }
-      if (wi == INT32_MAX) break;
-      if (bi == wi && bslot >= 0) taken |= 1 << bslot;
-      if (lane == 0) {
-        out.cv[r] = wv;
-        out.ci[r] = wi;
-      }
-      nc = r + 1;
-    }
-    if (lane == 0) out.nc = nc;
-  }
-  __syncthreads();
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// --------------------------------------------------------- row finalizer --
-// Runs on one thread once all K+1 positions of row b have published.
-__device__ void finalize_row(const Params &P, int b) {
-  const int K = P.K;
-  const float T = P.temps[b];
-  const bool tvalid = (T >= 0.f) && (T <= 3.4e38f);
-  bool dvalid = true;
-  for (int j = 0; j < K; ++j) {
-    const int d = P.tokens[(int64_t)b * K + j];
-    if (d < 0 || d >= P.V) dvalid = false;
-  }
-  int32_t *out = P.out_tokens + (int64_t)b * (K + 1);
-  int32_t *ptok = P.pos_token + (int64_t)b * (K + 1);
-  int8_t *pacc = P.pos_accept + (int64_t)b * (K + 1);
-  if (!tvalid || !dvalid) {
-    for (int j = 0; j <= K; ++j) {  // leave the scratch zeroed
-      ptok[j] = 0;
-      pacc[j] = 0;
-    }
-    for (int j = 0; j <= K; ++j) out[j] = -1;
-    P.num_accepted[b] = 0;
-    P.tau[b] = 0;
-    if (P.hit) P.hit[b] = 0;
-    if (P.status) atomicOr(P.status, (tvalid ? 0 : (int)SD_STATUS_BAD_TEMP) |
-                                         (dvalid ? 0 : (int)SD_STATUS_BAD_TOKEN));
-    return;
-  }
-  int n_acc = K;
-  const int8_t *acc = P.pos_accept + (int64_t)b * (K + 1);
-  for (int j = 0; j < K; ++j) {
-    if (__ldcg(reinterpret_cast<const signed char *>(acc + j)) == 0) {
-      n_acc = j;
-      break;
-    }
-  }
-  const int tok = __ldcg(ptok + n_acc);
-  for (int j = 0; j <= K; ++j) {  // leave the scratch zeroed for the next call
-    ptok[j] = 0;
-    pacc[j] = 0;
-  }
-  for (int j = 0; j < n_acc; ++j) out[j] = P.tokens[(int64_t)b * K + j];
-  out[n_acc] = tok;
-  for (int j = n_acc + 1; j <= K; ++j) out[j] = -1;
-  P.num_accepted[b] = n_acc;
-  P.tau[b] = n_acc + 1;
-  if (P.hit) {
-    int h = 0;
-    if (P.keys && P.keys_out) {
-      const int32_t *kb = P.keys_out + (int64_t)b * P.n_keys_out * 2;
-      for (int k = 0; k < P.n_keys_out; ++k)
-        if (__ldcg(kb + 2 * k) == n_acc && __ldcg(kb + 2 * k + 1) == tok) h = 1;
-    } else if (P.keys_in) {
-      const int32_t *kb = P.keys_in + (int64_t)b * P.n_keys_in * 2;
-      for (int k = 0; k < P.n_keys_in; ++k)
-        if (kb[2 * k] == n_acc && kb[2 * k + 1] == tok) h = 1;
-    }
-    P.hit[b] = (uint8_t)h;
-  }
+// Vector q of row R's slice read directly (128-bit load when it lies inside
+// the slice), -inf past `R.nvec`.
+template <typename E>
+__device__ __forceinline__ uint4 load_vec_direct(const RowInfo &R, int q, int v0, int v1) {
+  if (q >= R.qlo && q < R.qhi) return ld_stream(R.gbase + 16 * q);
+  return load_vec_slow<E>(R, q, v0, v1);
 }
 
+// One 16-byte vector q (< qend) of row R into this thread's k-th slot of
+// ring slot `slot`; ragged ends are read when consumed.
+template <int NT>
+__device__ __forceinline__ void issue_vec(const RowInfo &R, int q, int qend, uint32_t ring,
+                                          int slot, int k) {
+  if (q < qend && q >= R.qlo && q < R.qhi)
+    cp_async16(ring + (uint32_t)(((slot * kU + k) * NT + threadIdx.x) * 16), R.gbase + 16 * q);
+}
+template <typename E, int NT>
+__device__ __forceinline__ uint4 fetch_vec(const RowInfo &R, int q, int qend, const uint8_t *ring,
+                                           int slot, int k, int v0, int v1) {
+  if (q < qend && q >= R.qlo && q < R.qhi)
+    return *reinterpret_cast<const uint4 *>(ring + ((slot * kU + k) * NT + threadIdx.x) * 16);
+  if (q >= qend || q >= R.nvec) {
+    const uint32_t w = Elt<E>::kNegInfWord;
+    return make_uint4(w, w, w, w);
+  }
+  return load_vec_slow<E>(R, q, v0, v1);
+}
+
+// Each thread copies its own kU vectors of one step of row R into its own
+// slots of ring slot `slot` (vectors inside the slice only).
+template <int NT>
+__device__ __forceinline__ void issue_unit(const RowInfo &R, int step, uint32_t ring, int slot) {
+  constexpr int kStepVec = NT * kU;
+#pragma unroll
+  for (int k = 0; k < kU; ++k) {
+    const int q = step * kStepVec + threadIdx.x + k * NT;
+    if (q >= R.qlo && q < R.qhi)
+      cp_async16(ring + (uint32_t)(((slot * kU + k) * NT + threadIdx.x) * 16), R.gbase + 16 * q);
+  }
+}
+// Vector k of this thread's part of one step: from the ring, or assembled.
+template <typename E, int NT>
+__device__ __forceinline__ uint4 unit_vec(const RowInfo &R, int step, int k, const uint8_t *ring,
+                                          int slot, int v0, int v1) {
+  constexpr int kStepVec = NT * kU;
+  const int q = step * kStepVec + threadIdx.x + k * NT;
+  if (q >= R.qlo && q < R.qhi)
+    return *reinterpret_cast<const uint4 *>(ring + ((slot * kU + k) * NT + threadIdx.x) * 16);
+  if (q >= R.nvec) {  // past the slice
+    const uint32_t w = Elt<E>::kNegInfWord;
+    return make_uint4(w, w, w, w);
+  }
+  return load_vec_slow<E>(R, q, v0, v1);
+}
+
+// -------------------------------------------------------- shared memory --
+// Dynamic shared memory carve-out (byte offsets), identical on host and
+// device.  nrows: rows streamed per sequence; KF: keys kept per row.
+struct Layout {
+  int ring, wstat, wtop, part_m, part_i, part_c, part_z, part_tv, part_ti, total;
+};
+__host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
+__host__ __device__ inline Layout make_layout(int NT, int nrows, int KF) {
+  const int nw = NT / 32;
+  Layout L;
+  int o = 0;
+  L.ring = o;                                    // [kDepth][kU][NT] 16-byte slots
+  o = align128(o + kDepth * kU * NT * 16);
+  L.wstat = o;                                   // [nrows][nw] WStat
+  o = align128(o + 16 * nrows * nw);
+  L.wtop = o;                                    // [nrows][nw][KF] {v, i}
+  o = align128(o + 8 * nrows * nw * KF);
+  L.part_m = o;                                  // [nrows] float
+  o = align128(o + 4 * nrows);
+  L.part_i = o;                                  // [nrows] int
+  o = align128(o + 4 * nrows);
+  L.part_c = o;                                  // [nrows] float
+  o = align128(o + 4 * nrows);
+  L.part_z = o;                                  // [nrows] double
+  o = align128(o + 8 * nrows);
+  L.part_tv = o;                                 // [nrows][KF] float
+  o = align128(o + 4 * nrows * KF);
+  L.part_ti = o;                                 // [nrows][KF] int
+  o = align128(o + 4 * nrows * KF);
+  L.total = o;
+  return L;
+}
+
+// Warp partial of one row: max, sum z of 2^(l s + c), offset c, argmax.
+struct WStat {
+  float m, z, c;
+  int idx;
+};
+
+struct Static {
+  RowInfo rows[kMaxRows];
+  int trow[SD_MAX_K + 1];  // row slot of target row j
+  int drow[SD_MAX_K + 1];  // row slot of draft row j (K: bonus row), -1 if absent
+  int nrows;
+  int d[SD_MAX_K];         // drafted tokens
+  float ld_t[SD_MAX_K];    // target logit of d_j
+  float ld_d[SD_MAX_K];    // draft logit of d_j
+  float M[kMaxRows];       // combined row statistics: max,
+  float C[kMaxRows];       //   offset C: sum over the row of 2^(l s) = Z 2^-C
+  double Z[kMaxRows];
+  int amax[kMaxRows];      //   lowest index of the max
+  int m, kind, owner, valid;  // kind: 0 none, 1 residual at m, 2 from p at m
+  double t_loc;
+  int cstar;
+  double s_part;              // this CTA's mass of the sampling pass
+  double wmass[kMaxWarps];    //   per warp (contiguous ranges), and its prefix
+  double wpre[kMaxWarps];
+  int wsel;                   //   the warp holding the crossing point
+  double t_w;
+  double red_d[kMaxWarps];
+  int red_i[kMaxWarps];
+  int tok;
+  int flag_compact;
+};
+
+// --------------------------------------------------------- finalization --
 // Exclusive scan of tau and packing of out_tokens, one CTA.  `cg_loads`
 // reads values written by other CTAs of the same grid through L2.
 __device__ void compact_block(int B, int K, const int32_t *out_tokens, const int32_t *tau,
                               int32_t *offsets, int32_t *packed, int32_t *status, bool cg_loads,
-                              Red &red) {
+                              int *red) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int carry = 0;
   for (int base = 0; base < B; base += blockDim.x) {
@@ -775,482 +486,893 @@ __device__ void compact_block(int B, int K, const int32_t *out_tokens, const int
       const int y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
-    if (lane == 31) red.i[w] = x;
+    if (lane == 31) red[w] = x;
     __syncthreads();
     if (w == 0) {
-      int v = lane < nw ? red.i[lane] : 0;
+      int v = lane < nw ? red[lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += y;
       }
-      if (lane < nw) red.i[lane] = v;  // inclusive warp totals
+      if (lane < nw) red[lane] = v;  // inclusive warp totals
     }
     __syncthreads();
-    const int excl = carry + (w > 0 ? red.i[w - 1] : 0) + x - t;
+    const int excl = carry + (w > 0 ? red[w - 1] : 0) + x - t;
     if (b < B) {
       offsets[b] = excl;
       const int32_t *src = out_tokens + (int64_t)b * (K + 1);
       for (int i = 0; i < t; ++i) packed[excl + i] = cg_loads ? __ldcg(src + i) : src[i];
     }
-    carry += red.i[nw - 1];
+    carry += red[nw - 1];
     __syncthreads();
   }
   if (threadIdx.x == 0) offsets[B] = carry;
 }
 
 // ------------------------------------------------------------ the kernel --
+// Weights of the sampling pass for the elements of one target vector:
+// residual Zt (p - q)+ = max(0, 2^(l s + Ct) - 2^(l' s + Cd) R), R = Zt / Zd,
+// or Zt p = 2^(l s + Ct) for a draw from p.
 template <typename E>
-__global__ void __launch_bounds__(kThreads, 1) sd_verify_kernel(const __grid_constant__ Params P) {
+__device__ __forceinline__ void pass_weights(const float *ft, const float *fd, bool residual,
+                                             float Ct, float Cd, float s, float R, float *w) {
+  constexpr int N = Elt<E>::kPerVec;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const float pt = ex2(fmaf(ft[k], s, Ct));
+    w[k] = residual ? fmaxf(0.f, pt - ex2(fmaf(fd[k], s, Cd)) * R) : pt;
+  }
+}
+
+// Per-thread state of the row being streamed.
+template <int KF>
+struct RowAcc {
+  static constexpr int KFm = KF > 0 ? KF : 1;
+  float m;        // running max
+  float c;        // exp offset: z = sum 2^(l s + c); +inf before the first finite value
+  float z, zc;    // Kahan sum and compensation
+  uint4 bv;       // first vector that reached the running max
+  int bq;         // its slice vector index
+  float kv[KFm];  // keys: this thread's best vectors by (masked max, index)
+  int kq[KFm];
+  float theta;    // keys: lower bound of the warp's KF-th best vector max
+  __device__ __forceinline__ void reset() {
+    m = -INFINITY;
+    c = INFINITY;
+    z = zc = 0.f;
+    bq = -1;
+    theta = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < KFm; ++k) {
+      kv[k] = -INFINITY;
+      kq[k] = INT32_MAX;
+    }
+  }
+};
+
+// One step of one row: kU vectors per thread.
+template <typename E, int KF, int NT>
+__device__ __forceinline__ void process_step(RowAcc<KF> &A, int flags, int hp, int qd, int excl,
+                                             int step, const uint4 *v, int v0, float s) {
+  constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec;
+  const int qbase = step * (NT * kU) + threadIdx.x;
+  float vm[kU];
+  float gmax = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kU; ++k) {
+    vm[k] = Elt<E>::vmax(v[k]);
+    gmax = fmaxf(gmax, vm[k]);
+  }
+  if (gmax > A.m) {
+    A.m = gmax;
+    if (flags & kNeedArg) {
+      int kb = kU - 1;
+#pragma unroll
+      for (int k = kU - 1; k >= 0; --k)
+        if (vm[k] == gmax) kb = k;
+#pragma unroll
+      for (int k = 0; k < kU; ++k)
+        if (k == kb) {
+          A.bv = v[k];
+          A.bq = qbase + k * NT;
+        }
+    }
+  }
+  if ((flags & kNeedExp) && gmax > -INFINITY) {
+    const float cg = -(gmax * s);
+    if (A.c == INFINITY) {
+      A.c = cg;
+    } else if (A.c - cg > kRebase) {  // the max rose by more than kRebase (log2)
+      const float f = ex2(cg - A.c);
+      A.z *= f;
+      A.zc *= f;
+      A.c = cg;
+    }
+    float vs[kU];  // independent per-vector sums, then one compensated add
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      float f[N];
+      Elt<E>::unpack(v[k], f);
+#pragma unroll
+      for (int i = 0; i < N; ++i) f[i] = ex2(fmaf(f[i], s, A.c));
+#pragma unroll
+      for (int h = N / 2; h > 0; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) f[i] += f[i + h];
+      vs[k] = f[0];
+    }
+#pragma unroll
+    for (int h = kU / 2; h > 0; h >>= 1)
+#pragma unroll
+      for (int k = 0; k < h; ++k) vs[k] += vs[k + h];
+    kahan_add(A.z, A.zc, vs[0]);
+  }
+  if (KF > 0 && (flags & kNeedKeys)) {
+    // The top-KF elements of a set lie in its top-KF vectors ranked by
+    // (max, index): every vector holding one of them has a max at least the
+    // KF-th value, and at most KF vectors reach it.  Track those vectors.
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      const int q = qbase + k * NT;
+      if (q == qd) {  // the vector holding the excluded token: its max without it
+        float f[N];
+        Elt<E>::unpack(v[k], f);
+        float mm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+          if (elem_index(v0, hp, q, i, sz) != excl) mm = fmaxf(mm, f[i]);
+        vm[k] = mm;
+      }
+    }
+    if (step == 0) {  // first step of the row: a warp-wide lower bound
+      const float srt = warp_sort_desc(vm[0]);
+      A.theta = __shfl_sync(0xffffffffu, srt, KF - 1);
+    }
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      if (vm[k] > A.kv[KF - 1] && vm[k] >= A.theta) {
+        A.kv[KF - 1] = vm[k];
+        A.kq[KF - 1] = qbase + k * NT;
+#pragma unroll
+        for (int x = KF - 1; x > 0; --x) {
+          if (better(A.kv[x], A.kq[x], A.kv[x - 1], A.kq[x - 1])) {
+            const float t1 = A.kv[x];
+            A.kv[x] = A.kv[x - 1];
+            A.kv[x - 1] = t1;
+            const int t2 = A.kq[x];
+            A.kq[x] = A.kq[x - 1];
+            A.kq[x - 1] = t2;
+          }
+        }
+      }
+    }
+  }
+}
+
+// End of a row: warp-level statistics into wstat / wtop.
+template <typename E, int KF>
+__device__ __forceinline__ void row_end(RowAcc<KF> &A, const RowInfo &R, int v0, int v1,
+                                        WStat *ws, float2 *wt) {
+  constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec;
+  constexpr int KFm = RowAcc<KF>::KFm;
+  const int lane = threadIdx.x & 31;
+  const float mw = warp_max(A.m);
+  int idx = INT32_MAX;
+  if ((R.flags & kNeedArg) && A.m == mw && A.m > -INFINITY && A.bq >= 0) {
+    float f[N];
+    Elt<E>::unpack(A.bv, f);
+#pragma unroll
+    for (int i = N - 1; i >= 0; --i)
+      if (f[i] == A.m) idx = elem_index(v0, R.hp, A.bq, i, sz);
+  }
+  const int iw = warp_min_i(idx);
+  const bool has = A.z > 0.f;
+  const float cw = -warp_max(has ? -A.c : -INFINITY);  // min offset of the warp
+  const float zt = has ? (A.z - A.zc) * ex2(cw - A.c) : 0.f;
+  const float zw = warp_sum(zt);
+  if (lane == 0) *ws = WStat{mw, zw, cw, iw};
+  if (KF > 0 && (R.flags & kNeedKeys)) {
+    // the warp's best KF vectors, then its best KF elements among them
+    int selq[KFm];
+#pragma unroll
+    for (int r = 0; r < KFm; ++r) {
+      float bv = A.kv[0];
+      int bq = A.kq[0];
+      warp_best(bv, bq);
+      if (bq != INT32_MAX && A.kq[0] == bq) {
+#pragma unroll
+        for (int x = 0; x < KFm - 1; ++x) {
+          A.kv[x] = A.kv[x + 1];
+          A.kq[x] = A.kq[x + 1];
+        }
+        A.kv[KFm - 1] = -INFINITY;
+        A.kq[KFm - 1] = INT32_MAX;
+      }
+      selq[r] = bv > -INFINITY ? bq : INT32_MAX;
+    }
+    constexpr int NC = KFm * N;                   // candidate elements
+    constexpr int PER = (NC + 31) / 32;           // per lane
+    float cv[PER];
+    int ci[PER];
+#pragma unroll
+    for (int h = 0; h < PER; ++h) {
+      cv[h] = -INFINITY;
+      ci[h] = INT32_MAX;
+      const int c = lane + 32 * h;
+      if (c < NC) {
+        int qq = INT32_MAX;
+#pragma unroll
+        for (int r = 0; r < KFm; ++r)
+          if (r == c / N) qq = selq[r];
+        if (qq != INT32_MAX) {
+          const int e = elem_index(v0, R.hp, qq, c % N, sz);
+          if (e >= v0 && e < v1 && e != R.excl) {
+            const float x = Elt<E>::load_global(R.g + (int64_t)e * sz);
+            if (x > -INFINITY) {
+              cv[h] = x;
+              ci[h] = e;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < KFm; ++r) {
+      int hb = 0;
+#pragma unroll
+      for (int h = 1; h < PER; ++h)
+        if (better(cv[h], ci[h], cv[hb], ci[hb])) hb = h;
+      float bv = -INFINITY;
+      int bi = INT32_MAX;
+#pragma unroll
+      for (int h = 0; h < PER; ++h)
+        if (h == hb) {
+          bv = cv[h];
+          bi = ci[h];
+        }
+      warp_best(bv, bi);
+#pragma unroll
+      for (int h = 0; h < PER; ++h)
+        if (bi != INT32_MAX && ci[h] == bi) {
+          cv[h] = -INFINITY;
+          ci[h] = INT32_MAX;
+        }
+      if (lane == 0) wt[r] = make_float2(bv, __int_as_float(bi));
+    }
+  }
+  A.reset();
+}
+
+template <typename E, int KF, int NT>
+__global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_constant__ Params P) {
   constexpr int sz = Elt<E>::kSize, NV = Elt<E>::kPerVec;
+  constexpr int KFm = KF > 0 ? KF : 1;
+  constexpr int NW = NT / 32;
+  constexpr int kStepVec = NT * kU;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int cs = P.cs;
-  const int cid = blockIdx.x / cs;
-  const int ncl = gridDim.x / cs;
+  const int b = blockIdx.x / cs;
+  const int K = P.K;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  __shared__ Smem sm;
+  __shared__ Static S;
   extern __shared__ __align__(128) uint8_t dyn[];
-  // dynamic layout: stages (2 regions each), csum, candidate buffer
-  uint8_t *stage_base[2] = {dyn, dyn + (P.nstage > 1 ? 2 * P.region : 0)};
-  float *csum = reinterpret_cast<float *>(dyn + P.nstage * 2 * P.region);
-  const int nvec_max = P.region / 16;
-  float *cand_v = csum + nvec_max;
-  int *cand_i = reinterpret_cast<int *>(cand_v + kCandCap);
 
   const int v0 = min(rank * P.slice, P.V);
   const int v1 = min(v0 + P.slice, P.V);
+  const bool verify = P.mode == kVerify;
+  const float T = verify ? P.temps[b] : 0.f;
+  const bool tvalid = !verify || ((T >= 0.f) && (T <= 3.4e38f));  // rejects NaN / inf / < 0
+  const bool sampled = verify && tvalid && T > 0.f;
+  // scaled logits x = l s with s = log2(e) / T rounded to float; every
+  // exponential below uses this same s
+  const float s = sampled ? (float)(1.4426950408889634 / (double)T) : 0.f;
+  const double sd = (double)s;
 
-  if (threadIdx.x == 0) {
-    mbar_init(&sm.bar[0], 1);
-    mbar_init(&sm.bar[1], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    sm.flag_compact = 0;
+  // ---- drafted tokens
+  int dvalid_local = 1;
+  int my_d = -1;
+  for (int j = tid; j < K; j += NT) {
+    const int d = P.tokens[(int64_t)b * K + j];
+    S.d[j] = d;
+    if (!(d >= 0 && d < P.V)) dvalid_local = 0;
+    if (j == tid) my_d = d;
+  }
+  const bool dvalid = __syncthreads_and(dvalid_local) != 0;
+
+  // ---- the rows this CTA streams, in order (bonus, K, then K-1..0)
+  if (tid == 0) {
+    int n = 0;
+    const int64_t V = P.V;
+    for (int j = 0; j <= K; ++j) {
+      S.trow[j] = -1;
+      S.drow[j] = -1;
+    }
+    auto add = [&](const uint8_t *g, int kind, int j, int flags, int excl, int fan) {
+      RowInfo &R = S.rows[n];
+      R.g = g;
+      R.kind = kind;
+      R.j = j;
+      R.flags = flags;
+      R.excl = excl;
+      R.fan = fan;
+      row_geometry<NT>(R, v0, v1, sz);
+      if (kind == kTarget) S.trow[j] = n;
+      else S.drow[j] = n;
+      ++n;
+    };
+    const int fK = P.keys ? P.fanout[K] : 0;
+    if (fK > 0 && P.bonus) add(P.bonus + (int64_t)b * V * sz, kBonus, K, kNeedKeys, -1, fK);
+    if (verify)
+      add(P.target + ((int64_t)b * (K + 1) + K) * V * sz, kTarget, K,
+          kNeedArg | (sampled ? kNeedExp : 0), -1, 0);
+    for (int j = K - 1; j >= 0; --j) {
+      const int fj = P.keys ? P.fanout[j] : 0;
+      if (sampled || fj > 0)
+        add(P.draft + ((int64_t)b * K + j) * V * sz, kDraft, j,
+            (sampled ? kNeedExp : 0) | (fj > 0 ? kNeedKeys : 0), S.d[j], fj);
+      if (verify)
+        add(P.target + ((int64_t)b * (K + 1) + j) * V * sz, kTarget, j,
+            kNeedArg | (sampled ? kNeedExp : 0), -1, 0);
+    }
+    S.nrows = n;
+    S.flag_compact = 0;
   }
   __syncthreads();
 
-  uint32_t phase[2] = {0u, 0u};
-  bool timed_out = false;
-  int late_stage = -1;       // stage whose bounded wait gave up
-  uint32_t late_parity = 0u;
+  // the logits at the drafted tokens: loaded now, used after the stream
+  float my_lt = -INFINITY, my_ld = -INFINITY;
+  if (tid < K && sampled && my_d >= 0 && my_d < P.V) {
+    my_lt = Elt<E>::load_global(P.target + (((int64_t)b * (K + 1) + tid) * P.V + my_d) * sz);
+    my_ld = Elt<E>::load_global(P.draft + (((int64_t)b * K + tid) * P.V + my_d) * sz);
+  }
 
-  auto issue = [&](int k) {
-    // thread 0 only: loads of the k-th item of this cluster into stage k % nstage
-    const int it = cid + k * ncl;
-    const Item I = describe<E>(P, it);
-    uint8_t *sb = stage_base[k % P.nstage];
-    uint64_t *bar = &sm.bar[k % P.nstage];
-    Slice st{}, s1{};
-    uint32_t tx = 0;
-    if (I.need_t) {
-      st = make_slice(I.trow, v0, v1, sz);
-      tx += bulk_bytes<E>(I.trow, st);
+  const int nrows = S.nrows;
+  const Layout L = make_layout(NT, nrows, KF);
+  uint8_t *ring = dyn + L.ring;
+  const uint32_t ring_s = smem_u32(ring);
+  WStat *wstat = reinterpret_cast<WStat *>(dyn + L.wstat);
+  float2 *wtop = reinterpret_cast<float2 *>(dyn + L.wtop);  // .x value, .y index bits
+  float *part_m = reinterpret_cast<float *>(dyn + L.part_m);
+  int *part_i = reinterpret_cast<int *>(dyn + L.part_i);
+  float *part_c = reinterpret_cast<float *>(dyn + L.part_c);
+  double *part_z = reinterpret_cast<double *>(dyn + L.part_z);
+  float *part_tv = reinterpret_cast<float *>(dyn + L.part_tv);
+  int *part_ti = reinterpret_cast<int *>(dyn + L.part_ti);
+
+  // ---- stream every row once.  Each thread copies its own vectors
+  // kDepth-1 steps ahead into its own ring slots (cp.async).
+  int total = 0;
+  for (int r = 0; r < nrows; ++r) total += S.rows[r].nsteps;
+  RowAcc<KF> A;
+  A.reset();
+  auto advance = [&](int &row, int &step) {
+    ++step;
+    while (row < nrows && step >= S.rows[row].nsteps) {
+      ++row;
+      step = 0;
     }
-    if (I.need_1) {
-      s1 = make_slice(I.row1, v0, v1, sz);
-      tx += bulk_bytes<E>(I.row1, s1);
-    }
-    // the stage was last read through the generic proxy; order those reads
-    // before the bulk copies (async proxy) overwrite it
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive_expect_tx(bar, tx);
-    if (I.need_t) issue_slice<E>(sb, I.trow, st, bar);
-    if (I.need_1) issue_slice<E>(sb + P.region, I.row1, s1, bar);
   };
-
-  const int n_mine = cid < P.n_items ? (P.n_items - 1 - cid) / ncl + 1 : 0;
-  if (threadIdx.x == 0 && n_mine > 0) issue(0);
-
-  for (int k = 0; k < n_mine; ++k) {
-    const int it = cid + k * ncl;
-    const int par = k & 1;
-    const int stg = k % P.nstage;
-    if (threadIdx.x == 0) {
-      if (P.nstage > 1 && k + 1 < n_mine) issue(k + 1);
-      else if (P.nstage == 1 && k > 0) issue(k);
+  int i_row = 0, i_step = 0;  // next step to copy
+  while (i_row < nrows && S.rows[i_row].nsteps == 0) ++i_row;
+  int c_row = i_row, c_step = 0;  // step being consumed
+  auto issue_next = [&](int slot) {
+    if (i_row < nrows) {
+      issue_unit<NT>(S.rows[i_row], i_step, ring_s, slot);
+      advance(i_row, i_step);
     }
-    if (!mbar_wait_bounded(&sm.bar[stg], phase[stg])) {
-      timed_out = true;
-      late_stage = stg;
-      late_parity = phase[stg];
-    }
-    phase[stg] ^= 1u;
-    __syncthreads();
-
-    const Item I = describe<E>(P, it);
-    const uint8_t *rt = stage_base[stg];
-    const uint8_t *r1 = stage_base[stg] + P.region;
-    Slice st{}, s1{};
-    if (I.need_t) st = make_slice(I.trow, v0, v1, sz);
-    if (I.need_1) s1 = make_slice(I.row1, v0, v1, sz);
-    const double s_d = I.sampled ? 1.4426950408889634 / (double)I.T : 0.0;
-    // s = s_hi + s_lo with s_lo > 0, so that (-inf) * s_lo stays -inf
-    const float s_hi = __double2float_rd(s_d);
-    const float s_lo = fmaxf((float)(s_d - (double)s_hi), 1.17549435e-38f);
-    Part &mine = sm.part[par];
-
-    // ---- target row j: max, argmax, sum of exponentials, logit of d_j
-    if (I.need_t) {
-      const float mt = slice_max<E>(rt, st);
-      const float Mc = block_max(mt, sm.red);
-      int at = mt == Mc ? slice_first_eq<E>(rt, st, Mc) : INT32_MAX;
-      at = block_min_i(at, sm.red);
-      double zc = 0.0;
-      if (I.sampled) zc = block_sum_d((double)slice_expsum<E>(rt, st, Mc, s_hi, s_lo), sm.red);
-      if (threadIdx.x == 0) {
-        mine.mt = Mc;
-        mine.at = at;
-        mine.zt = zc;
-        mine.has_ld = 0;
-        mine.ld = -INFINITY;
-        if (I.j < P.K && I.dvalid && I.d >= st.v0 && I.d < st.v1) {
-          mine.has_ld = 1;
-          mine.ld = Elt<E>::load(rt + st.hp + (I.d - st.v0) * sz);
-        }
-      }
-    }
-    // ---- second row (draft row j, or the bonus draft row at j == K)
-    if (threadIdx.x == 0) {
-      mine.nc = 0;
-      mine.has_l1d = 0;
-      mine.m1 = -INFINITY;
-      mine.z1 = 0.0;
-      if (!I.need_t) {
-        mine.mt = -INFINITY;
-        mine.at = INT32_MAX;
-        mine.zt = 0.0;
-        mine.has_ld = 0;
-      }
-    }
-    if (I.need_1) {
-      const float m1 = slice_max<E>(r1, s1);
-      const float M1c = block_max(m1, sm.red);
-      double z1 = 0.0;
-      if (I.sampled && I.j < P.K && P.mode == kVerify)
-        z1 = block_sum_d((double)slice_expsum<E>(r1, s1, M1c, s_hi, s_lo), sm.red);
-      if (threadIdx.x == 0) {
-        mine.m1 = M1c;
-        mine.z1 = z1;
-        if (I.j < P.K && I.dvalid && I.d >= s1.v0 && I.d < s1.v1) {
-          mine.has_l1d = 1;
-          mine.l1d = Elt<E>::load(r1 + s1.hp + (I.d - s1.v0) * sz);
-        }
-      }
-      if (I.fan > 0) {
-        __syncthreads();
-        slice_topf<E>(r1, s1, m1, I.fan, I.j < P.K ? I.d : -1, cand_v, cand_i, sm, mine);
-      }
-    }
-    cluster.sync();
-
-    // ---- gather the cluster's partials (one thread per peer, 16-byte loads)
-    if ((int)threadIdx.x < cs) {
-      const int4 *src =
-          reinterpret_cast<const int4 *>(cluster.map_shared_rank(&sm.part[par], (int)threadIdx.x));
-      int4 *dst = reinterpret_cast<int4 *>(&sm.peer[threadIdx.x]);
+    cp_commit();
+  };
 #pragma unroll
-      for (int w = 0; w < (int)(sizeof(Part) / 16); ++w) dst[w] = src[w];
+  for (int d = 0; d < kDepth - 1; ++d) issue_next(d);
+  for (int st = 0; st < total; ++st) {
+    issue_next((st + kDepth - 1) % kDepth);
+    cp_wait<kDepth - 1>();  // this step's copies have landed
+    const RowInfo &R = S.rows[c_row];
+    const int flags = R.flags, hp = R.hp, qd = R.qd, excl = R.excl, nsteps = R.nsteps;
+    uint4 cur[kU];
+#pragma unroll
+    for (int k = 0; k < kU; ++k)
+      cur[k] = unit_vec<E, NT>(R, c_step, k, ring, st % kDepth, v0, v1);
+    process_step<E, KF, NT>(A, flags, hp, qd, excl, c_step, cur, v0, s);
+    if (c_step == nsteps - 1)
+      row_end<E, KF>(A, S.rows[c_row], v0, v1, &wstat[c_row * NW + warp],
+                     &wtop[(c_row * NW + warp) * KFm]);
+    advance(c_row, c_step);
+  }
+  cp_wait<0>();
+
+  // rows with an empty slice (this CTA holds no vocabulary) still need entries
+  if (total == 0) {
+    for (int x = tid; x < nrows * NW; x += NT) wstat[x] = WStat{-INFINITY, 0.f, INFINITY, INT32_MAX};
+    if (KF > 0)
+      for (int x = tid; x < nrows * NW * KFm; x += NT)
+        wtop[x] = make_float2(-INFINITY, __int_as_float(INT32_MAX));
+  }
+  if (tid < K) {
+    S.ld_t[tid] = my_lt;
+    S.ld_d[tid] = my_ld;
+  }
+  __syncthreads();
+
+  // ---- CTA statistics per row (one warp per row)
+  for (int r = warp; r < nrows; r += NW) {
+    const RowInfo &R = S.rows[r];
+    const WStat wsl = lane < NW ? wstat[r * NW + lane] : WStat{-INFINITY, 0.f, INFINITY, INT32_MAX};
+    const float Mc = warp_max(wsl.m);
+    const int ic = warp_min_i(wsl.m == Mc ? wsl.idx : INT32_MAX);
+    const bool has = wsl.z > 0.f;
+    const float cb = -warp_max(has ? -wsl.c : -INFINITY);
+    const double term = has ? (double)wsl.z * (double)ex2(cb - wsl.c) : 0.0;
+    const double Zc = warp_sum_d(term);
+    if (lane == 0) {
+      part_m[r] = Mc;
+      part_i[r] = ic;
+      part_c[r] = cb;
+      part_z[r] = Zc;
     }
-    __syncthreads();
-    // ---- combine them (same order in every CTA, so every CTA decides alike)
-    if (threadIdx.x == 0) {
-      float M = -INFINITY, M1 = -INFINITY;
-      for (int c = 0; c < cs; ++c) {
-        M = fmaxf(M, sm.peer[c].mt);
-        M1 = fmaxf(M1, sm.peer[c].m1);
-      }
-      sm.dec.M = M;
-      sm.dec.M1 = M1;
-    }
-    __syncthreads();
-    if ((int)threadIdx.x < cs) {
-      const Part &pc = sm.peer[threadIdx.x];
-      sm.zterm[threadIdx.x] = (I.need_t && I.sampled && pc.zt > 0.0)
-                                  ? pc.zt * exp2(((double)pc.mt - (double)sm.dec.M) * s_d)
-                                  : 0.0;
-      sm.z1term[threadIdx.x] = (I.need_1 && I.sampled && pc.z1 > 0.0)
-                                   ? pc.z1 * exp2(((double)pc.m1 - (double)sm.dec.M1) * s_d)
-                                   : 0.0;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      Decision D;
-      D.s_hi = s_hi;
-      D.s_lo = s_lo;
-      D.accept = 0;
-      D.sample = 0;
-      D.token = -1;
-      D.owner = 0;
-      D.ratio = NAN;
-      D.p_d = NAN;
-      D.q_d = NAN;
-      D.M = sm.dec.M;
-      D.M1 = sm.dec.M1;
-      D.Zt = 0.0;
-      D.Z1 = 0.0;
-      float ld = -INFINITY, l1d = -INFINITY;
-      int amax = INT32_MAX;
-      for (int c = 0; c < cs; ++c) {
-        const Part &pc = sm.peer[c];
-        if (I.need_t) {
-          if (amax == INT32_MAX && pc.mt == D.M && pc.at != INT32_MAX) amax = pc.at;
-          D.Zt += sm.zterm[c];
-          if (pc.has_ld) ld = pc.ld;
+    if (KF > 0 && (R.flags & kNeedKeys)) {
+      // NW x KF candidates; lane l holds candidates l, l + 32, ...
+      constexpr int PER = (NW * KFm + 31) / 32;
+      float cv[PER];
+      int ci[PER];
+#pragma unroll
+      for (int h = 0; h < PER; ++h) {
+        const int c = lane + 32 * h;
+        cv[h] = -INFINITY;
+        ci[h] = INT32_MAX;
+        if (c < NW * KFm) {
+          const float2 e = wtop[r * NW * KFm + c];
+          cv[h] = e.x;
+          ci[h] = __float_as_int(e.y);
         }
-        if (I.need_1) {
-          D.Z1 += sm.z1term[c];
-          if (pc.has_l1d) l1d = pc.l1d;
+      }
+      for (int r2 = 0; r2 < KFm; ++r2) {
+        int hb = 0;
+#pragma unroll
+        for (int h = 1; h < PER; ++h)
+          if (better(cv[h], ci[h], cv[hb], ci[hb])) hb = h;
+        float bv = -INFINITY;
+        int bi = INT32_MAX;
+#pragma unroll
+        for (int h = 0; h < PER; ++h)
+          if (h == hb) {
+            bv = cv[h];
+            bi = ci[h];
+          }
+        warp_best(bv, bi);
+#pragma unroll
+        for (int h = 0; h < PER; ++h)
+          if (bi != INT32_MAX && ci[h] == bi) {
+            cv[h] = -INFINITY;
+            ci[h] = INT32_MAX;
+          }
+        if (lane == 0) {
+          part_tv[r * KFm + r2] = bv;
+          part_ti[r * KFm + r2] = bi;
         }
       }
-      D.amax = amax == INT32_MAX ? 0 : amax;
-      if (P.mode == kVerify) {
-        if (I.j < P.K) {
-          if (!I.sampled) {
-            D.accept = (I.dvalid && I.d == D.amax) ? 1 : 0;
-          } else if (I.dvalid) {
-            const double pd = exp2(((double)ld - (double)D.M) * s_d) / D.Zt;
-            const double qd = exp2(((double)l1d - (double)D.M1) * s_d) / D.Z1;
-            const double r = qd > 0.0 ? pd / qd : INFINITY;
-            const double u = uniform_u(P.seed, P.row_base + I.b, I.j, 0);
-            D.accept = (u <= r) ? 1 : 0;
-            D.ratio = (float)r;
-            D.p_d = (float)pd;
-            D.q_d = (float)qd;
+    }
+  }
+  cluster.sync();  // (1) every CTA's per-row partials are ready
+
+  // ---- combine the cluster's partials (same arithmetic in every CTA)
+  for (int r = warp; r < nrows; r += NW) {
+    const RowInfo &R = S.rows[r];
+    float pm = -INFINITY, pc = INFINITY;
+    double pz = 0.0;
+    int pi = INT32_MAX;
+    if (lane < cs) {
+      pm = *cluster.map_shared_rank(&part_m[r], lane);
+      pc = *cluster.map_shared_rank(&part_c[r], lane);
+      pz = *cluster.map_shared_rank(&part_z[r], lane);
+      pi = *cluster.map_shared_rank(&part_i[r], lane);
+    }
+    const float M = warp_max(pm);
+    const int am = warp_min_i(pm == M ? pi : INT32_MAX);
+    const bool has = pz > 0.0;
+    const float C = -warp_max(has ? -pc : -INFINITY);
+    const double term = has ? pz * (double)ex2(C - pc) : 0.0;
+    const double Z = warp_sum_d(term);
+    if (lane == 0) {
+      S.M[r] = M;
+      S.C[r] = C;
+      S.Z[r] = Z;
+      S.amax[r] = am == INT32_MAX ? 0 : am;
+    }
+    if (KF > 0 && (R.flags & kNeedKeys) && rank == 0 && P.keys_out) {
+      // merge cs x KF candidates into this row's keys
+      constexpr int PER = (kMaxCS * KFm + 31) / 32;
+      float cv[PER];
+      int ci[PER];
+#pragma unroll
+      for (int h = 0; h < PER; ++h) {
+        const int c = lane + 32 * h;  // candidate c: peer c / KF, rank c % KF
+        cv[h] = -INFINITY;
+        ci[h] = INT32_MAX;
+        if (c < cs * KFm) {
+          cv[h] = *cluster.map_shared_rank(&part_tv[r * KFm + c % KFm], c / KFm);
+          ci[h] = *cluster.map_shared_rank(&part_ti[r * KFm + c % KFm], c / KFm);
+        }
+      }
+      int32_t *kout = P.keys_out + ((int64_t)b * P.n_keys_out + P.fan_off[R.j]) * 2;
+      for (int r2 = 0; r2 < R.fan; ++r2) {
+        int hb = 0;
+#pragma unroll
+        for (int h = 1; h < PER; ++h)
+          if (better(cv[h], ci[h], cv[hb], ci[hb])) hb = h;
+        float bv = -INFINITY;
+        int bi = INT32_MAX;
+#pragma unroll
+        for (int h = 0; h < PER; ++h)
+          if (h == hb) {
+            bv = cv[h];
+            bi = ci[h];
+          }
+        warp_best(bv, bi);
+#pragma unroll
+        for (int h = 0; h < PER; ++h)
+          if (bi != INT32_MAX && ci[h] == bi) {
+            cv[h] = -INFINITY;
+            ci[h] = INT32_MAX;
+          }
+        if (lane == 0) {
+          kout[2 * r2] = bi == INT32_MAX ? -1 : R.j;
+          kout[2 * r2 + 1] = bi == INT32_MAX ? -1 : bi;
+        }
+      }
+    }
+  }
+  // keys of the bonus position when there is no bonus row: empty slots
+  if (P.keys && P.keys_out && rank == 0 && tid == 0 && P.fanout[K] > 0 && S.drow[K] < 0) {
+    int32_t *kout = P.keys_out + ((int64_t)b * P.n_keys_out + P.fan_off[K]) * 2;
+    for (int r2 = 0; r2 < P.fanout[K]; ++r2) {
+      kout[2 * r2] = -1;
+      kout[2 * r2 + 1] = -1;
+    }
+  }
+  __syncthreads();
+
+  if (verify) {
+    // ---- accept tests, one lane per position (K <= 32: warp 0)
+    if (warp == 0) {
+      const int j = lane;
+      int rej = 0;
+      if (j < K) {
+        const int rt = S.trow[j];
+        const int d = S.d[j];
+        int a = 0;
+        if (!sampled) {
+          a = (dvalid && d == S.amax[rt]) ? 1 : 0;
+        } else if (dvalid) {
+          const int rd = S.drow[j];
+          // log2 of 2^(l_d s + C): the product of two floats is exact in double
+          const double xt = (double)S.ld_t[j] * sd + (double)S.C[rt];
+          const double xd = (double)S.ld_d[j] * sd + (double)S.C[rd];
+          const float r = (S.ld_d[j] == -INFINITY)
+                              ? INFINITY  // q(d) = 0
+                              : exp2_split(xt - xd) * ((float)S.Z[rd] / (float)S.Z[rt]);
+          const double u = uniform_u(P.seed, P.row_base + b, j, 0);
+          a = (u <= (double)r) ? 1 : 0;
+          if (rank == 0) {
+            const int64_t pj = (int64_t)b * K + j;
+            if (P.ratio_out) P.ratio_out[pj] = r;
+            if (P.p_out) P.p_out[pj] = exp2_split(xt) / (float)S.Z[rt];
+            if (P.q_out) P.q_out[pj] = exp2_split(xd) / (float)S.Z[rd];
           }
         }
-        if (I.sampled && I.dvalid) {
-          if (I.j == P.K) D.sample = 2;
-          else if (!D.accept) D.sample = 1;
-        }
-        if (!I.sampled) D.token = D.amax;
-        D.A = (float)(1.0 / D.Zt);
-        D.Bq = I.j < P.K && I.sampled ? (float)(1.0 / D.Z1) : 0.f;
+        rej = !a;
       }
-      sm.dec = D;
+      const unsigned rejects = __ballot_sync(0xffffffffu, rej);
+      if (lane == 0) {
+        const int mm = rejects ? __ffs(rejects) - 1 : K;
+        S.m = mm;
+        S.valid = (tvalid && dvalid) ? 1 : 0;
+        S.kind = 0;
+        S.owner = 0;
+        S.tok = -1;
+        S.cstar = 0;
+        if (S.valid) {
+          if (!sampled) S.tok = S.amax[S.trow[mm]];
+          else S.kind = mm < K ? 1 : 2;
+        }
+      }
     }
+    if (rank == 0 && P.argmax_out)
+      for (int j = tid; j <= K; j += NT) P.argmax_out[(int64_t)b * (K + 1) + j] = S.amax[S.trow[j]];
     __syncthreads();
 
-    // ---- sampling pass: residual at a rejection, or p at the bonus position
-    if (sm.dec.sample != 0) {
-      for (int attempt = 0; attempt < 2; ++attempt) {
-        const Decision &D = sm.dec;
-        float tsum = 0.f, tcomp = 0.f;
-        for (int q = threadIdx.x; q < st.nvec; q += blockDim.x) {
-          float w[NV];
-          sample_weights<E>(rt, st, r1, s1, q, D, w);
-#pragma unroll
-          for (int h = NV / 2; h > 0; h >>= 1)
-#pragma unroll
-            for (int k2 = 0; k2 < h; ++k2) w[k2] += w[k2 + h];
-          csum[q] = w[0];
-          kahan_add(tsum, tcomp, w[0]);
-        }
-        const double Sc = block_sum_d((double)tsum, sm.red);
-        if (threadIdx.x == 0) mine.s = Sc;
-        cluster.sync();
-        if ((int)threadIdx.x < cs)
-          sm.sterm[threadIdx.x] = cluster.map_shared_rank(&sm.part[par], (int)threadIdx.x)->s;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          Decision &Dw = sm.dec;
-          double S = 0.0;
-          const double *pre = sm.sterm;
-          for (int c = 0; c < cs; ++c) S += pre[c];
-          if (S > 0.0 || Dw.sample == 2) {
-            const double u = uniform_u(P.seed, P.row_base + I.b, I.j, 1);
-            const double t = u * S;
-            int cstar = -1, last_pos = -1;
-            double acc = 0.0, acc_star = 0.0;
-            for (int c = 0; c < cs; ++c) {
-              if (pre[c] > 0.0) {
-                last_pos = c;
-                if (cstar < 0 && acc + pre[c] > t) {
-                  cstar = c;
-                  acc_star = acc;
-                }
-              }
-              acc += pre[c];
-            }
-            if (cstar < 0) {  // rounding pushed t past the total
-              cstar = last_pos < 0 ? 0 : last_pos;
-              acc_star = 0.0;
-              for (int c = 0; c < cstar; ++c) acc_star += pre[c];
-            }
-            Dw.t = t;
-            Dw.cstar = cstar;
-            Dw.t_loc = t - acc_star;
-            Dw.owner = cstar;
-            sm.found_thread = 0;  // non-zero: retry
+    // ---- one inverse-CDF draw per sequence (residual at m, or p at K).
+    // Each warp takes a contiguous range of the slice, so warp masses are in
+    // index order; the owning CTA finds the crossing warp, which re-scans its
+    // range in 32-vector chunks.
+    for (int attempt = 0; attempt < 2 && S.kind != 0; ++attempt) {
+      const int mm = S.m;
+      const bool residual = S.kind == 1;
+      const RowInfo &Rt = S.rows[S.trow[mm]];
+      const RowInfo *Rd = residual ? &S.rows[S.drow[mm]] : nullptr;
+      const bool d_vec = residual && Rd->hp == Rt.hp;  // same vector grid
+      const float Ct = S.C[S.trow[mm]];
+      const float Cd = residual ? S.C[S.drow[mm]] : 0.f;
+      const float Rz = residual ? (float)(S.Z[S.trow[mm]] / S.Z[S.drow[mm]]) : 0.f;
+      const int wr = (Rt.nvec + NW - 1) / NW;  // vectors per warp
+      const int wq0 = min(warp * wr, Rt.nvec), wq1 = min(wq0 + wr, Rt.nvec);
+      const int wsteps = (wr + 32 * kU - 1) / (32 * kU);
+      // weights of this lane's vector q of the target (and draft) row
+      auto vec_mass = [&](uint4 tvec, uint4 dvec, int q, bool dv_ok) -> float {
+        float ft[NV], fd[NV], w[NV];
+        Elt<E>::unpack(tvec, ft);
+        if (residual) {
+          if (dv_ok) {
+            Elt<E>::unpack(dvec, fd);
           } else {
-            // empty residual: draw from p instead
-            Dw.sample = 2;
-            sm.found_thread = 1;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+              const int e = elem_index(v0, Rt.hp, q, i, sz);
+              fd[i] = (e >= v0 && e < v1) ? Elt<E>::load_global(Rd->g + (int64_t)e * sz)
+                                          : -INFINITY;
+            }
           }
         }
-        __syncthreads();
-        if (sm.found_thread == 0) break;
-        // all CTAs retry with mode 2 (uniform decision: same S everywhere)
-        cluster.sync();
+        pass_weights<E>(ft, fd, residual, Ct, Cd, s, Rz, w);
+#pragma unroll
+        for (int h = NV / 2; h > 0; h >>= 1)
+#pragma unroll
+          for (int i = 0; i < h; ++i) w[i] += w[i + h];
+        return w[0];
+      };
+      // units: target step t, then (same vector grid) draft step t
+      const int per = d_vec ? 2 : 1;
+      const int nunits = wsteps * per;
+      int i_u = 0;
+      auto issue_pass = [&](int slot) {
+        if (i_u < nunits) {
+          const RowInfo &RR = (i_u % per == 0) ? Rt : *Rd;
+          const int t = i_u / per;
+#pragma unroll
+          for (int k = 0; k < kU; ++k)
+            issue_vec<NT>(RR, wq0 + t * 32 * kU + k * 32 + lane, wq1, ring_s, slot, k);
+          ++i_u;
+        }
+        cp_commit();
+      };
+#pragma unroll
+      for (int d = 0; d < kDepth - 1; ++d) issue_pass(d);
+      float tsum = 0.f, tcomp = 0.f;
+      uint4 tv4[kU];
+      for (int u = 0; u < nunits; ++u) {
+        issue_pass((u + kDepth - 1) % kDepth);
+        cp_wait<kDepth - 1>();
+        const int t = u / per;
+        if (u % per == 0) {
+#pragma unroll
+          for (int k = 0; k < kU; ++k)
+            tv4[k] = fetch_vec<E, NT>(Rt, wq0 + t * 32 * kU + k * 32 + lane, wq1, ring, u % kDepth,
+                                      k, v0, v1);
+          if (per == 2) continue;  // the draft unit follows
+        }
+        float vs[kU];
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int q = wq0 + t * 32 * kU + k * 32 + lane;
+          uint4 dvec = tv4[k];
+          if (d_vec) dvec = fetch_vec<E, NT>(*Rd, q, wq1, ring, u % kDepth, k, v0, v1);
+          vs[k] = q < wq1 ? vec_mass(tv4[k], dvec, q, d_vec) : 0.f;
+        }
+#pragma unroll
+        for (int h = kU / 2; h > 0; h >>= 1)
+#pragma unroll
+          for (int k = 0; k < h; ++k) vs[k] += vs[k + h];
+        kahan_add(tsum, tcomp, vs[0]);
       }
-      // inverse CDF inside the owning CTA
-      const Decision &D = sm.dec;
-      if (rank == D.cstar) {
-        const int nt = blockDim.x;
-        const int per = (st.nvec + nt - 1) / nt;
-        const int q0 = min(threadIdx.x * per, st.nvec), q1 = min(q0 + per, st.nvec);
-        double mysum = 0.0;
-        for (int q = q0; q < q1; ++q) mysum += (double)csum[q];
-        // exclusive block scan of mysum (double)
-        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-        double x = mysum;
+      cp_wait<0>();
+      // warp masses, their prefix, the CTA mass
+      const double wm = warp_sum_d((double)tsum - (double)tcomp);
+      if (lane == 0) S.wmass[warp] = wm;
+      __syncthreads();
+      if (warp == 0) {
+        const double m_l = lane < NW ? S.wmass[lane] : 0.0;
+        double incl = m_l;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const double y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
+          const double y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
         }
-        if (lane == 31) sm.red.d[w] = x;
-        __syncthreads();
-        if (w == 0) {
-          double v = lane < nw ? sm.red.d[lane] : 0.0;
+        if (lane < NW) S.wpre[lane] = incl - m_l;
+        if (lane == 31) S.s_part = incl;
+      }
+      cluster.sync();  // (2) slice masses ready
+      if (warp == 0) {
+        // prefix of the slice masses over the cluster (lane c: CTA c)
+        const double sc = lane < cs ? *cluster.map_shared_rank(&S.s_part, lane) : 0.0;
+        double incl = sc;
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += y;
-          }
-          if (lane < nw) sm.red.d[lane] = v;
+        for (int o = 1; o < 32; o <<= 1) {
+          const double y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
         }
-        __syncthreads();
-        const double pre = (w > 0 ? sm.red.d[w - 1] : 0.0) + x - mysum;
-        const bool crosses = mysum > 0.0 && pre + mysum > D.t_loc;
-        int first = block_min_i(crosses ? (int)threadIdx.x : INT32_MAX, sm.red);
-        if (first == INT32_MAX) first = -block_min_i(mysum > 0.0 ? -(int)threadIdx.x : INT32_MAX, sm.red);
-        if (first == INT32_MAX || first < 0) first = 0;
-        if ((int)threadIdx.x == first) {
-          double cum = pre;
-          int qs = -1, qlast = -1;
-          for (int q = q0; q < q1; ++q) {
-            if (csum[q] > 0.f) qlast = q;
-            if (qs < 0 && csum[q] > 0.f && cum + (double)csum[q] > D.t_loc) qs = q;
-            if (qs < 0) cum += (double)csum[q];
+        const double tot = __shfl_sync(0xffffffffu, incl, 31);
+        if (tot > 0.0 || !residual) {
+          const double u = uniform_u(P.seed, P.row_base + b, mm, 1);
+          const double t = u * tot;
+          const unsigned cross = __ballot_sync(0xffffffffu, sc > 0.0 && incl > t);
+          const unsigned pos = __ballot_sync(0xffffffffu, sc > 0.0);
+          // the first CTA whose range passes t; if rounding put t past the
+          // total, the last CTA with mass
+          const int cstar = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : 0);
+          const double before = __shfl_sync(0xffffffffu, incl - sc, cstar);
+          if (lane == 0) {
+            S.cstar = cstar;
+            S.t_loc = t - before;
+            S.owner = cstar;
           }
-          if (qs < 0) {
-            qs = qlast;
-            cum = pre;
-            for (int q = q0; q < qs; ++q) cum += (double)csum[q];
-          }
-          int tok = -1, klast = -1;
-          if (qs >= 0) {
-            float wv[NV];
-            sample_weights<E>(rt, st, r1, s1, qs, D, wv);
-            const int e0 = st.first_elem(qs, sz);
-            double c2 = cum;
-            for (int k2 = 0; k2 < NV; ++k2) {
-              if (wv[k2] > 0.f) {
-                klast = e0 + k2;
-                if (tok < 0 && c2 + (double)wv[k2] > D.t_loc) tok = e0 + k2;
-                c2 += (double)wv[k2];
-              }
-            }
-            if (tok < 0) tok = klast;
-          }
-          if (tok < 0) tok = D.amax;  // nothing positive in this slice (degenerate)
-          sm.tok = tok;
+        } else if (lane == 0) {
+          S.kind = 2;  // identically zero residual: draw from p at m
         }
-        __syncthreads();
-        if (threadIdx.x == 0) sm.dec.token = sm.tok;
-      }
-    }
-    __syncthreads();
-
-    // ---- publish (owner CTA): per-position results, keys, counters
-    const Decision &D = sm.dec;
-    if (rank == D.owner && threadIdx.x == 0) {
-      const int64_t pk = (int64_t)I.b * (P.K + 1) + I.j;
-      if (P.mode == kVerify) {
-        if (I.j < P.K) P.pos_accept[pk] = (int8_t)D.accept;
-        P.pos_token[pk] = D.token;
-        if (P.argmax_out) P.argmax_out[pk] = D.amax;
-        if (I.j < P.K && I.sampled) {
-          const int64_t pj = (int64_t)I.b * P.K + I.j;
-          if (P.ratio_out) P.ratio_out[pj] = D.ratio;
-          if (P.p_out) P.p_out[pj] = D.p_d;
-          if (P.q_out) P.q_out[pj] = D.q_d;
-        }
-      }
-      if (I.fan > 0 && P.keys_out) {
-        // merge the cluster's candidate lists
-        float lv = INFINITY;
-        int li = -1;
-        int32_t *kout = P.keys_out + ((int64_t)I.b * P.n_keys_out + P.fan_off[I.j]) * 2;
-        for (int r = 0; r < I.fan; ++r) {
-          float bv = -INFINITY;
-          int bi = INT32_MAX;
-          if (I.need_1) {
-            for (int c = 0; c < cs; ++c) {
-              const Part *pc = &sm.peer[c];
-              for (int x2 = 0; x2 < pc->nc; ++x2) {
-                const float v = pc->cv[x2];
-                const int ix = pc->ci[x2];
-                if (better(lv, li, v, ix) && !(v == lv && ix == li) && better(v, ix, bv, bi)) {
-                  bv = v;
-                  bi = ix;
-                }
-              }
-            }
-          }
-          if (bi == INT32_MAX) {
-            kout[2 * r] = -1;
-            kout[2 * r + 1] = -1;
-          } else {
-            kout[2 * r] = I.j;
-            kout[2 * r + 1] = bi;
-            lv = bv;
-            li = bi;
-          }
-        }
-      }
-      if (P.mode == kVerify) {
-        __threadfence();
-        const int old = atomicAdd(&P.row_counter[I.b], 1);
-        if (old == P.K) {
-          __threadfence();
-          finalize_row(P, I.b);
-          P.row_counter[I.b] = 0;
-          if (P.compact) {
-            __threadfence();
-            const int done = atomicAdd(P.done_counter, 1);
-            if (done == P.B - 1) {
-              __threadfence();
-              sm.flag_compact = 1;
-            }
-          }
-        }
-      }
-    }
-    __syncthreads();
-    if (sm.flag_compact) {
-      compact_block(P.B, P.K, P.out_tokens, P.tau, P.offsets, P.packed, P.status, true, sm.red);
-      if (threadIdx.x == 0) {
-        *P.done_counter = 0;
-        sm.flag_compact = 0;
       }
       __syncthreads();
+      if (residual && S.kind == 2) {
+        cluster.sync();  // peers are done reading this CTA's mass
+        continue;
+      }
+      if (rank == S.cstar) {
+        // the crossing warp: the first whose range passes t_loc, else the
+        // last with mass
+        if (warp == 0) {
+          const double m_l = lane < NW ? S.wmass[lane] : 0.0;
+          const double pre = lane < NW ? S.wpre[lane] : 0.0;
+          const unsigned cross = __ballot_sync(0xffffffffu, m_l > 0.0 && pre + m_l > S.t_loc);
+          const unsigned pos = __ballot_sync(0xffffffffu, m_l > 0.0);
+          const int ws = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : 0);
+          if (lane == 0) {
+            S.wsel = ws;
+            S.t_w = S.t_loc - S.wpre[ws];
+          }
+        }
+        __syncthreads();
+        if (warp == S.wsel) {
+          // masses of this warp's vectors, in index order, into the (now
+          // idle) ring memory; then a chunked scan
+          float *vm_s = reinterpret_cast<float *>(ring);
+          const int nq = wq1 - wq0;
+          for (int base = 0; base < nq; base += 32 * kU) {
+            uint4 tvv[kU], dvv[kU];
+#pragma unroll
+            for (int k = 0; k < kU; ++k) {
+              const int q = wq0 + base + k * 32 + lane;
+              tvv[k] = q < wq1 ? load_vec_direct<E>(Rt, q, v0, v1) : tvv[0];
+              dvv[k] = (q < wq1 && d_vec) ? load_vec_direct<E>(*Rd, q, v0, v1) : tvv[k];
+            }
+#pragma unroll
+            for (int k = 0; k < kU; ++k) {
+              const int q = wq0 + base + k * 32 + lane;
+              if (q < wq1) vm_s[q - wq0] = vec_mass(tvv[k], dvv[k], q, d_vec);
+            }
+          }
+          __syncwarp();
+          const double tw = S.t_w;
+          double cum = 0.0;
+          int qsel = -1;
+          double before = 0.0;
+          int qlast = -1;
+          double before_last = 0.0;
+          for (int base = 0; base < nq && qsel < 0; base += 32) {
+            const int i = base + lane;
+            const double mv = i < nq ? (double)vm_s[i] : 0.0;
+            double incl = mv;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const double y = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += y;
+            }
+            const unsigned cross = __ballot_sync(0xffffffffu, mv > 0.0 && cum + incl > tw);
+            const unsigned pos = __ballot_sync(0xffffffffu, mv > 0.0);
+            if (cross) {
+              const int l = __ffs(cross) - 1;
+              qsel = wq0 + base + l;
+              before = cum + __shfl_sync(0xffffffffu, incl - mv, l);
+            } else if (pos) {
+              const int l = 31 - __clz(pos);
+              qlast = wq0 + base + l;
+              before_last = cum + __shfl_sync(0xffffffffu, incl - mv, l);
+            }
+            cum += __shfl_sync(0xffffffffu, incl, 31);
+          }
+          if (qsel < 0) {  // rounding put the target past this warp's mass
+            qsel = qlast;
+            before = before_last;
+          }
+          if (lane == 0) {
+            int tok = -1, klast = -1;
+            if (qsel >= 0) {
+              float ft[NV], fd[NV], w[NV];
+              Elt<E>::unpack(load_vec_direct<E>(Rt, qsel, v0, v1), ft);
+              if (residual) Elt<E>::unpack(load_vec_direct<E>(*Rd, qsel, v0, v1), fd);
+              if (residual && !d_vec) {
+#pragma unroll
+                for (int i = 0; i < NV; ++i) {
+                  const int e = elem_index(v0, Rt.hp, qsel, i, sz);
+                  fd[i] = (e >= v0 && e < v1) ? Elt<E>::load_global(Rd->g + (int64_t)e * sz)
+                                              : -INFINITY;
+                }
+              }
+              pass_weights<E>(ft, fd, residual, Ct, Cd, s, Rz, w);
+              double c2 = before;
+              for (int i = 0; i < NV; ++i) {
+                const int e = elem_index(v0, Rt.hp, qsel, i, sz);
+                if (e < v0 || e >= v1 || !(w[i] > 0.f)) continue;
+                klast = e;
+                if (tok < 0 && c2 + (double)w[i] > tw) tok = e;
+                c2 += (double)w[i];
+              }
+              if (tok < 0) tok = klast;
+            }
+            if (tok < 0) tok = S.amax[S.trow[mm]];  // degenerate: no mass in this slice
+            S.tok = tok;
+          }
+        }
+        __syncthreads();
+      }
+      break;
+    }
+
+    // ---- the sequence's outputs (owning CTA)
+    if (rank == S.owner && tid == 0) {
+      int32_t *out = P.out_tokens + (int64_t)b * (K + 1);
+      if (!S.valid) {
+        for (int j = 0; j <= K; ++j) out[j] = -1;
+        P.num_accepted[b] = 0;
+        P.tau[b] = 0;
+        if (P.hit) P.hit[b] = 0;
+        if (P.status)
+          atomicOr(P.status, (tvalid ? 0 : (int)SD_STATUS_BAD_TEMP) |
+                                 (dvalid ? 0 : (int)SD_STATUS_BAD_TOKEN));
+      } else {
+        const int mm = S.m, tok = S.tok;
+        for (int j = 0; j < mm; ++j) out[j] = S.d[j];
+        out[mm] = tok;
+        for (int j = mm + 1; j <= K; ++j) out[j] = -1;
+        P.num_accepted[b] = mm;
+        P.tau[b] = mm + 1;
+        if (P.hit) {
+          int h = 0;
+          if (P.keys && P.keys_out) {
+            // written by rank 0 of this cluster before barrier (2), or by
+            // this very CTA when it is rank 0
+            const int32_t *kb = P.keys_out + (int64_t)b * P.n_keys_out * 2;
+            for (int k2 = 0; k2 < P.n_keys_out; ++k2)
+              if (__ldcg(kb + 2 * k2) == mm && __ldcg(kb + 2 * k2 + 1) == tok) h = 1;
+          } else if (P.keys_in) {
+            const int32_t *kb = P.keys_in + (int64_t)b * P.n_keys_in * 2;
+            for (int k2 = 0; k2 < P.n_keys_in; ++k2)
+              if (kb[2 * k2] == mm && kb[2 * k2 + 1] == tok) h = 1;
+          }
+          P.hit[b] = (uint8_t)h;
+        }
+      }
+      if (P.compact) {
+        __threadfence();
+        const int done = atomicAdd(P.done_counter, 1);
+        if (done == P.B - 1) {
+          __threadfence();
+          S.flag_compact = 1;
+        }
+      }
+    }
+    __syncthreads();
+    if (S.flag_compact) {
+      compact_block(P.B, K, P.out_tokens, P.tau, P.offsets, P.packed, P.status, true, S.red_i);
+      if (tid == 0) *P.done_counter = 0;
     }
   }
-
-  // Every issued copy was waited for in the loop; after a wait that gave up,
-  // wait once more (bounded) so that no copy is in flight at exit.
-  if (timed_out && threadIdx.x == 0) {
-    (void)mbar_wait_bounded(&sm.bar[late_stage], late_parity);
-    if (P.status) atomicOr(P.status, (int)SD_STATUS_TIMEOUT);
-  }
-  // peers may still read this CTA's partials
-  cluster.sync();
+  cluster.sync();  // peers may still read this CTA's shared memory
 }
 
 __global__ void sd_compact_kernel(int B, int K, const int32_t *out_tokens, const int32_t *tau,
                                   int32_t *offsets, int32_t *packed, int32_t *status) {
-  __shared__ Red red;
+  __shared__ int red[32];
   compact_block(B, K, out_tokens, tau, offsets, packed, status, false, red);
 }
 
@@ -1261,40 +1383,6 @@ __global__ void sd_uniforms_kernel(uint64_t seed, int n, const int32_t *row, con
 }
 
 // ------------------------------------------------------------------- host --
-struct Plan {
-  int cs, nstage, nt, slice, region, smem, clusters;
-};
-
-static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-struct WsLayout {
-  size_t done, row_counter, pos_token, pos_accept, total;
-};
-static WsLayout ws_layout(int B, int K) {
-  WsLayout L;
-  const size_t n = (size_t)B * (size_t)(K + 1);
-  L.done = 0;
-  L.row_counter = 16;
-  L.pos_token = align_up(L.row_counter + 4 * (size_t)B, 16);
-  L.pos_accept = align_up(L.pos_token + 4 * n, 16);
-  L.total = align_up(L.pos_accept + n, 256);
-  return L;
-}
-
-static const size_t kDynSmemCap = 227 * 1024 - sizeof(Smem) - 256;
-
-template <typename E>
-static void *kernel_ptr() {
-  static std::once_flag once;
-  void *fn = (void *)sd_verify_kernel<E>;
-  std::call_once(once, [fn] {
-    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmemCap);
-    cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    cudaGetLastError();
-  });
-  return fn;
-}
-
 static int env_int(const char *name, int dflt) {
   const char *s = getenv(name);
   return s && *s ? atoi(s) : dflt;
@@ -1311,26 +1399,51 @@ static int sm_count() {
   return n;
 }
 
-static size_t smem_bytes(int nstage, int region, bool cand) {
-  size_t b = (size_t)nstage * 2 * region;      // stages
-  b += (size_t)(region / 16) * 4;              // csum
-  b += (size_t)kCandCap * 8;                   // candidates (always reserved)
-  (void)cand;
-  return align_up(b, 128);
+static const int kDynSmemCap = 227 * 1024 - (int)sizeof(Static) - 256;
+
+template <typename E, int KF, int NT>
+static void *kernel_fn() {
+  static std::once_flag once;
+  void *fn = (void *)sd_seq_kernel<E, KF, NT>;
+  std::call_once(once, [fn] {
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmemCap);
+    cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaGetLastError();
+  });
+  return fn;
 }
 
-// Resident clusters for a configuration (cached).
-static int active_clusters(void *fn, int cs, int nt, size_t smem) {
-  static std::mutex mu;
-  static std::map<std::tuple<void *, int, int, size_t>, int> cache;
-  std::lock_guard<std::mutex> g(mu);
-  auto key = std::make_tuple(fn, cs, nt, smem);
-  auto it = cache.find(key);
-  if (it != cache.end()) return it->second;
+// Rows streamed per sequence (upper bound used for the shared-memory size).
+static int rows_per_seq(const Params &P) {
+  int n = P.mode == kVerify ? 2 * P.K + 1 : P.K;
+  if (P.keys && P.bonus && P.fanout[P.K] > 0) n += 1;
+  return std::max(n, 1);
+}
+
+// Cluster size: slices of at most kMaxSliceVec vectors, then enough CTAs to
+// give every SM two, at most kMaxCS.
+static int choose_cs(int B, int V, int sz) {
+  const int forced = env_int("SDV_CS", 0);
+  if (forced) return forced;
+  int cs = 1;
+  while (cs < kMaxCS && (((int64_t)V + cs - 1) / cs * sz + 31) / 16 + 2 > kMaxSliceVec) cs <<= 1;
+  while (cs < kMaxCS && (int64_t)B * cs < 2LL * sm_count()) cs <<= 1;
+  return cs;
+}
+
+template <typename E, int KF, int NT>
+static sd_status_t launch_nt(Params &P, int cs, cudaStream_t stream) {
+  constexpr int sz = Elt<E>::kSize;
+  P.cs = cs;
+  P.slice = (int)((((int64_t)P.V + cs - 1) / cs + 15) / 16 * 16);
+  const Layout L = make_layout(NT, rows_per_seq(P), KF);
+  if (L.total > kDynSmemCap) return SD_ERR_UNSUPPORTED;
+  void *fn = kernel_fn<E, KF, NT>();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cs * 64, 1, 1);
-  cfg.blockDim = dim3(nt, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3((unsigned)(P.B * cs), 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)L.total;
+  cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
@@ -1338,96 +1451,40 @@ static int active_clusters(void *fn, int cs, int nt, size_t smem) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    n = 0;
-  }
-  cache[key] = n;
-  return n;
-}
-
-template <typename E>
-static bool make_plan(int items, int V, int rows_per_item, Plan &pl) {
-  constexpr int sz = Elt<E>::kSize;
-  (void)rows_per_item;
-  void *fn = kernel_ptr<E>();
-  const int nt = kThreads;
-  const int force_cs = env_int("SDV_CS", 0);
-  const int force_ns = env_int("SDV_NSTAGE", 0);
-  const size_t smem_cap = kDynSmemCap;
-  const int sms = sm_count();
-  int best_cs = -1, best_ns = 1;
-  double best_cost = 1e300;
-  for (int cs = 1; cs <= kMaxCS; cs <<= 1) {
-    if (force_cs && cs != force_cs) continue;
-    const int slice = (int)align_up((size_t)((V + cs - 1) / cs), 16);
-    const int region = (int)align_up((size_t)slice * sz + 32, 128);
-    for (int ns = 1; ns <= 2; ++ns) {
-      if (force_ns && ns != force_ns) continue;
-      const size_t smem = smem_bytes(ns, region, true);
-      if (smem > smem_cap) continue;
-      const int ac = active_clusters(fn, cs, nt, smem);
-      if (ac <= 0) continue;
-      // cost model: waves of items over resident clusters, each item's
-      // slice streamed at the SM's share of bandwidth; a single stage
-      // cannot overlap the next item's copy with this item's reductions.
-      const double waves = (double)((items + ac - 1) / ac);
-      const double per_item = (double)slice * sz * 2.0;  // bytes per CTA per item
-      const double active_frac = (double)std::min(items, ac) * cs / (double)sms;
-      double cost = waves * per_item * (ns == 1 && waves > 1 ? 1.8 : 1.0) /
-                    std::min(1.0, std::max(active_frac, 1e-3));
-      cost += waves * 3000.0;  // per-item fixed latency (syncs), in byte units
-      if (cost < best_cost * 0.999) {
-        best_cost = cost;
-        best_cs = cs;
-        best_ns = ns;
-      }
-    }
-  }
-  if (best_cs < 0) return false;
-  pl.cs = best_cs;
-  pl.nstage = best_ns;
-  pl.nt = nt;
-  pl.slice = (int)align_up((size_t)((V + best_cs - 1) / best_cs), 16);
-  pl.region = (int)align_up((size_t)pl.slice * sz + 32, 128);
-  pl.smem = (int)smem_bytes(pl.nstage, pl.region, true);
-  const int ac = active_clusters(fn, pl.cs, nt, pl.smem);
-  pl.clusters = std::max(1, std::min(items, ac));
-  return true;
-}
-
-template <typename E>
-static sd_status_t launch(Params &P, cudaStream_t stream) {
-  Plan pl;
-  const int rows = 2;
-  if (!make_plan<E>(P.n_items, P.V, rows, pl)) return SD_ERR_UNSUPPORTED;
-  P.cs = pl.cs;
-  P.nstage = pl.nstage;
-  P.slice = pl.slice;
-  P.region = pl.region;
-  void *fn = kernel_ptr<E>();
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.clusters * pl.cs, 1, 1);
-  cfg.blockDim = dim3(pl.nt, 1, 1);
-  cfg.dynamicSmemBytes = pl.smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = pl.cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (env_int("SDV_VERBOSE", 0))
-    fprintf(stderr, "sd_verify plan: mode=%d items=%d cs=%d nstage=%d nt=%d slice=%d smem=%d clusters=%d\n",
-            P.mode, P.n_items, pl.cs, pl.nstage, pl.nt, pl.slice, pl.smem, pl.clusters);
+    fprintf(stderr, "sd_verify: mode=%d B=%d K=%d V=%d cs=%d NT=%d slice=%d KF=%d smem=%d\n",
+            P.mode, P.B, P.K, P.V, cs, NT, P.slice, KF, L.total);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, (void (*)(const Params))fn, P);
   if (e != cudaSuccess) {
     fprintf(stderr, "sd_verify launch failed: %s\n", cudaGetErrorString(e));
     return SD_ERR_CUDA;
   }
   return SD_OK;
+}
+
+// 512-thread CTAs when the grid would leave SMs short of warps.
+template <typename E, int KF>
+static sd_status_t launch_kf(Params &P, cudaStream_t s) {
+  constexpr int sz = Elt<E>::kSize;
+  const int cs = choose_cs(P.B, P.V, sz);
+  if (cs < 1 || cs > kMaxCS) return SD_ERR_INVALID_ARG;
+  int nt = env_int("SDV_NT", 0);
+  if (nt != 256 && nt != 512) nt = 256;
+  return nt == 512 ? launch_nt<E, KF, 512>(P, cs, s) : launch_nt<E, KF, 256>(P, cs, s);
+}
+
+template <typename E>
+static sd_status_t launch(Params &P, cudaStream_t s) {
+  int fmax = 0;
+  if (P.keys)
+    for (int k = 0; k <= P.K; ++k) fmax = std::max(fmax, P.fanout[k]);
+  if (fmax == 0) {
+    P.keys = 0;
+    return launch_kf<E, 0>(P, s);
+  }
+  if (fmax <= 2) return launch_kf<E, 2>(P, s);
+  if (fmax <= 4) return launch_kf<E, 4>(P, s);
+  return launch_kf<E, 8>(P, s);
 }
 
 static sd_status_t dispatch(Params &P, sd_dtype_t dt, cudaStream_t s) {
@@ -1444,7 +1501,7 @@ extern "C" {
 
 size_t sd_verify_workspace_size(int32_t B, int32_t K) {
   if (B < 0 || K < 0 || K > SD_MAX_K) return 0;
-  return ws_layout(B, K).total;
+  return 256;  // one completion counter, padded
 }
 
 sd_status_t sd_verify(const sd_verify_args *a, void *stream) {
@@ -1452,7 +1509,7 @@ sd_status_t sd_verify(const sd_verify_args *a, void *stream) {
   if (a->B < 0 || a->K < 0 || a->K > SD_MAX_K || a->V < 1 || a->V > SD_MAX_V)
     return SD_ERR_INVALID_ARG;
   if (a->dtype != SD_F32 && a->dtype != SD_BF16) return SD_ERR_INVALID_ARG;
-  if ((int64_t)a->B * (a->K + 1) > INT32_MAX) return SD_ERR_INVALID_ARG;
+  if ((int64_t)a->B * kMaxCS > INT32_MAX) return SD_ERR_INVALID_ARG;
   const bool predict = (a->flags & SD_FLAG_PREDICT) != 0;
   const bool compact = (a->flags & SD_FLAG_COMPACT) != 0;
   if (a->flags & ~(SD_FLAG_PREDICT | SD_FLAG_COMPACT)) return SD_ERR_INVALID_ARG;
@@ -1499,6 +1556,7 @@ sd_status_t sd_verify(const sd_verify_args *a, void *stream) {
   P.K = a->K;
   P.V = a->V;
   P.compact = compact ? 1 : 0;
+  P.done_counter = (int32_t *)a->workspace;
   if (predict) {
     if (!a->fanout_host || !a->keys_out) return SD_ERR_INVALID_ARG;
     if (a->draft_bonus_logits && !aligned(a->draft_bonus_logits, esz)) return SD_ERR_INVALID_ARG;
@@ -1519,13 +1577,6 @@ sd_status_t sd_verify(const sd_verify_args *a, void *stream) {
     P.keys_in = a->cache_keys;
     P.n_keys_in = a->cache_keys ? a->n_keys : 0;
   }
-  const WsLayout L = ws_layout(a->B, a->K);
-  uint8_t *ws = (uint8_t *)a->workspace;
-  P.done_counter = (int32_t *)(ws + L.done);
-  P.row_counter = (int32_t *)(ws + L.row_counter);
-  P.pos_token = (int32_t *)(ws + L.pos_token);
-  P.pos_accept = (int8_t *)(ws + L.pos_accept);
-  P.n_items = a->B * (a->K + 1);
   return dispatch(P, a->dtype, s);
 }
 
@@ -1537,6 +1588,7 @@ sd_status_t sd_outcome_predict(int32_t B, int32_t K, int32_t V, sd_dtype_t dtype
   if (B < 0 || K < 0 || K > SD_MAX_K || V < 1 || V > SD_MAX_V) return SD_ERR_INVALID_ARG;
   if (dtype != SD_F32 && dtype != SD_BF16) return SD_ERR_INVALID_ARG;
   if (!fanout_host) return SD_ERR_INVALID_ARG;
+  if ((int64_t)B * kMaxCS > INT32_MAX) return SD_ERR_INVALID_ARG;
   Params P;
   memset(&P, 0, sizeof(P));
   int off = 0;
@@ -1566,7 +1618,6 @@ sd_status_t sd_outcome_predict(int32_t B, int32_t K, int32_t V, sd_dtype_t dtype
   P.B = B;
   P.K = K;
   P.V = V;
-  P.n_items = B * (K + 1);
   return dispatch(P, dtype, (cudaStream_t)stream);
 }
 
@@ -1594,7 +1645,7 @@ sd_status_t sd_uniforms(uint64_t seed, int32_t n, const int32_t *row, const int3
 
 size_t sd_verify_args_size(void) { return sizeof(sd_verify_args); }
 
-const char *sd_version(void) { return "sdverify 0.1 (sm_103a)"; }
+const char *sd_version(void) { return "sdverify 0.2 (sm_103a)"; }
 
 const char *sd_status_string(sd_status_t s) {
   switch (s) {
