@@ -57,8 +57,10 @@ constexpr int kDepth = 3;                    // steps in each thread's copy ring
 constexpr int kMaxWarps = 16;                // threads per CTA <= 512
 constexpr int kMaxCS = 16;                   // cluster size limit
 constexpr int kMaxRows = 2 * SD_MAX_K + 2;   // K+1 target, K draft, 1 bonus
-constexpr int kMaxSliceVec = 4096;           // vectors in one row slice
 constexpr float kRebase = 16.f;              // log2 headroom of the exp offset
+constexpr float kBig = 1048576.f;            // a step sum above 2^20 moves the offset
+constexpr float kL2eHi = 1.44269502162933349609375f;  // log2(e) = hi + lo
+constexpr float kL2eLo = 1.925963033500011e-08f;
 
 enum Mode : int { kVerify = 0, kPredict = 1 };
 enum RowKind : int { kTarget = 0, kDraft = 1, kBonus = 2 };
@@ -116,10 +118,10 @@ __device__ __forceinline__ uint32_t philox_w0(uint64_t seed, uint32_t row, uint3
   return c0;
 }
 
-// u in (0, 1], a multiple of 2^-24: exact in float and double.
-__device__ __forceinline__ double uniform_u(uint64_t seed, int64_t row, int pos, int slot) {
+// u in (0, 1], a multiple of 2^-24: exact in float.
+__device__ __forceinline__ float uniform_u(uint64_t seed, int64_t row, int pos, int slot) {
   const uint32_t x = philox_w0(seed, (uint32_t)row, (uint32_t)pos, (uint32_t)slot);
-  return (double)((x >> 8) + 1u) * (1.0 / 16777216.0);
+  return (float)((x >> 8) + 1u) * 5.9604644775390625e-8f;
 }
 
 // ------------------------------------------------------------- primitives --
@@ -131,15 +133,79 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 2^d for a double d without a double-precision transcendental: the integer
-// part goes into the float exponent, the fraction (exact in double) through
-// ex2 (relative error about 2^-22).  Results below the normal range are 0.
-__device__ __forceinline__ float exp2_split(double d) {
-  if (!(d > -126.0)) return 0.f;
-  if (d >= 128.0) return INFINITY;
-  const double n = floor(d);
-  const float y = ex2((float)(d - n));  // in [1, 2)
-  return __int_as_float(__float_as_int(y) + ((int)n << 23));
+// ---------------------------------------------- float-float arithmetic --
+// Sums and products carried as an unevaluated pair hi + lo: Knuth's two-sum,
+// Dekker's fast two-sum (|a| >= |b|) and the fma form of the exact product,
+// about 48 significant bits on the fp32 pipe.  (The fp64 pipe of this part
+// is slow enough that a handful of dependent double operations costs
+// microseconds.)
+struct ff {
+  float hi, lo;
+};
+__device__ __forceinline__ ff two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  return ff{s, (a - (s - bb)) + (b - bb)};
+}
+__device__ __forceinline__ ff fast_two_sum(float a, float b) {
+  const float s = a + b;
+  return ff{s, b - (s - a)};
+}
+__device__ __forceinline__ ff two_prod(float a, float b) {
+  const float p = a * b;
+  return ff{p, fmaf(a, b, -p)};
+}
+__device__ __forceinline__ ff ff_add(ff x, ff y) {
+  const ff t = two_sum(x.hi, y.hi);
+  return fast_two_sum(t.hi, t.lo + (x.lo + y.lo));
+}
+__device__ __forceinline__ ff ff_add_f(ff x, float y) {
+  const ff t = two_sum(x.hi, y);
+  return fast_two_sum(t.hi, t.lo + x.lo);
+}
+__device__ __forceinline__ ff ff_sub(ff x, ff y) { return ff_add(x, ff{-y.hi, -y.lo}); }
+__device__ __forceinline__ ff ff_mul_f(ff x, float y) {
+  const ff p = two_prod(x.hi, y);
+  return fast_two_sum(p.hi, fmaf(x.lo, y, p.lo));
+}
+__device__ __forceinline__ bool ff_gt(ff x, ff y) {
+  return x.hi > y.hi || (x.hi == y.hi && x.lo > y.lo);
+}
+__device__ __forceinline__ bool ff_pos(ff x) { return x.hi > 0.f; }
+__device__ __forceinline__ float ff_f(ff x) { return x.hi + x.lo; }
+__device__ __forceinline__ ff ff_shfl(ff x, int src) {
+  return ff{__shfl_sync(0xffffffffu, x.hi, src), __shfl_sync(0xffffffffu, x.lo, src)};
+}
+__device__ __forceinline__ ff ff_shfl_up(ff x, int o) {
+  return ff{__shfl_up_sync(0xffffffffu, x.hi, o), __shfl_up_sync(0xffffffffu, x.lo, o)};
+}
+__device__ __forceinline__ ff ff_shfl_xor(ff x, int o) {
+  return ff{__shfl_xor_sync(0xffffffffu, x.hi, o), __shfl_xor_sync(0xffffffffu, x.lo, o)};
+}
+// inclusive warp scan and warp sum
+__device__ __forceinline__ ff ff_warp_scan(ff x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const ff y = ff_shfl_up(x, o);
+    if (lane >= o) x = ff_add(x, y);
+  }
+  return x;
+}
+__device__ __forceinline__ ff ff_warp_sum(ff x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = ff_add(x, ff_shfl_xor(x, o));
+  return x;
+}
+
+// 2^(x.hi + x.lo) without a double-precision transcendental: the integer
+// part of hi scales the result exactly, the fraction (hi - n exact, plus
+// lo) goes through ex2 (relative error about 2^-22).  Below 2^-126: 0.
+__device__ __forceinline__ float exp2_ff(ff x) {
+  if (!(x.hi > -126.f)) return 0.f;
+  if (x.hi >= 128.f) return INFINITY;
+  const float n = floorf(x.hi);
+  return ldexpf(ex2((x.hi - n) + x.lo), (int)n);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -182,44 +248,44 @@ __device__ __forceinline__ int warp_min_i(int v) {
   for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+
+// ------------------------------------------------------ packed fp32 pairs --
+// Two fp32 lanes per instruction (fma / add on a 64-bit register pair).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
-// Order of (value, index) candidates: larger value first, then lower index.
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
+// Order-preserving integer image of a float (-0 taken as +0), so warp-wide
+// float minima and maxima run as single integer reductions.
+__device__ __forceinline__ int ford(float x) {
+  const int i = __float_as_int(x);
+  return i >= 0 ? i : (i == (int)0x80000000 ? 0 : (i ^ 0x7fffffff));
 }
+__device__ __forceinline__ float fdeord(int i) { return __int_as_float(i >= 0 ? i : (i ^ 0x7fffffff)); }
+__device__ __forceinline__ float rmax_f(float x) { return fdeord(__reduce_max_sync(0xffffffffu, ford(x))); }
+__device__ __forceinline__ float rmin_f(float x) { return fdeord(__reduce_min_sync(0xffffffffu, ford(x))); }
+__device__ __forceinline__ int rmin_i(int x) { return __reduce_min_sync(0xffffffffu, x); }
 
-// Warp-wide best (value desc, index asc) of one candidate per lane.
+// Warp-wide best (value desc, then index asc) of one candidate per lane.
 __device__ __forceinline__ void warp_best(float &v, int &i) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    if (better(ov, oi, v, i)) {
-      v = ov;
-      i = oi;
-    }
-  }
-}
-
-// Bitonic sort of one value per lane, descending; returns this lane's value.
-__device__ __forceinline__ float warp_sort_desc(float v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const float o = __shfl_xor_sync(0xffffffffu, v, j);
-      const bool up = ((lane & k) == 0);
-      const bool lower = ((lane & j) == 0);
-      v = (lower == up) ? fmaxf(v, o) : fminf(v, o);
-    }
-  }
-  return v;
+  const float mv = rmax_f(v);
+  i = rmin_i(v == mv ? i : INT32_MAX);
+  v = mv;
 }
 
 // --------------------------------------------------------- element types --
@@ -275,22 +341,25 @@ struct Elt<__nv_bfloat16> {
 };
 
 // ---------------------------------------------------------------- rows ----
+// What a row's stream computes: exp-sums (E), argmax (A), key vectors (K).
+enum RowType : int { kRowE = 0, kRowEA = 1, kRowA = 2, kRowK = 3, kRowEK = 4 };
+
 // One logit row as this CTA sees it: the slice [v0, v1) occupies `nvec`
 // 16-byte vectors starting at `gbase`, the 16-byte boundary at or below
 // element v0 (element v0 sits `hp` bytes into vector 0).  Vectors in
 // [qlo, qhi) lie wholly inside the slice and are copied with cp.async; the
 // (at most two) others are assembled from element loads with -inf in the
 // bytes outside the slice, so every vector a thread sees is a plain list of
-// logits with -inf padding.  `qd` is the vector holding the token excluded
-// from this row's keys (-1 if it is not in this slice).
+// logits with -inf padding.  Step t covers vectors [t NT kU, (t+1) NT kU);
+// steps [sf0, sf1) lie wholly inside [qlo, qhi).  `qd` is the vector holding
+// the token excluded from this row's keys (-1 if it is not in this slice).
 struct RowInfo {
   const uint8_t *g;      // element 0 of the row
   const uint8_t *gbase;  // 16-byte boundary at or below element v0
-  int kind, j;           // RowKind, position
-  int flags;             // RowFlag bits
+  int kind, j, type;     // RowKind, position, RowType
   int excl;              // token excluded from the keys (-1: none)
   int fan;               // keys wanted from this row
-  int hp, nvec, nsteps, qlo, qhi, qd;
+  int hp, nvec, nsteps, qlo, qhi, sf0, sf1, qd, qd_step;
 };
 
 // Element index of element i of slice vector q.
@@ -302,8 +371,8 @@ template <int NT>
 __device__ __forceinline__ void row_geometry(RowInfo &R, int v0, int v1, int sz) {
   constexpr int kStepVec = NT * kU;
   R.gbase = R.g;
-  R.hp = R.nvec = R.nsteps = R.qlo = R.qhi = 0;
-  R.qd = -1;
+  R.hp = R.nvec = R.nsteps = R.qlo = R.qhi = R.sf0 = R.sf1 = 0;
+  R.qd = R.qd_step = -1;
   if (v1 <= v0) return;
   const uintptr_t a0 = (uintptr_t)(R.g + (int64_t)v0 * sz);
   const uintptr_t a1 = (uintptr_t)(R.g + (int64_t)v1 * sz);
@@ -314,11 +383,16 @@ __device__ __forceinline__ void row_geometry(RowInfo &R, int v0, int v1, int sz)
   R.nsteps = (R.nvec + kStepVec - 1) / kStepVec;
   R.qlo = R.hp == 0 ? 0 : 1;
   R.qhi = (a1 & 15) == 0 ? R.nvec : R.nvec - 1;
-  if (R.excl >= v0 && R.excl < v1) R.qd = ((R.excl - v0) * sz + R.hp) / 16;
+  R.sf0 = R.qlo > 0 ? 1 : 0;
+  R.sf1 = umax(R.sf0, R.qhi / kStepVec);
+  if (R.excl >= v0 && R.excl < v1) {
+    R.qd = ((R.excl - v0) * sz + R.hp) / 16;
+    R.qd_step = R.qd / kStepVec;
+  }
 }
 
-// Vector q of row R's slice assembled from element loads (ragged ends, or
-// -inf past the slice).
+// Vector q of row R's slice assembled from element loads (ragged ends), or
+// all -inf past the slice.
 template <typename E>
 __device__ __noinline__ uint4 load_vec_slow(const RowInfo &R, int q, int v0, int v1) {
   constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec;
@@ -342,27 +416,26 @@ __device__ __noinline__ uint4 load_vec_slow(const RowInfo &R, int q, int v0, int
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Vector q of row R's slice read directly (128-bit load when it lies inside
-// the slice), -inf past `R.nvec`.
+// Vector q of row R's slice read directly (128-bit load through L2 when it
+// lies inside the slice).
 template <typename E>
 __device__ __forceinline__ uint4 load_vec_direct(const RowInfo &R, int q, int v0, int v1) {
-  if (q >= R.qlo && q < R.qhi) return ld_stream(R.gbase + 16 * q);
+  if (q >= R.qlo && q < R.qhi) return __ldcg(reinterpret_cast<const uint4 *>(R.gbase + 16 * q));
   return load_vec_slow<E>(R, q, v0, v1);
 }
 
-// One 16-byte vector q (< qend) of row R into this thread's k-th slot of
-// ring slot `slot`; ragged ends are read when consumed.
+// One 16-byte vector q (< qend) of row R into this thread's k-th slot of a
+// ring slot (`slot`: shared address of this thread's vector 0 there); the
+// ragged ends are read when consumed.
 template <int NT>
-__device__ __forceinline__ void issue_vec(const RowInfo &R, int q, int qend, uint32_t ring,
-                                          int slot, int k) {
-  if (q < qend && q >= R.qlo && q < R.qhi)
-    cp_async16(ring + (uint32_t)(((slot * kU + k) * NT + threadIdx.x) * 16), R.gbase + 16 * q);
+__device__ __forceinline__ void issue_vec(const RowInfo &R, int q, int qend, uint32_t slot, int k) {
+  if (q < qend && q >= R.qlo && q < R.qhi) cp_async16(slot + k * NT * 16, R.gbase + 16 * q);
 }
 template <typename E, int NT>
-__device__ __forceinline__ uint4 fetch_vec(const RowInfo &R, int q, int qend, const uint8_t *ring,
-                                           int slot, int k, int v0, int v1) {
+__device__ __forceinline__ uint4 fetch_vec(const RowInfo &R, int q, int qend, const uint8_t *slot,
+                                           int k, int v0, int v1) {
   if (q < qend && q >= R.qlo && q < R.qhi)
-    return *reinterpret_cast<const uint4 *>(ring + ((slot * kU + k) * NT + threadIdx.x) * 16);
+    return *reinterpret_cast<const uint4 *>(slot + k * NT * 16);
   if (q >= qend || q >= R.nvec) {
     const uint32_t w = Elt<E>::kNegInfWord;
     return make_uint4(w, w, w, w);
@@ -370,98 +443,131 @@ __device__ __forceinline__ uint4 fetch_vec(const RowInfo &R, int q, int qend, co
   return load_vec_slow<E>(R, q, v0, v1);
 }
 
-// Each thread copies its own kU vectors of one step of row R into its own
-// slots of ring slot `slot` (vectors inside the slice only).
-template <int NT>
-__device__ __forceinline__ void issue_unit(const RowInfo &R, int step, uint32_t ring, int slot) {
-  constexpr int kStepVec = NT * kU;
-#pragma unroll
-  for (int k = 0; k < kU; ++k) {
-    const int q = step * kStepVec + threadIdx.x + k * NT;
-    if (q >= R.qlo && q < R.qhi)
-      cp_async16(ring + (uint32_t)(((slot * kU + k) * NT + threadIdx.x) * 16), R.gbase + 16 * q);
-  }
-}
-// Vector k of this thread's part of one step: from the ring, or assembled.
-template <typename E, int NT>
-__device__ __forceinline__ uint4 unit_vec(const RowInfo &R, int step, int k, const uint8_t *ring,
-                                          int slot, int v0, int v1) {
-  constexpr int kStepVec = NT * kU;
-  const int q = step * kStepVec + threadIdx.x + k * NT;
-  if (q >= R.qlo && q < R.qhi)
-    return *reinterpret_cast<const uint4 *>(ring + ((slot * kU + k) * NT + threadIdx.x) * 16);
-  if (q >= R.nvec) {  // past the slice
-    const uint32_t w = Elt<E>::kNegInfWord;
-    return make_uint4(w, w, w, w);
-  }
-  return load_vec_slow<E>(R, q, v0, v1);
-}
-
 // -------------------------------------------------------- shared memory --
-// Dynamic shared memory carve-out (byte offsets), identical on host and
-// device.  nrows: rows streamed per sequence; KF: keys kept per row.
-struct Layout {
-  int ring, wstat, wtop, part_m, part_i, part_c, part_z, part_tv, part_ti, total;
-};
-__host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
-__host__ __device__ inline Layout make_layout(int NT, int nrows, int KF) {
-  const int nw = NT / 32;
-  Layout L;
-  int o = 0;
-  L.ring = o;                                    // [kDepth][kU][NT] 16-byte slots
-  o = align128(o + kDepth * kU * NT * 16);
-  L.wstat = o;                                   // [nrows][nw] WStat
-  o = align128(o + 16 * nrows * nw);
-  L.wtop = o;                                    // [nrows][nw][KF] {v, i}
-  o = align128(o + 8 * nrows * nw * KF);
-  L.part_m = o;                                  // [nrows] float
-  o = align128(o + 4 * nrows);
-  L.part_i = o;                                  // [nrows] int
-  o = align128(o + 4 * nrows);
-  L.part_c = o;                                  // [nrows] float
-  o = align128(o + 4 * nrows);
-  L.part_z = o;                                  // [nrows] double
-  o = align128(o + 8 * nrows);
-  L.part_tv = o;                                 // [nrows][KF] float
-  o = align128(o + 4 * nrows * KF);
-  L.part_ti = o;                                 // [nrows][KF] int
-  o = align128(o + 4 * nrows * KF);
-  L.total = o;
-  return L;
-}
-
-// Warp partial of one row: max, sum z of 2^(l s + c), offset c, argmax.
+// Per-warp statistics of one row: max, sum z of 2^(l s + c), offset c,
+// lowest index of the max.
 struct WStat {
   float m, z, c;
   int idx;
 };
+// Per-CTA statistics of one row, pushed into every CTA of the cluster.
+struct CStat {
+  float m;
+  int idx;
+  float c;
+  float zhi, zlo;  // sum of 2^(l s + c) as a float-float pair
+};
+
+// Dynamic shared memory carve-out (byte offsets), identical on host and
+// device.  nrows: rows streamed per sequence; npos: K + 1 key positions;
+// KF: keys kept per row; cs: cluster size.
+struct Layout {
+  int ring, wstat, wsel, cstat, ckeys, cmass, pmass, pw, total;
+};
+// Steps of 32 kU vectors in one warp's share of a slice of `slice` elements.
+__host__ __device__ inline int pass_steps(int slice, int sz, int NT) {
+  const int nvec = (slice * sz + 31) / 16 + 1, nw = NT / 32;
+  return ((nvec + nw - 1) / nw + 32 * kU - 1) / (32 * kU);
+}
+__host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
+__host__ __device__ inline Layout make_layout(int NT, int nrows, int npos, int KF, int cs,
+                                              int slice, int sz) {
+  const int nw = NT / 32, kf = KF > 0 ? KF : 1, kp = KF > 0 ? npos : 0;
+  Layout L;
+  int o = 0;
+  L.ring = o;                                   // [kDepth][kU][NT] 16-byte vectors
+  o = align128(o + kDepth * kU * NT * 16);
+  L.wstat = o;                                  // [nrows][nw] WStat
+  o = align128(o + 16 * nrows * nw);
+  L.wsel = o;                                   // [npos][nw][KF] key vectors chosen by each warp
+  o = align128(o + 4 * kp * nw * kf);
+  L.cstat = o;                                  // [cs][nrows] CStat, slot p written by CTA p
+  o = align128(o + 20 * cs * nrows);
+  L.ckeys = o;                                  // [cs][npos][KF] {value, index}
+  o = align128(o + 8 * cs * kp * kf);
+  L.cmass = o;                                  // [2][cs] float-float: slice masses of the draw
+  o = align128(o + 16 * cs);
+  L.pw = pass_steps(slice, sz, NT);
+  L.pmass = o;                                  // [nw][pw][32] float: masses of the draw
+  o = align128(o + 4 * nw * L.pw * 32);
+  L.total = o;
+  return L;
+}
 
 struct Static {
   RowInfo rows[kMaxRows];
   int trow[SD_MAX_K + 1];  // row slot of target row j
   int drow[SD_MAX_K + 1];  // row slot of draft row j (K: bonus row), -1 if absent
   int nrows;
+  int dvalid;
   int d[SD_MAX_K];         // drafted tokens
   float ld_t[SD_MAX_K];    // target logit of d_j
   float ld_d[SD_MAX_K];    // draft logit of d_j
   float M[kMaxRows];       // combined row statistics: max,
   float C[kMaxRows];       //   offset C: sum over the row of 2^(l s) = Z 2^-C
-  double Z[kMaxRows];
+  ff Z[kMaxRows];
   int amax[kMaxRows];      //   lowest index of the max
+  int2 keys[(SD_MAX_K + 1) * SD_MAX_FANOUT];  // this sequence's keys (fused prediction)
   int m, kind, owner, valid;  // kind: 0 none, 1 residual at m, 2 from p at m
-  double t_loc;
+  ff t_loc;
   int cstar;
-  double s_part;              // this CTA's mass of the sampling pass
-  double wmass[kMaxWarps];    //   per warp (contiguous ranges), and its prefix
-  double wpre[kMaxWarps];
+  ff wmass[kMaxWarps];        // draw: mass of each warp's range, and its prefix
+  ff wpre[kMaxWarps];
   int wsel;                   //   the warp holding the crossing point
-  double t_w;
-  double red_d[kMaxWarps];
+  ff t_w;
   int red_i[kMaxWarps];
   int tok;
   int flag_compact;
 };
 
+// Copy-ahead cursor: the next step this thread copies.
+struct Issuer {
+  const uint8_t *ptr;  // this thread's vector 0 of `step`
+  uint32_t slot;       // shared address of this thread's vector 0 in the slot to fill
+  int row, step, nsteps, sf0, sf1, qlo, qhi;
+};
+
+template <int NT>
+__device__ __forceinline__ void issuer_row(Issuer &I, const Static &S, int nrows) {
+  while (I.row < nrows && S.rows[I.row].nsteps == 0) ++I.row;
+  if (I.row < nrows) {
+    const RowInfo &R = S.rows[I.row];
+    I.step = 0;
+    I.nsteps = R.nsteps;
+    I.sf0 = R.sf0;
+    I.sf1 = R.sf1;
+    I.qlo = R.qlo;
+    I.qhi = R.qhi;
+    I.ptr = R.gbase + 16 * threadIdx.x;
+  }
+}
+
+// Copy one step (kU vectors per thread) into the next ring slot.
+template <int NT>
+__device__ __forceinline__ void issue_step(Issuer &I, const Static &S, int nrows, uint32_t ring_t) {
+  constexpr int kStepVec = NT * kU;
+  constexpr uint32_t kSlot = kU * NT * 16;
+  if (I.row < nrows) {
+    if (I.step >= I.sf0 && I.step < I.sf1) {
+#pragma unroll
+      for (int k = 0; k < kU; ++k) cp_async16(I.slot + k * NT * 16, I.ptr + k * NT * 16);
+    } else {
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
+        const int q = I.step * kStepVec + k * NT + (int)threadIdx.x;
+        if (q >= I.qlo && q < I.qhi) cp_async16(I.slot + k * NT * 16, I.ptr + k * NT * 16);
+      }
+    }
+    I.ptr += kStepVec * 16;
+    if (++I.step == I.nsteps) {
+      ++I.row;
+      issuer_row<NT>(I, S, nrows);
+    }
+  }
+  cp_commit();
+  I.slot += kSlot;
+  if (I.slot == ring_t + kDepth * kSlot) I.slot = ring_t;
+}
 // --------------------------------------------------------- finalization --
 // Exclusive scan of tau and packing of out_tokens, one CTA.  `cg_loads`
 // reads values written by other CTAs of the same grid through L2.
@@ -510,7 +616,8 @@ __device__ void compact_block(int B, int K, const int32_t *out_tokens, const int
   if (threadIdx.x == 0) offsets[B] = carry;
 }
 
-// ------------------------------------------------------------ the kernel --
+
+// ------------------------------------------------------------ streaming --
 // Weights of the sampling pass for the elements of one target vector:
 // residual Zt (p - q)+ = max(0, 2^(l s + Ct) - 2^(l' s + Cd) R), R = Zt / Zd,
 // or Zt p = 2^(l s + Ct) for a draw from p.
@@ -551,130 +658,188 @@ struct RowAcc {
   }
 };
 
-// One step of one row: kU vectors per thread.
-template <typename E, int KF, int NT>
-__device__ __forceinline__ void process_step(RowAcc<KF> &A, int flags, int hp, int qd, int excl,
-                                             int step, const uint4 *v, int v0, float s) {
-  constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec;
-  const int qbase = step * (NT * kU) + threadIdx.x;
-  float vm[kU];
-  float gmax = -INFINITY;
+// Sum of 2^(l s + c) over this thread's vectors of one step, two lanes per
+// instruction; vectors k >= kv are skipped unless FULL.
+template <typename E, bool FULL>
+__device__ __forceinline__ float exp_sum(const uint4 (&v)[kU], int kv, uint64_t s2, uint64_t c2) {
+  constexpr int N = Elt<E>::kPerVec;
+  static_assert(kU == 4, "the combine below pairs four vectors");
+  uint64_t acc[kU];
 #pragma unroll
   for (int k = 0; k < kU; ++k) {
-    vm[k] = Elt<E>::vmax(v[k]);
-    gmax = fmaxf(gmax, vm[k]);
-  }
-  if (gmax > A.m) {
-    A.m = gmax;
-    if (flags & kNeedArg) {
-      int kb = kU - 1;
-#pragma unroll
-      for (int k = kU - 1; k >= 0; --k)
-        if (vm[k] == gmax) kb = k;
-#pragma unroll
-      for (int k = 0; k < kU; ++k)
-        if (k == kb) {
-          A.bv = v[k];
-          A.bq = qbase + k * NT;
-        }
-    }
-  }
-  if ((flags & kNeedExp) && gmax > -INFINITY) {
-    const float cg = -(gmax * s);
-    if (A.c == INFINITY) {
-      A.c = cg;
-    } else if (A.c - cg > kRebase) {  // the max rose by more than kRebase (log2)
-      const float f = ex2(cg - A.c);
-      A.z *= f;
-      A.zc *= f;
-      A.c = cg;
-    }
-    float vs[kU];  // independent per-vector sums, then one compensated add
-#pragma unroll
-    for (int k = 0; k < kU; ++k) {
+    acc[k] = 0ull;  // the pair (+0, +0)
+    if (FULL || k < kv) {
       float f[N];
       Elt<E>::unpack(v[k], f);
 #pragma unroll
-      for (int i = 0; i < N; ++i) f[i] = ex2(fmaf(f[i], s, A.c));
-#pragma unroll
-      for (int h = N / 2; h > 0; h >>= 1)
-#pragma unroll
-        for (int i = 0; i < h; ++i) f[i] += f[i + h];
-      vs[k] = f[0];
-    }
-#pragma unroll
-    for (int h = kU / 2; h > 0; h >>= 1)
-#pragma unroll
-      for (int k = 0; k < h; ++k) vs[k] += vs[k + h];
-    kahan_add(A.z, A.zc, vs[0]);
-  }
-  if (KF > 0 && (flags & kNeedKeys)) {
-    // The top-KF elements of a set lie in its top-KF vectors ranked by
-    // (max, index): every vector holding one of them has a max at least the
-    // KF-th value, and at most KF vectors reach it.  Track those vectors.
-#pragma unroll
-    for (int k = 0; k < kU; ++k) {
-      const int q = qbase + k * NT;
-      if (q == qd) {  // the vector holding the excluded token: its max without it
-        float f[N];
-        Elt<E>::unpack(v[k], f);
-        float mm = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < N; ++i)
-          if (elem_index(v0, hp, q, i, sz) != excl) mm = fmaxf(mm, f[i]);
-        vm[k] = mm;
+      for (int i = 0; i < N; i += 2) {
+        float a, b;
+        upk2(fma2(pk2(f[i], f[i + 1]), s2, c2), a, b);
+        const uint64_t e = pk2(ex2(a), ex2(b));
+        acc[k] = i == 0 ? e : add2(acc[k], e);
       }
     }
-    if (step == 0) {  // first step of the row: a warp-wide lower bound
-      const float srt = warp_sort_desc(vm[0]);
-      A.theta = __shfl_sync(0xffffffffu, srt, KF - 1);
+  }
+  float lo, hi;
+  upk2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), lo, hi);
+  return lo + hi;
+}
+
+template <typename E, bool FULL>
+__device__ __forceinline__ float step_max(const uint4 (&v)[kU], int kv, float *vm) {
+  float g = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kU; ++k) {
+    vm[k] = (FULL || k < kv) ? Elt<E>::vmax(v[k]) : -INFINITY;
+    g = fmaxf(g, vm[k]);
+  }
+  return g;
+}
+
+// One step of one row: kU vectors per thread (the first kv of them unless
+// FULL).  EXP: offset exp-sum; ARG: running max and the first vector that
+// reached it; KEYS: the thread's best KF vectors by masked max.
+template <typename E, int KF, int NT, bool EXP, bool ARG, bool KEYS, bool FULL>
+__device__ __forceinline__ void step_body(RowAcc<KF> &A, const uint4 (&v)[kU], int kv, int step,
+                                          int qd_step, int qd, int excl, int v0, int hp, float s,
+                                          uint64_t s2) {
+  constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec;
+  const int qbase = step * (NT * kU) + threadIdx.x;
+  if (ARG || KEYS) {
+    float vm[kU];
+    const float gmax = step_max<E, FULL>(v, kv, vm);
+    if (gmax > A.m) {
+      A.m = gmax;
+      if (ARG) {
+        int kb = kU - 1;
+#pragma unroll
+        for (int k = kU - 1; k >= 0; --k)
+          if (vm[k] == gmax) kb = k;
+#pragma unroll
+        for (int k = 0; k < kU; ++k)
+          if (k == kb) {
+            A.bv = v[k];
+            A.bq = qbase + k * NT;
+          }
+      }
+      if (EXP) {
+        const float cn = -(gmax * s);
+        if (A.c == INFINITY) {
+          A.c = cn;
+        } else if (A.c - cn > kRebase) {  // the max rose by more than kRebase (log2)
+          const float f = ex2(cn - A.c);
+          A.z *= f;
+          A.zc *= f;
+          A.c = cn;
+        }
+      }
     }
+    if (EXP && A.c != INFINITY) kahan_add(A.z, A.zc, exp_sum<E, FULL>(v, kv, s2, pk2(A.c, A.c)));
+    if (KEYS) {
+      // The top-KF elements of a set lie in its top-KF vectors ranked by
+      // (max, index): every vector holding one of them has a max at least the
+      // KF-th value, and at most KF vectors reach it.  Track those vectors.
+      if (step == qd_step) {
 #pragma unroll
-    for (int k = 0; k < kU; ++k) {
-      if (vm[k] > A.kv[KF - 1] && vm[k] >= A.theta) {
-        A.kv[KF - 1] = vm[k];
-        A.kq[KF - 1] = qbase + k * NT;
+        for (int k = 0; k < kU; ++k) {
+          const int q = qbase + k * NT;
+          if (q == qd) {  // the vector holding the excluded token: its max without it
+            float f[N];
+            Elt<E>::unpack(v[k], f);
+            float mm = -INFINITY;
 #pragma unroll
-        for (int x = KF - 1; x > 0; --x) {
-          if (better(A.kv[x], A.kq[x], A.kv[x - 1], A.kq[x - 1])) {
-            const float t1 = A.kv[x];
-            A.kv[x] = A.kv[x - 1];
-            A.kv[x - 1] = t1;
-            const int t2 = A.kq[x];
-            A.kq[x] = A.kq[x - 1];
-            A.kq[x - 1] = t2;
+            for (int i = 0; i < N; ++i)
+              if (elem_index(v0, hp, q, i, sz) != excl) mm = fmaxf(mm, f[i]);
+            vm[k] = mm;
+          }
+        }
+      }
+      if (step == 0) {  // the warp's KF-th best first vector bounds the rest from below
+        const int lane = threadIdx.x & 31;
+        float x = vm[0], th = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < KF; ++r) {
+          th = rmax_f(x);
+          const unsigned w = __ballot_sync(0xffffffffu, x == th);
+          if (lane == __ffs(w) - 1) x = -INFINITY;
+        }
+        A.theta = th;
+      }
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
+        if (vm[k] > A.kv[KF - 1] && vm[k] >= A.theta) {
+          A.kv[KF - 1] = vm[k];
+          A.kq[KF - 1] = qbase + k * NT;
+#pragma unroll
+          for (int x = KF - 1; x > 0; --x) {
+            if (A.kv[x] > A.kv[x - 1]) {  // later vectors lose ties
+              const float t1 = A.kv[x];
+              A.kv[x] = A.kv[x - 1];
+              A.kv[x - 1] = t1;
+              const int t2 = A.kq[x];
+              A.kq[x] = A.kq[x - 1];
+              A.kq[x - 1] = t2;
+            }
           }
         }
       }
     }
+  } else if (EXP) {
+    // Exp-only rows: the offset comes from the first step that has a finite
+    // value and moves only when a step's sum shows a far larger value.
+    if (A.c == INFINITY) {
+      float vm[kU];
+      const float g = step_max<E, FULL>(v, kv, vm);
+      if (g > -INFINITY) A.c = -(g * s);
+    }
+    if (A.c != INFINITY) {
+      float ss = exp_sum<E, FULL>(v, kv, s2, pk2(A.c, A.c));
+      if (!(ss <= kBig)) {
+        float vm[kU];
+        const float cn = -(step_max<E, FULL>(v, kv, vm) * s);
+        if (cn < A.c) {
+          const float f = ex2(cn - A.c);
+          A.z *= f;
+          A.zc *= f;
+          A.c = cn;
+        }
+        ss = exp_sum<E, FULL>(v, kv, s2, pk2(A.c, A.c));
+      }
+      kahan_add(A.z, A.zc, ss);
+    }
   }
 }
 
-// End of a row: warp-level statistics into wstat / wtop.
-template <typename E, int KF>
-__device__ __forceinline__ void row_end(RowAcc<KF> &A, const RowInfo &R, int v0, int v1,
-                                        WStat *ws, float2 *wt) {
+// End of a row: warp statistics into `ws`, the warp's best KF key vectors
+// into wsel[0..KF).
+template <typename E, int KF, bool EXP, bool ARG, bool KEYS>
+__device__ __forceinline__ void row_end(RowAcc<KF> &A, int v0, int hp, WStat *ws, int *wsel) {
   constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec;
   constexpr int KFm = RowAcc<KF>::KFm;
   const int lane = threadIdx.x & 31;
-  const float mw = warp_max(A.m);
-  int idx = INT32_MAX;
-  if ((R.flags & kNeedArg) && A.m == mw && A.m > -INFINITY && A.bq >= 0) {
-    float f[N];
-    Elt<E>::unpack(A.bv, f);
+  WStat st{-INFINITY, 0.f, INFINITY, INT32_MAX};
+  if (ARG) {
+    const float mw = rmax_f(A.m);
+    int idx = INT32_MAX;
+    if (A.m == mw && mw > -INFINITY && A.bq >= 0) {
+      float f[N];
+      Elt<E>::unpack(A.bv, f);
 #pragma unroll
-    for (int i = N - 1; i >= 0; --i)
-      if (f[i] == A.m) idx = elem_index(v0, R.hp, A.bq, i, sz);
+      for (int i = N - 1; i >= 0; --i)
+        if (f[i] == mw) idx = elem_index(v0, hp, A.bq, i, sz);
+    }
+    st.m = mw;
+    st.idx = rmin_i(idx);
   }
-  const int iw = warp_min_i(idx);
-  const bool has = A.z > 0.f;
-  const float cw = -warp_max(has ? -A.c : -INFINITY);  // min offset of the warp
-  const float zt = has ? (A.z - A.zc) * ex2(cw - A.c) : 0.f;
-  const float zw = warp_sum(zt);
-  if (lane == 0) *ws = WStat{mw, zw, cw, iw};
-  if (KF > 0 && (R.flags & kNeedKeys)) {
-    // the warp's best KF vectors, then its best KF elements among them
-    int selq[KFm];
+  if (EXP) {
+    const bool has = A.z > 0.f;
+    const float cw = rmin_f(has ? A.c : INFINITY);  // smallest offset: the largest max
+    const float zt = has ? (A.z - A.zc) * ex2(cw - A.c) : 0.f;
+    st.z = warp_sum(zt);
+    st.c = cw;
+  }
+  if (lane == 0) *ws = st;
+  if (KEYS) {
 #pragma unroll
     for (int r = 0; r < KFm; ++r) {
       float bv = A.kv[0];
@@ -689,67 +854,130 @@ __device__ __forceinline__ void row_end(RowAcc<KF> &A, const RowInfo &R, int v0,
         A.kv[KFm - 1] = -INFINITY;
         A.kq[KFm - 1] = INT32_MAX;
       }
-      selq[r] = bv > -INFINITY ? bq : INT32_MAX;
-    }
-    constexpr int NC = KFm * N;                   // candidate elements
-    constexpr int PER = (NC + 31) / 32;           // per lane
-    float cv[PER];
-    int ci[PER];
-#pragma unroll
-    for (int h = 0; h < PER; ++h) {
-      cv[h] = -INFINITY;
-      ci[h] = INT32_MAX;
-      const int c = lane + 32 * h;
-      if (c < NC) {
-        int qq = INT32_MAX;
-#pragma unroll
-        for (int r = 0; r < KFm; ++r)
-          if (r == c / N) qq = selq[r];
-        if (qq != INT32_MAX) {
-          const int e = elem_index(v0, R.hp, qq, c % N, sz);
-          if (e >= v0 && e < v1 && e != R.excl) {
-            const float x = Elt<E>::load_global(R.g + (int64_t)e * sz);
-            if (x > -INFINITY) {
-              cv[h] = x;
-              ci[h] = e;
-            }
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < KFm; ++r) {
-      int hb = 0;
-#pragma unroll
-      for (int h = 1; h < PER; ++h)
-        if (better(cv[h], ci[h], cv[hb], ci[hb])) hb = h;
-      float bv = -INFINITY;
-      int bi = INT32_MAX;
-#pragma unroll
-      for (int h = 0; h < PER; ++h)
-        if (h == hb) {
-          bv = cv[h];
-          bi = ci[h];
-        }
-      warp_best(bv, bi);
-#pragma unroll
-      for (int h = 0; h < PER; ++h)
-        if (bi != INT32_MAX && ci[h] == bi) {
-          cv[h] = -INFINITY;
-          ci[h] = INT32_MAX;
-        }
-      if (lane == 0) wt[r] = make_float2(bv, __int_as_float(bi));
+      if (lane == 0) wsel[r] = bv > -INFINITY ? bq : INT32_MAX;
     }
   }
   A.reset();
 }
 
+// Stream this CTA's slice of one row: each step first copies the step
+// kDepth-1 ahead (possibly of a later row), then waits for its own copies.
+template <typename E, int KF, int NT, bool EXP, bool ARG, bool KEYS>
+__device__ __forceinline__ void stream_row(RowAcc<KF> &A, const RowInfo &R, Issuer &I,
+                                           const Static &S, int nrows, const uint8_t *ring,
+                                           uint32_t ring_t, uint32_t &c_off, int v0, int v1,
+                                           float s, uint64_t s2, WStat *ws, int *wsel) {
+  constexpr int kStepVec = NT * kU;
+  constexpr uint32_t kSlot = kU * NT * 16;
+  const int nsteps = R.nsteps, sf0 = R.sf0, sf1 = R.sf1, qlo = R.qlo, qhi = R.qhi;
+  const int nvec = R.nvec, qd_step = R.qd_step, qd = R.qd, excl = R.excl, hp = R.hp;
+  for (int step = 0; step < nsteps; ++step) {
+    issue_step<NT>(I, S, nrows, ring_t);
+    cp_wait<kDepth - 1>();  // this step's copies have landed
+    const uint8_t *src = ring + c_off;
+    uint4 v[kU];
+    if (step >= sf0 && step < sf1) {
+#pragma unroll
+      for (int k = 0; k < kU; ++k) v[k] = *reinterpret_cast<const uint4 *>(src + k * NT * 16);
+      step_body<E, KF, NT, EXP, ARG, KEYS, true>(A, v, kU, step, qd_step, qd, excl, v0, hp, s, s2);
+    } else {
+      const int kv = min(kU, (nvec - step * kStepVec + NT - 1) / NT);
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
+        const int q = step * kStepVec + k * NT + (int)threadIdx.x;
+        if (q >= qlo && q < qhi) {
+          v[k] = *reinterpret_cast<const uint4 *>(src + k * NT * 16);
+        } else if (q < nvec) {
+          v[k] = load_vec_slow<E>(R, q, v0, v1);
+        } else {
+          const uint32_t w = Elt<E>::kNegInfWord;
+          v[k] = make_uint4(w, w, w, w);
+        }
+      }
+      step_body<E, KF, NT, EXP, ARG, KEYS, false>(A, v, kv, step, qd_step, qd, excl, v0, hp, s,
+                                                  s2);
+    }
+    c_off += kSlot;
+    if (c_off >= kDepth * kSlot) c_off -= kDepth * kSlot;
+  }
+  row_end<E, KF, EXP, ARG, KEYS>(A, v0, hp, ws, wsel);
+}
+
+// The CTA's best KF elements (value desc, index asc) of key row R from the
+// NW x KF vectors its warps kept, by one warp: the lanes expand the vectors
+// into elements (without the excluded token, -inf and anything outside the
+// slice), then KF rounds of a warp-wide best.  Lane 0 returns them.
 template <typename E, int KF, int NT>
-__global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_constant__ Params P) {
+__device__ __forceinline__ void cta_keys(const RowInfo &R, const int *wsel, int v0, int v1,
+                                         float *outv, int *outi) {
+  constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec, NW = NT / 32;
+  constexpr int NC = NW * KF;
+  constexpr int PER = (NC + 31) / 32;
+  const int lane = threadIdx.x & 31;
+  float cv[PER * N];
+  int ci[PER * N];
+  uint4 x[PER];
+  int qv[PER];
+#pragma unroll
+  for (int h = 0; h < PER; ++h) {
+    const int c = lane + 32 * h;
+    qv[h] = c < NC ? wsel[c] : INT32_MAX;
+    if (qv[h] != INT32_MAX) x[h] = load_vec_direct<E>(R, qv[h], v0, v1);
+  }
+#pragma unroll
+  for (int h = 0; h < PER; ++h) {
+    float f[N];
+    if (qv[h] != INT32_MAX) Elt<E>::unpack(x[h], f);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      cv[h * N + i] = -INFINITY;
+      ci[h * N + i] = INT32_MAX;
+      if (qv[h] != INT32_MAX) {
+        const int e = elem_index(v0, R.hp, qv[h], i, sz);
+        if (e >= v0 && e < v1 && e != R.excl && f[i] > -INFINITY) {
+          cv[h * N + i] = f[i];
+          ci[h * N + i] = e;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < KF; ++r) {
+    float bv = -INFINITY;
+    int bi = INT32_MAX;
+#pragma unroll
+    for (int t = 0; t < PER * N; ++t)
+      if (cv[t] > bv || (cv[t] == bv && ci[t] < bi)) {
+        bv = cv[t];
+        bi = ci[t];
+      }
+    warp_best(bv, bi);
+#pragma unroll
+    for (int t = 0; t < PER * N; ++t)
+      if (bi != INT32_MAX && ci[t] == bi) {
+        cv[t] = -INFINITY;
+        ci[t] = INT32_MAX;
+      }
+    if (lane == 0) {
+      outv[r] = bi == INT32_MAX ? -INFINITY : bv;
+      outi[r] = bi;
+    }
+  }
+}
+
+// ------------------------------------------------------------ the kernel --
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+template <typename E, int KF, int NT>
+__global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ Params P) {
   constexpr int sz = Elt<E>::kSize, NV = Elt<E>::kPerVec;
   constexpr int KFm = KF > 0 ? KF : 1;
   constexpr int NW = NT / 32;
-  constexpr int kStepVec = NT * kU;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int cs = P.cs;
@@ -760,254 +988,275 @@ __global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_const
   __shared__ Static S;
   extern __shared__ __align__(128) uint8_t dyn[];
 
+  // every CTA of the cluster has started before any pushes into its memory
+  cluster_arrive_relaxed();
+
   const int v0 = min(rank * P.slice, P.V);
   const int v1 = min(v0 + P.slice, P.V);
   const bool verify = P.mode == kVerify;
+  // both loads issued before anything waits on either
+  const int d_pre = (warp == 0 && lane < K) ? P.tokens[(int64_t)b * K + (K - 1 - lane)] : -1;
   const float T = verify ? P.temps[b] : 0.f;
   const bool tvalid = !verify || ((T >= 0.f) && (T <= 3.4e38f));  // rejects NaN / inf / < 0
   const bool sampled = verify && tvalid && T > 0.f;
   // scaled logits x = l s with s = log2(e) / T rounded to float; every
   // exponential below uses this same s
-  const float s = sampled ? (float)(1.4426950408889634 / (double)T) : 0.f;
-  const double sd = (double)s;
-
-  // ---- drafted tokens
-  int dvalid_local = 1;
-  int my_d = -1;
-  for (int j = tid; j < K; j += NT) {
-    const int d = P.tokens[(int64_t)b * K + j];
-    S.d[j] = d;
-    if (!(d >= 0 && d < P.V)) dvalid_local = 0;
-    if (j == tid) my_d = d;
+  float s = 0.f;
+  if (sampled) {  // log2(e) = kL2eHi + kL2eLo, divided with one correction step
+    const float q = __fdiv_rn(kL2eHi, T);
+    s = q + __fdiv_rn(fmaf(-q, T, kL2eHi) + kL2eLo, T);
   }
-  const bool dvalid = __syncthreads_and(dvalid_local) != 0;
+  const bool has_bonus = P.keys && P.bonus && P.fanout[K] > 0;
 
-  // ---- the rows this CTA streams, in order (bonus, K, then K-1..0)
-  if (tid == 0) {
-    int n = 0;
-    const int64_t V = P.V;
-    for (int j = 0; j <= K; ++j) {
-      S.trow[j] = -1;
+  // ---- the rows this CTA streams, in order: bonus, target K, then
+  // (draft j, target j) for j = K-1..0.  Lane l of warp 0 places position
+  // j = K-1-l; warp 1 the bonus row and target row K.
+  float my_lt = -INFINITY, my_ld = -INFINITY;  // logits at d_j (lane j of warp 0)
+  const int base = (has_bonus ? 1 : 0) + (verify ? 1 : 0);
+  if (warp == 0) {
+    const int l = lane, j = K - 1 - l;
+    const bool act = l < K;
+    const int fj = (act && P.keys) ? P.fanout[j] : 0;
+    const bool dpres = act && (sampled || fj > 0);
+    const unsigned dm = __ballot_sync(0xffffffffu, dpres);
+    const int d = d_pre;
+    if (act) S.d[j] = d;
+    const bool dok = !act || (d >= 0 && d < P.V);
+    const bool dvalid = __all_sync(0xffffffffu, dok);
+    const int r_d = base + __popc(dm & ((1u << l) - 1u)) + (verify ? l : 0);
+    const int r_t = r_d + (dpres ? 1 : 0);
+    if (dpres) {
+      RowInfo &R = S.rows[r_d];
+      R.g = P.draft + ((int64_t)b * K + j) * P.V * sz;
+      R.kind = kDraft;
+      R.j = j;
+      R.type = sampled ? (fj > 0 ? kRowEK : kRowE) : kRowK;
+      R.excl = d;
+      R.fan = fj;
+      row_geometry<NT>(R, v0, v1, sz);
+      S.drow[j] = r_d;
+    } else if (act) {
       S.drow[j] = -1;
     }
-    auto add = [&](const uint8_t *g, int kind, int j, int flags, int excl, int fan) {
-      RowInfo &R = S.rows[n];
-      R.g = g;
-      R.kind = kind;
+    if (act && verify) {
+      RowInfo &R = S.rows[r_t];
+      R.g = P.target + ((int64_t)b * (K + 1) + j) * P.V * sz;
+      R.kind = kTarget;
       R.j = j;
-      R.flags = flags;
-      R.excl = excl;
-      R.fan = fan;
+      R.type = sampled ? (P.argmax_out ? kRowEA : kRowE) : kRowA;
+      R.excl = -1;
+      R.fan = 0;
       row_geometry<NT>(R, v0, v1, sz);
-      if (kind == kTarget) S.trow[j] = n;
-      else S.drow[j] = n;
-      ++n;
-    };
-    const int fK = P.keys ? P.fanout[K] : 0;
-    if (fK > 0 && P.bonus) add(P.bonus + (int64_t)b * V * sz, kBonus, K, kNeedKeys, -1, fK);
-    if (verify)
-      add(P.target + ((int64_t)b * (K + 1) + K) * V * sz, kTarget, K,
-          kNeedArg | (sampled ? kNeedExp : 0), -1, 0);
-    for (int j = K - 1; j >= 0; --j) {
-      const int fj = P.keys ? P.fanout[j] : 0;
-      if (sampled || fj > 0)
-        add(P.draft + ((int64_t)b * K + j) * V * sz, kDraft, j,
-            (sampled ? kNeedExp : 0) | (fj > 0 ? kNeedKeys : 0), S.d[j], fj);
-      if (verify)
-        add(P.target + ((int64_t)b * (K + 1) + j) * V * sz, kTarget, j,
-            kNeedArg | (sampled ? kNeedExp : 0), -1, 0);
+      S.trow[j] = r_t;
     }
-    S.nrows = n;
-    S.flag_compact = 0;
+    if (act && sampled && dvalid) {
+      my_lt = Elt<E>::load_global(P.target + (((int64_t)b * (K + 1) + j) * P.V + d) * sz);
+      my_ld = Elt<E>::load_global(P.draft + (((int64_t)b * K + j) * P.V + d) * sz);
+    }
+    if (lane == 0) {
+      S.nrows = base + __popc(dm) + (verify ? K : 0);
+      S.dvalid = dvalid ? 1 : 0;
+      S.flag_compact = 0;
+    }
+  } else if (warp == 1 && lane < 2) {
+    if (lane == 0 && has_bonus) {
+      RowInfo &R = S.rows[0];
+      R.g = P.bonus + (int64_t)b * P.V * sz;
+      R.kind = kBonus;
+      R.j = K;
+      R.type = kRowK;
+      R.excl = -1;
+      R.fan = P.fanout[K];
+      row_geometry<NT>(R, v0, v1, sz);
+      S.drow[K] = 0;
+    } else if (lane == 0) {
+      S.drow[K] = -1;
+    }
+    if (lane == 1 && verify) {
+      RowInfo &R = S.rows[has_bonus ? 1 : 0];
+      R.g = P.target + ((int64_t)b * (K + 1) + K) * P.V * sz;
+      R.kind = kTarget;
+      R.j = K;
+      R.type = sampled ? (P.argmax_out ? kRowEA : kRowE) : kRowA;
+      R.excl = -1;
+      R.fan = 0;
+      row_geometry<NT>(R, v0, v1, sz);
+      S.trow[K] = has_bonus ? 1 : 0;
+    }
   }
   __syncthreads();
-
-  // the logits at the drafted tokens: loaded now, used after the stream
-  float my_lt = -INFINITY, my_ld = -INFINITY;
-  if (tid < K && sampled && my_d >= 0 && my_d < P.V) {
-    my_lt = Elt<E>::load_global(P.target + (((int64_t)b * (K + 1) + tid) * P.V + my_d) * sz);
-    my_ld = Elt<E>::load_global(P.draft + (((int64_t)b * K + tid) * P.V + my_d) * sz);
-  }
 
   const int nrows = S.nrows;
-  const Layout L = make_layout(NT, nrows, KF);
+  const int npos = K + 1;
+  const Layout L = make_layout(NT, nrows, npos, KF, cs, P.slice, sz);
   uint8_t *ring = dyn + L.ring;
-  const uint32_t ring_s = smem_u32(ring);
+  const uint32_t ring_t = smem_u32(ring) + tid * 16;
   WStat *wstat = reinterpret_cast<WStat *>(dyn + L.wstat);
-  float2 *wtop = reinterpret_cast<float2 *>(dyn + L.wtop);  // .x value, .y index bits
-  float *part_m = reinterpret_cast<float *>(dyn + L.part_m);
-  int *part_i = reinterpret_cast<int *>(dyn + L.part_i);
-  float *part_c = reinterpret_cast<float *>(dyn + L.part_c);
-  double *part_z = reinterpret_cast<double *>(dyn + L.part_z);
-  float *part_tv = reinterpret_cast<float *>(dyn + L.part_tv);
-  int *part_ti = reinterpret_cast<int *>(dyn + L.part_ti);
+  int *wsel = reinterpret_cast<int *>(dyn + L.wsel);
+  CStat *cstat = reinterpret_cast<CStat *>(dyn + L.cstat);
+  float2 *ckeys = reinterpret_cast<float2 *>(dyn + L.ckeys);  // .x value, .y index bits
+  ff *cmass = reinterpret_cast<ff *>(dyn + L.cmass);
+  float *pmass = reinterpret_cast<float *>(dyn + L.pmass);
 
-  // ---- stream every row once.  Each thread copies its own vectors
-  // kDepth-1 steps ahead into its own ring slots (cp.async).
-  int total = 0;
-  for (int r = 0; r < nrows; ++r) total += S.rows[r].nsteps;
-  RowAcc<KF> A;
-  A.reset();
-  auto advance = [&](int &row, int &step) {
-    ++step;
-    while (row < nrows && step >= S.rows[row].nsteps) {
-      ++row;
-      step = 0;
-    }
-  };
-  int i_row = 0, i_step = 0;  // next step to copy
-  while (i_row < nrows && S.rows[i_row].nsteps == 0) ++i_row;
-  int c_row = i_row, c_step = 0;  // step being consumed
-  auto issue_next = [&](int slot) {
-    if (i_row < nrows) {
-      issue_unit<NT>(S.rows[i_row], i_step, ring_s, slot);
-      advance(i_row, i_step);
-    }
-    cp_commit();
-  };
+  // ---- stream every row once
+  {
+    const uint64_t s2 = pk2(s, s);
+    Issuer I;
+    I.row = 0;
+    I.slot = ring_t;
+    issuer_row<NT>(I, S, nrows);
 #pragma unroll
-  for (int d = 0; d < kDepth - 1; ++d) issue_next(d);
-  for (int st = 0; st < total; ++st) {
-    issue_next((st + kDepth - 1) % kDepth);
-    cp_wait<kDepth - 1>();  // this step's copies have landed
-    const RowInfo &R = S.rows[c_row];
-    const int flags = R.flags, hp = R.hp, qd = R.qd, excl = R.excl, nsteps = R.nsteps;
-    uint4 cur[kU];
-#pragma unroll
-    for (int k = 0; k < kU; ++k)
-      cur[k] = unit_vec<E, NT>(R, c_step, k, ring, st % kDepth, v0, v1);
-    process_step<E, KF, NT>(A, flags, hp, qd, excl, c_step, cur, v0, s);
-    if (c_step == nsteps - 1)
-      row_end<E, KF>(A, S.rows[c_row], v0, v1, &wstat[c_row * NW + warp],
-                     &wtop[(c_row * NW + warp) * KFm]);
-    advance(c_row, c_step);
+    for (int d = 0; d < kDepth - 1; ++d) issue_step<NT>(I, S, nrows, ring_t);
+    uint32_t c_off = tid * 16;
+    RowAcc<KF> A;
+    A.reset();
+    for (int r = 0; r < nrows; ++r) {
+      const RowInfo &R = S.rows[r];
+      WStat *ws = &wstat[r * NW + warp];
+      int *wk = &wsel[(R.j * NW + warp) * KFm];
+      if (R.nsteps == 0) {  // this CTA holds none of the row
+        if (lane == 0) *ws = WStat{-INFINITY, 0.f, INFINITY, INT32_MAX};
+        if (KF > 0 && (R.type == kRowK || R.type == kRowEK) && lane < KFm) wk[lane] = INT32_MAX;
+        continue;
+      }
+      switch (R.type) {
+        case kRowE:
+          stream_row<E, KF, NT, true, false, false>(A, R, I, S, nrows, ring, ring_t, c_off, v0, v1,
+                                                   s, s2, ws, wk);
+          break;
+        case kRowEA:
+          stream_row<E, KF, NT, true, true, false>(A, R, I, S, nrows, ring, ring_t, c_off, v0, v1,
+                                                  s, s2, ws, wk);
+          break;
+        case kRowA:
+          stream_row<E, KF, NT, false, true, false>(A, R, I, S, nrows, ring, ring_t, c_off, v0,
+                                                   v1, s, s2, ws, wk);
+          break;
+        default:
+          if (KF > 0) {
+            if (R.type == kRowK)
+              stream_row<E, KF, NT, false, false, (KF > 0)>(A, R, I, S, nrows, ring, ring_t, c_off,
+                                                            v0, v1, s, s2, ws, wk);
+            else
+              stream_row<E, KF, NT, true, false, (KF > 0)>(A, R, I, S, nrows, ring, ring_t, c_off,
+                                                           v0, v1, s, s2, ws, wk);
+          }
+          break;
+      }
+    }
+    cp_wait<0>();
   }
-  cp_wait<0>();
-
-  // rows with an empty slice (this CTA holds no vocabulary) still need entries
-  if (total == 0) {
-    for (int x = tid; x < nrows * NW; x += NT) wstat[x] = WStat{-INFINITY, 0.f, INFINITY, INT32_MAX};
-    if (KF > 0)
-      for (int x = tid; x < nrows * NW * KFm; x += NT)
-        wtop[x] = make_float2(-INFINITY, __int_as_float(INT32_MAX));
-  }
-  if (tid < K) {
-    S.ld_t[tid] = my_lt;
-    S.ld_d[tid] = my_ld;
+  if (warp == 0 && lane < K) {
+    S.ld_t[lane] = my_lt;  // lane l holds position K-1-l
+    S.ld_d[lane] = my_ld;
   }
   __syncthreads();
 
-  // ---- CTA statistics per row (one warp per row)
-  for (int r = warp; r < nrows; r += NW) {
-    const RowInfo &R = S.rows[r];
-    const WStat wsl = lane < NW ? wstat[r * NW + lane] : WStat{-INFINITY, 0.f, INFINITY, INT32_MAX};
-    const float Mc = warp_max(wsl.m);
-    const int ic = warp_min_i(wsl.m == Mc ? wsl.idx : INT32_MAX);
-    const bool has = wsl.z > 0.f;
-    const float cb = -warp_max(has ? -wsl.c : -INFINITY);
-    const double term = has ? (double)wsl.z * (double)ex2(cb - wsl.c) : 0.0;
-    const double Zc = warp_sum_d(term);
-    if (lane == 0) {
-      part_m[r] = Mc;
-      part_i[r] = ic;
-      part_c[r] = cb;
-      part_z[r] = Zc;
+  // ---- CTA statistics per row (thread per row), pushed into every CTA
+  cluster_wait();  // pairs with the arrive at the top
+  if (tid < nrows) {
+    const int r = tid;
+    float M = -INFINITY;
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, wstat[r * NW + w].m);
+    int I = INT32_MAX;
+    float C = INFINITY;
+    for (int w = 0; w < NW; ++w) {
+      const WStat x = wstat[r * NW + w];
+      if (x.m == M) I = min(I, x.idx);
+      if (x.z > 0.f) C = fminf(C, x.c);
     }
-    if (KF > 0 && (R.flags & kNeedKeys)) {
-      // NW x KF candidates; lane l holds candidates l, l + 32, ...
-      constexpr int PER = (NW * KFm + 31) / 32;
-      float cv[PER];
-      int ci[PER];
+    ff Z{0.f, 0.f};
+    for (int w = 0; w < NW; ++w) {
+      const WStat x = wstat[r * NW + w];
+      if (x.z > 0.f) Z = ff_add(Z, two_prod(x.z, ex2(C - x.c)));
+    }
+    CStat cst;
+    cst.m = M;
+    cst.idx = I;
+    cst.c = C;
+    cst.zhi = Z.hi;
+    cst.zlo = Z.lo;
+    for (int p = 0; p < cs; ++p) *cluster.map_shared_rank(&cstat[rank * nrows + r], p) = cst;
+  }
+  if (KF > 0) {
+    for (int r = warp; r < nrows; r += NW) {
+      const RowInfo &R = S.rows[r];
+      if (!(R.type == kRowK || R.type == kRowEK)) continue;
+      float tv[KFm];
+      int ti[KFm];
+      if (R.nsteps > 0) {
+        cta_keys<E, KFm, NT>(R, &wsel[R.j * NW * KFm], v0, v1, tv, ti);
+      } else {
 #pragma unroll
-      for (int h = 0; h < PER; ++h) {
-        const int c = lane + 32 * h;
-        cv[h] = -INFINITY;
-        ci[h] = INT32_MAX;
-        if (c < NW * KFm) {
-          const float2 e = wtop[r * NW * KFm + c];
-          cv[h] = e.x;
-          ci[h] = __float_as_int(e.y);
+        for (int x = 0; x < KFm; ++x) {
+          tv[x] = -INFINITY;
+          ti[x] = INT32_MAX;
         }
       }
-      for (int r2 = 0; r2 < KFm; ++r2) {
-        int hb = 0;
+      // lane 0 holds the CTA's keys; lanes p < cs push them to CTA p
 #pragma unroll
-        for (int h = 1; h < PER; ++h)
-          if (better(cv[h], ci[h], cv[hb], ci[hb])) hb = h;
-        float bv = -INFINITY;
-        int bi = INT32_MAX;
-#pragma unroll
-        for (int h = 0; h < PER; ++h)
-          if (h == hb) {
-            bv = cv[h];
-            bi = ci[h];
-          }
-        warp_best(bv, bi);
-#pragma unroll
-        for (int h = 0; h < PER; ++h)
-          if (bi != INT32_MAX && ci[h] == bi) {
-            cv[h] = -INFINITY;
-            ci[h] = INT32_MAX;
-          }
-        if (lane == 0) {
-          part_tv[r * KFm + r2] = bv;
-          part_ti[r * KFm + r2] = bi;
-        }
+      for (int x = 0; x < KFm; ++x) {
+        const float vx = __shfl_sync(0xffffffffu, tv[x], 0);
+        const int ix = __shfl_sync(0xffffffffu, ti[x], 0);
+        if (lane < cs)
+          *cluster.map_shared_rank(&ckeys[(rank * npos + R.j) * KFm + x], lane) =
+              make_float2(vx, __int_as_float(ix));
       }
     }
   }
-  cluster.sync();  // (1) every CTA's per-row partials are ready
+  cluster.sync();  // (1) every CTA's statistics are in every CTA
 
-  // ---- combine the cluster's partials (same arithmetic in every CTA)
-  for (int r = warp; r < nrows; r += NW) {
-    const RowInfo &R = S.rows[r];
-    float pm = -INFINITY, pc = INFINITY;
-    double pz = 0.0;
-    int pi = INT32_MAX;
-    if (lane < cs) {
-      pm = *cluster.map_shared_rank(&part_m[r], lane);
-      pc = *cluster.map_shared_rank(&part_c[r], lane);
-      pz = *cluster.map_shared_rank(&part_z[r], lane);
-      pi = *cluster.map_shared_rank(&part_i[r], lane);
+  // ---- combine the cluster's statistics (same arithmetic in every CTA)
+  if (tid < nrows) {
+    const int r = tid;
+    float M = -INFINITY;
+    for (int p = 0; p < cs; ++p) M = fmaxf(M, cstat[p * nrows + r].m);
+    int I = INT32_MAX;
+    float C = INFINITY;
+    for (int p = 0; p < cs; ++p) {
+      const CStat &x = cstat[p * nrows + r];
+      if (x.m == M) I = min(I, x.idx);
+      if (x.zhi > 0.f) C = fminf(C, x.c);
     }
-    const float M = warp_max(pm);
-    const int am = warp_min_i(pm == M ? pi : INT32_MAX);
-    const bool has = pz > 0.0;
-    const float C = -warp_max(has ? -pc : -INFINITY);
-    const double term = has ? pz * (double)ex2(C - pc) : 0.0;
-    const double Z = warp_sum_d(term);
-    if (lane == 0) {
-      S.M[r] = M;
-      S.C[r] = C;
-      S.Z[r] = Z;
-      S.amax[r] = am == INT32_MAX ? 0 : am;
+    ff Z{0.f, 0.f};
+    for (int p = 0; p < cs; ++p) {
+      const CStat &x = cstat[p * nrows + r];
+      if (x.zhi > 0.f) Z = ff_add(Z, ff_mul_f(ff{x.zhi, x.zlo}, ex2(C - x.c)));
     }
-    if (KF > 0 && (R.flags & kNeedKeys) && rank == 0 && P.keys_out) {
-      // merge cs x KF candidates into this row's keys
+    S.M[r] = M;
+    S.C[r] = C;
+    S.Z[r] = Z;
+    S.amax[r] = I == INT32_MAX ? 0 : I;
+  }
+  if (KF > 0 && P.keys) {
+    // keys of each position: the best fan of the cs x KF CTA candidates
+    for (int j = warp; j <= K; j += NW) {
+      const int fan = P.fanout[j];
+      if (fan <= 0) continue;
+      int2 *kdst = &S.keys[P.fan_off[j]];
+      int32_t *kout = P.keys_out ? P.keys_out + ((int64_t)b * P.n_keys_out + P.fan_off[j]) * 2
+                                 : nullptr;
+      const bool present = S.drow[j] >= 0;
       constexpr int PER = (kMaxCS * KFm + 31) / 32;
       float cv[PER];
       int ci[PER];
 #pragma unroll
       for (int h = 0; h < PER; ++h) {
-        const int c = lane + 32 * h;  // candidate c: peer c / KF, rank c % KF
+        const int c = lane + 32 * h;  // candidate c: CTA c / KF, rank c % KF
         cv[h] = -INFINITY;
         ci[h] = INT32_MAX;
-        if (c < cs * KFm) {
-          cv[h] = *cluster.map_shared_rank(&part_tv[r * KFm + c % KFm], c / KFm);
-          ci[h] = *cluster.map_shared_rank(&part_ti[r * KFm + c % KFm], c / KFm);
+        if (present && c < cs * KFm) {
+          const float2 e = ckeys[((c / KFm) * npos + j) * KFm + c % KFm];
+          cv[h] = e.x;
+          ci[h] = __float_as_int(e.y);
         }
       }
-      int32_t *kout = P.keys_out + ((int64_t)b * P.n_keys_out + P.fan_off[R.j]) * 2;
-      for (int r2 = 0; r2 < R.fan; ++r2) {
-        int hb = 0;
-#pragma unroll
-        for (int h = 1; h < PER; ++h)
-          if (better(cv[h], ci[h], cv[hb], ci[hb])) hb = h;
+      for (int r2 = 0; r2 < fan; ++r2) {
         float bv = -INFINITY;
         int bi = INT32_MAX;
 #pragma unroll
         for (int h = 0; h < PER; ++h)
-          if (h == hb) {
+          if (cv[h] > bv || (cv[h] == bv && ci[h] < bi)) {
             bv = cv[h];
             bi = ci[h];
           }
@@ -1019,18 +1268,14 @@ __global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_const
             ci[h] = INT32_MAX;
           }
         if (lane == 0) {
-          kout[2 * r2] = bi == INT32_MAX ? -1 : R.j;
-          kout[2 * r2 + 1] = bi == INT32_MAX ? -1 : bi;
+          const int2 key = bi == INT32_MAX ? make_int2(-1, -1) : make_int2(j, bi);
+          kdst[r2] = key;
+          if (rank == 0 && kout) {
+            kout[2 * r2] = key.x;
+            kout[2 * r2 + 1] = key.y;
+          }
         }
       }
-    }
-  }
-  // keys of the bonus position when there is no bonus row: empty slots
-  if (P.keys && P.keys_out && rank == 0 && tid == 0 && P.fanout[K] > 0 && S.drow[K] < 0) {
-    int32_t *kout = P.keys_out + ((int64_t)b * P.n_keys_out + P.fan_off[K]) * 2;
-    for (int r2 = 0; r2 < P.fanout[K]; ++r2) {
-      kout[2 * r2] = -1;
-      kout[2 * r2 + 1] = -1;
     }
   }
   __syncthreads();
@@ -1039,6 +1284,7 @@ __global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_const
     // ---- accept tests, one lane per position (K <= 32: warp 0)
     if (warp == 0) {
       const int j = lane;
+      const bool dvalid = S.dvalid != 0;
       int rej = 0;
       if (j < K) {
         const int rt = S.trow[j];
@@ -1048,19 +1294,21 @@ __global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_const
           a = (dvalid && d == S.amax[rt]) ? 1 : 0;
         } else if (dvalid) {
           const int rd = S.drow[j];
-          // log2 of 2^(l_d s + C): the product of two floats is exact in double
-          const double xt = (double)S.ld_t[j] * sd + (double)S.C[rt];
-          const double xd = (double)S.ld_d[j] * sd + (double)S.C[rd];
-          const float r = (S.ld_d[j] == -INFINITY)
+          const float lt = S.ld_t[K - 1 - j], ldr = S.ld_d[K - 1 - j];
+          // log2 of 2^(l_d s + C), carried as float-float (the products exact)
+          const ff xt = ff_add_f(two_prod(lt, s), S.C[rt]);
+          const ff xd = ff_add_f(two_prod(ldr, s), S.C[rd]);
+          const float zt = ff_f(S.Z[rt]), zd = ff_f(S.Z[rd]);
+          const float r = (ldr == -INFINITY)
                               ? INFINITY  // q(d) = 0
-                              : exp2_split(xt - xd) * ((float)S.Z[rd] / (float)S.Z[rt]);
-          const double u = uniform_u(P.seed, P.row_base + b, j, 0);
-          a = (u <= (double)r) ? 1 : 0;
+                              : exp2_ff(ff_sub(xt, xd)) * __fdiv_rn(zd, zt);
+          const float u = uniform_u(P.seed, P.row_base + b, j, 0);
+          a = (u <= r) ? 1 : 0;
           if (rank == 0) {
             const int64_t pj = (int64_t)b * K + j;
             if (P.ratio_out) P.ratio_out[pj] = r;
-            if (P.p_out) P.p_out[pj] = exp2_split(xt) / (float)S.Z[rt];
-            if (P.q_out) P.q_out[pj] = exp2_split(xd) / (float)S.Z[rd];
+            if (P.p_out) P.p_out[pj] = __fdiv_rn(exp2_ff(xt), zt);
+            if (P.q_out) P.q_out[pj] = __fdiv_rn(exp2_ff(xd), zd);
           }
         }
         rej = !a;
@@ -1085,9 +1333,11 @@ __global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_const
     __syncthreads();
 
     // ---- one inverse-CDF draw per sequence (residual at m, or p at K).
-    // Each warp takes a contiguous range of the slice, so warp masses are in
-    // index order; the owning CTA finds the crossing warp, which re-scans its
-    // range in 32-vector chunks.
+    // Each warp takes a contiguous range of the slice and lane l the four
+    // consecutive vectors 4l..4l+3 of each 128-vector step, so the masses
+    // kept per (step, lane) are in index order.  The CTA holding the crossing
+    // point finds its warp, step and lane from those masses, and that lane
+    // re-reads only its four vectors.
     for (int attempt = 0; attempt < 2 && S.kind != 0; ++attempt) {
       const int mm = S.m;
       const bool residual = S.kind == 1;
@@ -1096,16 +1346,18 @@ __global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_const
       const bool d_vec = residual && Rd->hp == Rt.hp;  // same vector grid
       const float Ct = S.C[S.trow[mm]];
       const float Cd = residual ? S.C[S.drow[mm]] : 0.f;
-      const float Rz = residual ? (float)(S.Z[S.trow[mm]] / S.Z[S.drow[mm]]) : 0.f;
+      const float Rz =
+          residual ? __fdiv_rn(ff_f(S.Z[S.trow[mm]]), ff_f(S.Z[S.drow[mm]])) : 0.f;
       const int wr = (Rt.nvec + NW - 1) / NW;  // vectors per warp
       const int wq0 = min(warp * wr, Rt.nvec), wq1 = min(wq0 + wr, Rt.nvec);
-      const int wsteps = (wr + 32 * kU - 1) / (32 * kU);
-      // weights of this lane's vector q of the target (and draft) row
-      auto vec_mass = [&](uint4 tvec, uint4 dvec, int q, bool dv_ok) -> float {
-        float ft[NV], fd[NV], w[NV];
+      const int wsteps = (wq1 - wq0 + 32 * kU - 1) / (32 * kU);
+      // element weights of vector q of the target row (tvec) against the
+      // draft (dvec, or element loads when the draft row's grid differs)
+      auto vec_weights = [&](const uint4 &tvec, const uint4 &dvec, int q, float *w) {
+        float ft[NV], fd[NV];
         Elt<E>::unpack(tvec, ft);
         if (residual) {
-          if (dv_ok) {
+          if (d_vec) {
             Elt<E>::unpack(dvec, fd);
           } else {
 #pragma unroll
@@ -1117,95 +1369,90 @@ __global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_const
           }
         }
         pass_weights<E>(ft, fd, residual, Ct, Cd, s, Rz, w);
+      };
+      auto vec_mass = [&](const uint4 &tvec, const uint4 &dvec, int q) -> float {
+        float w[NV];
+        vec_weights(tvec, dvec, q, w);
 #pragma unroll
         for (int h = NV / 2; h > 0; h >>= 1)
 #pragma unroll
           for (int i = 0; i < h; ++i) w[i] += w[i + h];
         return w[0];
       };
-      // units: target step t, then (same vector grid) draft step t
-      const int per = d_vec ? 2 : 1;
-      const int nunits = wsteps * per;
-      int i_u = 0;
-      auto issue_pass = [&](int slot) {
-        if (i_u < nunits) {
-          const RowInfo &RR = (i_u % per == 0) ? Rt : *Rd;
-          const int t = i_u / per;
+      float *pmw = pmass + warp * L.pw * 32;  // [step][lane] masses of this warp
+      {
+        // unit u: target step u / per, then (same vector grid) the draft step
+        constexpr uint32_t kSlot = kU * NT * 16;
+        const int per = d_vec ? 2 : 1;
+        const int nunits = wsteps * per;
+        int i_u = 0;
+        auto issue_pass = [&](int slot) {
+          if (i_u < nunits) {
+            const RowInfo &RR = (i_u % per == 0) ? Rt : *Rd;
+            const int t = i_u / per;
 #pragma unroll
-          for (int k = 0; k < kU; ++k)
-            issue_vec<NT>(RR, wq0 + t * 32 * kU + k * 32 + lane, wq1, ring_s, slot, k);
-          ++i_u;
+            for (int k = 0; k < kU; ++k)
+              issue_vec<NT>(RR, wq0 + t * 32 * kU + kU * lane + k, wq1, ring_t + slot * kSlot, k);
+            ++i_u;
+          }
+          cp_commit();
+        };
+#pragma unroll
+        for (int d = 0; d < kDepth - 1; ++d) issue_pass(d);
+        float tsum = 0.f, tcomp = 0.f;
+        uint4 tv4[kU];
+        for (int u = 0; u < nunits; ++u) {
+          issue_pass((u + kDepth - 1) % kDepth);
+          cp_wait<kDepth - 1>();
+          const int t = u / per;
+          const uint8_t *slot = ring + (u % kDepth) * kSlot + tid * 16;
+          const int q0 = wq0 + t * 32 * kU + kU * lane;
+          if (u % per == 0) {
+#pragma unroll
+            for (int k = 0; k < kU; ++k) tv4[k] = fetch_vec<E, NT>(Rt, q0 + k, wq1, slot, k, v0, v1);
+            if (per == 2) continue;  // the draft unit follows
+          }
+          float vs[kU];
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            uint4 dvec = tv4[k];
+            if (d_vec) dvec = fetch_vec<E, NT>(*Rd, q0 + k, wq1, slot, k, v0, v1);
+            vs[k] = q0 + k < wq1 ? vec_mass(tv4[k], dvec, q0 + k) : 0.f;
+          }
+          const float ms = (vs[0] + vs[1]) + (vs[2] + vs[3]);
+          pmw[t * 32 + lane] = ms;
+          kahan_add(tsum, tcomp, ms);
         }
-        cp_commit();
-      };
-#pragma unroll
-      for (int d = 0; d < kDepth - 1; ++d) issue_pass(d);
-      float tsum = 0.f, tcomp = 0.f;
-      uint4 tv4[kU];
-      for (int u = 0; u < nunits; ++u) {
-        issue_pass((u + kDepth - 1) % kDepth);
-        cp_wait<kDepth - 1>();
-        const int t = u / per;
-        if (u % per == 0) {
-#pragma unroll
-          for (int k = 0; k < kU; ++k)
-            tv4[k] = fetch_vec<E, NT>(Rt, wq0 + t * 32 * kU + k * 32 + lane, wq1, ring, u % kDepth,
-                                      k, v0, v1);
-          if (per == 2) continue;  // the draft unit follows
-        }
-        float vs[kU];
-#pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int q = wq0 + t * 32 * kU + k * 32 + lane;
-          uint4 dvec = tv4[k];
-          if (d_vec) dvec = fetch_vec<E, NT>(*Rd, q, wq1, ring, u % kDepth, k, v0, v1);
-          vs[k] = q < wq1 ? vec_mass(tv4[k], dvec, q, d_vec) : 0.f;
-        }
-#pragma unroll
-        for (int h = kU / 2; h > 0; h >>= 1)
-#pragma unroll
-          for (int k = 0; k < h; ++k) vs[k] += vs[k + h];
-        kahan_add(tsum, tcomp, vs[0]);
+        cp_wait<0>();
+        const ff wm = ff_warp_sum(two_sum(tsum, -tcomp));
+        if (lane == 0) S.wmass[warp] = wm;
       }
-      cp_wait<0>();
-      // warp masses, their prefix, the CTA mass
-      const double wm = warp_sum_d((double)tsum - (double)tcomp);
-      if (lane == 0) S.wmass[warp] = wm;
       __syncthreads();
       if (warp == 0) {
-        const double m_l = lane < NW ? S.wmass[lane] : 0.0;
-        double incl = m_l;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const double y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        if (lane < NW) S.wpre[lane] = incl - m_l;
-        if (lane == 31) S.s_part = incl;
+        // prefix over the warps, the CTA mass pushed into every CTA
+        const ff m_l = lane < NW ? S.wmass[lane] : ff{0.f, 0.f};
+        const ff incl = ff_warp_scan(m_l);
+        if (lane < NW) S.wpre[lane] = ff_sub(incl, m_l);
+        const ff tot_cta = ff_shfl(incl, 31);
+        if (lane < cs) *cluster.map_shared_rank(&cmass[attempt * cs + rank], lane) = tot_cta;
       }
-      cluster.sync();  // (2) slice masses ready
+      cluster.sync();  // (2) slice masses are in every CTA
       if (warp == 0) {
-        // prefix of the slice masses over the cluster (lane c: CTA c)
-        const double sc = lane < cs ? *cluster.map_shared_rank(&S.s_part, lane) : 0.0;
-        double incl = sc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const double y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const double tot = __shfl_sync(0xffffffffu, incl, 31);
-        if (tot > 0.0 || !residual) {
-          const double u = uniform_u(P.seed, P.row_base + b, mm, 1);
-          const double t = u * tot;
-          const unsigned cross = __ballot_sync(0xffffffffu, sc > 0.0 && incl > t);
-          const unsigned pos = __ballot_sync(0xffffffffu, sc > 0.0);
+        const ff sc = lane < cs ? cmass[attempt * cs + lane] : ff{0.f, 0.f};  // lane c: CTA c
+        const ff incl = ff_warp_scan(sc);
+        const ff tot = ff_shfl(incl, 31);
+        if (ff_pos(tot) || !residual) {
+          const float u = uniform_u(P.seed, P.row_base + b, mm, 1);
+          const ff t = ff_mul_f(tot, u);
+          const unsigned cross = __ballot_sync(0xffffffffu, ff_pos(sc) && ff_gt(incl, t));
+          const unsigned pos = __ballot_sync(0xffffffffu, ff_pos(sc));
           // the first CTA whose range passes t; if rounding put t past the
           // total, the last CTA with mass
           const int cstar = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : 0);
-          const double before = __shfl_sync(0xffffffffu, incl - sc, cstar);
+          const ff before = ff_shfl(ff_sub(incl, sc), cstar);
           if (lane == 0) {
             S.cstar = cstar;
-            S.t_loc = t - before;
+            S.t_loc = ff_sub(t, before);
             S.owner = cstar;
           }
         } else if (lane == 0) {
@@ -1213,105 +1460,96 @@ __global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_const
         }
       }
       __syncthreads();
-      if (residual && S.kind == 2) {
-        cluster.sync();  // peers are done reading this CTA's mass
-        continue;
-      }
+      if (S.kind == 2 && residual) continue;  // every CTA takes this branch
       if (rank == S.cstar) {
-        // the crossing warp: the first whose range passes t_loc, else the
-        // last with mass
         if (warp == 0) {
-          const double m_l = lane < NW ? S.wmass[lane] : 0.0;
-          const double pre = lane < NW ? S.wpre[lane] : 0.0;
-          const unsigned cross = __ballot_sync(0xffffffffu, m_l > 0.0 && pre + m_l > S.t_loc);
-          const unsigned pos = __ballot_sync(0xffffffffu, m_l > 0.0);
+          // the crossing warp: the first whose range passes t_loc, else the
+          // last with mass
+          const ff m_l = lane < NW ? S.wmass[lane] : ff{0.f, 0.f};
+          const ff pre = lane < NW ? S.wpre[lane] : ff{0.f, 0.f};
+          const unsigned cross =
+              __ballot_sync(0xffffffffu, ff_pos(m_l) && ff_gt(ff_add(pre, m_l), S.t_loc));
+          const unsigned pos = __ballot_sync(0xffffffffu, ff_pos(m_l));
           const int ws = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : 0);
           if (lane == 0) {
             S.wsel = ws;
-            S.t_w = S.t_loc - S.wpre[ws];
+            S.t_w = ff_sub(S.t_loc, S.wpre[ws]);
           }
         }
         __syncthreads();
         if (warp == S.wsel) {
-          // masses of this warp's vectors, in index order, into the (now
-          // idle) ring memory; then a chunked scan
-          float *vm_s = reinterpret_cast<float *>(ring);
-          const int nq = wq1 - wq0;
-          for (int base = 0; base < nq; base += 32 * kU) {
-            uint4 tvv[kU], dvv[kU];
+          const ff tw = S.t_w;
+          // the crossing step: step masses (lane t sums row t of the warp's
+          // [step][lane] masses pairwise, reading it rotated across the banks)
+          int tsel = -1, tlast = -1;
+          ff before{0.f, 0.f}, before_last{0.f, 0.f}, cum{0.f, 0.f};
+          for (int tb = 0; tb < wsteps && tsel < 0; tb += 32) {
+            const int t = tb + lane;
+            float row[32];
 #pragma unroll
-            for (int k = 0; k < kU; ++k) {
-              const int q = wq0 + base + k * 32 + lane;
-              tvv[k] = q < wq1 ? load_vec_direct<E>(Rt, q, v0, v1) : tvv[0];
-              dvv[k] = (q < wq1 && d_vec) ? load_vec_direct<E>(*Rd, q, v0, v1) : tvv[k];
-            }
+            for (int i = 0; i < 32; ++i) row[i] = t < wsteps ? pmw[t * 32 + ((i + lane) & 31)] : 0.f;
 #pragma unroll
-            for (int k = 0; k < kU; ++k) {
-              const int q = wq0 + base + k * 32 + lane;
-              if (q < wq1) vm_s[q - wq0] = vec_mass(tvv[k], dvv[k], q, d_vec);
-            }
-          }
-          __syncwarp();
-          const double tw = S.t_w;
-          double cum = 0.0;
-          int qsel = -1;
-          double before = 0.0;
-          int qlast = -1;
-          double before_last = 0.0;
-          for (int base = 0; base < nq && qsel < 0; base += 32) {
-            const int i = base + lane;
-            const double mv = i < nq ? (double)vm_s[i] : 0.0;
-            double incl = mv;
+            for (int h = 16; h > 0; h >>= 1)
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const double y = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += y;
-            }
-            const unsigned cross = __ballot_sync(0xffffffffu, mv > 0.0 && cum + incl > tw);
-            const unsigned pos = __ballot_sync(0xffffffffu, mv > 0.0);
+              for (int i = 0; i < h; ++i) row[i] += row[i + h];
+            const float mt = row[0];
+            const ff incl = ff_warp_scan(ff{mt, 0.f});
+            const unsigned cross = __ballot_sync(0xffffffffu, mt > 0.f && ff_gt(ff_add(cum, incl), tw));
+            const unsigned pos = __ballot_sync(0xffffffffu, mt > 0.f);
             if (cross) {
               const int l = __ffs(cross) - 1;
-              qsel = wq0 + base + l;
-              before = cum + __shfl_sync(0xffffffffu, incl - mv, l);
+              tsel = tb + l;
+              before = ff_add(cum, ff_shfl(ff_add_f(incl, -mt), l));
             } else if (pos) {
               const int l = 31 - __clz(pos);
-              qlast = wq0 + base + l;
-              before_last = cum + __shfl_sync(0xffffffffu, incl - mv, l);
+              tlast = tb + l;
+              before_last = ff_add(cum, ff_shfl(ff_add_f(incl, -mt), l));
             }
-            cum += __shfl_sync(0xffffffffu, incl, 31);
+            cum = ff_add(cum, ff_shfl(incl, 31));
           }
-          if (qsel < 0) {  // rounding put the target past this warp's mass
-            qsel = qlast;
+          if (tsel < 0) {  // rounding put the target past the warp's mass
+            tsel = tlast;
             before = before_last;
           }
-          if (lane == 0) {
+          // the crossing lane within that step
+          int lsel = -1;
+          ff before_l{0.f, 0.f};
+          if (tsel >= 0) {
+            const float ml = pmw[tsel * 32 + lane];
+            const ff incl = ff_warp_scan(ff{ml, 0.f});
+            const unsigned cross =
+                __ballot_sync(0xffffffffu, ml > 0.f && ff_gt(ff_add(before, incl), tw));
+            const unsigned pos = __ballot_sync(0xffffffffu, ml > 0.f);
+            lsel = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : -1);
+            if (lsel >= 0) before_l = ff_add(before, ff_shfl(ff_add_f(incl, -ml), lsel));
+          }
+          if (lsel >= 0 && lane == lsel) {
+            // the crossing lane's four vectors, element by element
+            const int q0 = wq0 + tsel * 32 * kU + kU * lane;
             int tok = -1, klast = -1;
-            if (qsel >= 0) {
-              float ft[NV], fd[NV], w[NV];
-              Elt<E>::unpack(load_vec_direct<E>(Rt, qsel, v0, v1), ft);
-              if (residual) Elt<E>::unpack(load_vec_direct<E>(*Rd, qsel, v0, v1), fd);
-              if (residual && !d_vec) {
-#pragma unroll
-                for (int i = 0; i < NV; ++i) {
-                  const int e = elem_index(v0, Rt.hp, qsel, i, sz);
-                  fd[i] = (e >= v0 && e < v1) ? Elt<E>::load_global(Rd->g + (int64_t)e * sz)
-                                              : -INFINITY;
-                }
-              }
-              pass_weights<E>(ft, fd, residual, Ct, Cd, s, Rz, w);
-              double c2 = before;
+            ff c2 = before_l;
+            for (int k = 0; k < kU && tok < 0; ++k) {
+              const int q = q0 + k;
+              if (q >= wq1) break;
+              const uint4 tvv = load_vec_direct<E>(Rt, q, v0, v1);
+              const uint4 dvv = d_vec ? load_vec_direct<E>(*Rd, q, v0, v1) : tvv;
+              float w[NV];
+              vec_weights(tvv, dvv, q, w);
               for (int i = 0; i < NV; ++i) {
-                const int e = elem_index(v0, Rt.hp, qsel, i, sz);
+                const int e = elem_index(v0, Rt.hp, q, i, sz);
                 if (e < v0 || e >= v1 || !(w[i] > 0.f)) continue;
                 klast = e;
-                if (tok < 0 && c2 + (double)w[i] > tw) tok = e;
-                c2 += (double)w[i];
+                const ff c3 = ff_add_f(c2, w[i]);
+                if (ff_gt(c3, tw)) {
+                  tok = e;
+                  break;
+                }
+                c2 = c3;
               }
-              if (tok < 0) tok = klast;
             }
-            if (tok < 0) tok = S.amax[S.trow[mm]];  // degenerate: no mass in this slice
-            S.tok = tok;
+            S.tok = tok >= 0 ? tok : klast;
           }
+          if (lsel < 0 && lane == 0) S.tok = S.amax[S.trow[mm]];  // no mass in this warp
         }
         __syncthreads();
       }
@@ -1328,7 +1566,7 @@ __global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_const
         if (P.hit) P.hit[b] = 0;
         if (P.status)
           atomicOr(P.status, (tvalid ? 0 : (int)SD_STATUS_BAD_TEMP) |
-                                 (dvalid ? 0 : (int)SD_STATUS_BAD_TOKEN));
+                                 (S.dvalid ? 0 : (int)SD_STATUS_BAD_TOKEN));
       } else {
         const int mm = S.m, tok = S.tok;
         for (int j = 0; j < mm; ++j) out[j] = S.d[j];
@@ -1338,12 +1576,9 @@ __global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_const
         P.tau[b] = mm + 1;
         if (P.hit) {
           int h = 0;
-          if (P.keys && P.keys_out) {
-            // written by rank 0 of this cluster before barrier (2), or by
-            // this very CTA when it is rank 0
-            const int32_t *kb = P.keys_out + (int64_t)b * P.n_keys_out * 2;
+          if (P.keys) {
             for (int k2 = 0; k2 < P.n_keys_out; ++k2)
-              if (__ldcg(kb + 2 * k2) == mm && __ldcg(kb + 2 * k2 + 1) == tok) h = 1;
+              if (S.keys[k2].x == mm && S.keys[k2].y == tok) h = 1;
           } else if (P.keys_in) {
             const int32_t *kb = P.keys_in + (int64_t)b * P.n_keys_in * 2;
             for (int k2 = 0; k2 < P.n_keys_in; ++k2)
@@ -1353,12 +1588,12 @@ __global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_const
         }
       }
       if (P.compact) {
-        __threadfence();
-        const int done = atomicAdd(P.done_counter, 1);
-        if (done == P.B - 1) {
-          __threadfence();
-          S.flag_compact = 1;
-        }
+        // release: this thread's outputs above; acquire: every other
+        // sequence's, for the one that arrives last
+        int done;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                     : "=r"(done) : "l"(P.done_counter) : "memory");
+        if (done == P.B - 1) S.flag_compact = 1;
       }
     }
     __syncthreads();
@@ -1367,7 +1602,8 @@ __global__ void __launch_bounds__(NT, 768 / NT) sd_seq_kernel(const __grid_const
       if (tid == 0) *P.done_counter = 0;
     }
   }
-  cluster.sync();  // peers may still read this CTA's shared memory
+  // No CTA touches another's shared memory after barrier (1) or (2), which
+  // every CTA passes, so the CTAs may leave independently.
 }
 
 __global__ void sd_compact_kernel(int B, int K, const int32_t *out_tokens, const int32_t *tau,
@@ -1379,7 +1615,7 @@ __global__ void sd_compact_kernel(int B, int K, const int32_t *out_tokens, const
 __global__ void sd_uniforms_kernel(uint64_t seed, int n, const int32_t *row, const int32_t *pos,
                                    const int32_t *slot, double *out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) out[i] = uniform_u(seed, row[i], pos[i], slot[i]);
+  if (i < n) out[i] = (double)uniform_u(seed, row[i], pos[i], slot[i]);
 }
 
 // ------------------------------------------------------------------- host --
@@ -1420,23 +1656,84 @@ static int rows_per_seq(const Params &P) {
   return std::max(n, 1);
 }
 
-// Cluster size: slices of at most kMaxSliceVec vectors, then enough CTAs to
-// give every SM two, at most kMaxCS.
-static int choose_cs(int B, int V, int sz) {
+// Vocabulary slice of one CTA for cluster size cs (a multiple of 16 elements).
+static int slice_for(int V, int cs) { return (int)((((int64_t)V + cs - 1) / cs + 15) / 16 * 16); }
+
+template <typename E, int KF, int NT>
+static int smem_bytes(const Params &P, int cs) {
+  return make_layout(NT, rows_per_seq(P), P.K + 1, KF, cs, slice_for(P.V, cs), Elt<E>::kSize)
+      .total;
+}
+
+// Clusters of cs CTAs with `smem` bytes each that the device holds at once.
+template <typename E, int KF, int NT>
+static int max_active_clusters(int cs, int smem) {
+  static std::mutex mu;
+  static int cache[kMaxCS + 1][8];
+  static int cache_smem[kMaxCS + 1][8];
+  std::lock_guard<std::mutex> g(mu);
+  const int slot = (smem / 1024) % 8;
+  if (cache_smem[cs][slot] == smem + 1) return cache[cs][slot];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cs, 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel_fn<E, KF, NT>(), &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[cs][slot] = n;
+  cache_smem[cs][slot] = smem + 1;
+  return n;
+}
+
+// Cluster size: the largest cs up to about SDV_CPS (default 2) CTAs per SM
+// for which all B clusters are resident at once (one wave); if none is,
+// the size that leaves the fewest waves.
+template <typename E, int KF, int NT>
+static int choose_cs(const Params &P) {
   const int forced = env_int("SDV_CS", 0);
   if (forced) return forced;
-  int cs = 1;
-  while (cs < kMaxCS && (((int64_t)V + cs - 1) / cs * sz + 31) / 16 + 2 > kMaxSliceVec) cs <<= 1;
-  while (cs < kMaxCS && (int64_t)B * cs < 2LL * sm_count()) cs <<= 1;
-  return cs;
+  const int per_sm = std::max(1, env_int("SDV_CPS", 2));
+  const int B = std::max(P.B, 1);
+  const int target = (int)std::min<int64_t>(
+      kMaxCS, std::max<int64_t>(1, (int64_t)per_sm * sm_count() / B));
+  int best = -1;
+  int64_t best_waves = INT64_MAX;
+  for (int cs = target; cs >= 1; --cs) {
+    const int smem = smem_bytes<E, KF, NT>(P, cs);
+    if (smem > kDynSmemCap) break;
+    const int n = max_active_clusters<E, KF, NT>(cs, smem);
+    if (n <= 0) continue;
+    if (n >= B) return cs;
+    const int64_t waves = (B + n - 1) / n;
+    if (waves < best_waves) {
+      best_waves = waves;
+      best = cs;
+    }
+  }
+  if (best > 0) return best;
+  for (int cs = target; cs <= kMaxCS; ++cs)
+    if (smem_bytes<E, KF, NT>(P, cs) <= kDynSmemCap) return cs;
+  return kMaxCS;
 }
 
 template <typename E, int KF, int NT>
-static sd_status_t launch_nt(Params &P, int cs, cudaStream_t stream) {
+static sd_status_t launch_nt(Params &P, cudaStream_t stream) {
   constexpr int sz = Elt<E>::kSize;
+  const int cs = choose_cs<E, KF, NT>(P);
+  if (cs < 1 || cs > kMaxCS) return SD_ERR_INVALID_ARG;
   P.cs = cs;
-  P.slice = (int)((((int64_t)P.V + cs - 1) / cs + 15) / 16 * 16);
-  const Layout L = make_layout(NT, rows_per_seq(P), KF);
+  P.slice = slice_for(P.V, cs);
+  const Layout L = make_layout(NT, rows_per_seq(P), P.K + 1, KF, cs, P.slice, sz);
   if (L.total > kDynSmemCap) return SD_ERR_UNSUPPORTED;
   void *fn = kernel_fn<E, KF, NT>();
   cudaLaunchConfig_t cfg = {};
@@ -1462,15 +1759,9 @@ static sd_status_t launch_nt(Params &P, int cs, cudaStream_t stream) {
   return SD_OK;
 }
 
-// 512-thread CTAs when the grid would leave SMs short of warps.
 template <typename E, int KF>
 static sd_status_t launch_kf(Params &P, cudaStream_t s) {
-  constexpr int sz = Elt<E>::kSize;
-  const int cs = choose_cs(P.B, P.V, sz);
-  if (cs < 1 || cs > kMaxCS) return SD_ERR_INVALID_ARG;
-  int nt = env_int("SDV_NT", 0);
-  if (nt != 256 && nt != 512) nt = 256;
-  return nt == 512 ? launch_nt<E, KF, 512>(P, cs, s) : launch_nt<E, KF, 256>(P, cs, s);
+  return launch_nt<E, KF, 256>(P, s);
 }
 
 template <typename E>

@@ -156,6 +156,44 @@ def test_outcome_keys_standalone_and_fused(dev, dt):
     _check(*compare_verify(r2, o, inp.temperature.cpu().numpy(), check_stats=False))
 
 
+@pytest.mark.parametrize("cs", [1, 3, 7, 16])
+def test_forced_cluster_sizes(dev, cs, monkeypatch):
+    # every cluster size streams the same rows: slices off the 16-byte grid
+    # (odd V, bf16), fan-outs up to the largest key count, greedy and sampled
+    monkeypatch.setenv("SDV_CS", str(cs))
+    B, K, V = 3, 5, 50021
+    fan = [8, 2, 1, 0, 3, 1]
+    temps = [0.7, 0.0, 1.3]
+    inp = W.synth(B, K, V, "bf16", kind="peaked", sigma=3.0, draft_sigma=1.0, peaks=20,
+                  temperature=temps, seed=40 + cs, device=dev, bonus_row=True)
+    keys_ref = oracle.outcome_predict(_np(inp.draft), inp.tokens.cpu().numpy(), fan,
+                                      _np(inp.draft_bonus))
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, fanout=fan,
+                  draft_bonus=inp.draft_bonus, stats=True, compact=True)
+    np.testing.assert_array_equal(r.keys.cpu().numpy(), keys_ref)
+    o = _oracle_for(inp, keys=keys_ref)
+    _check(*compare_verify(r, o, temps))
+    offs, packed = oracle.compact(r.out_tokens.cpu().numpy(), r.tau.cpu().numpy())
+    np.testing.assert_array_equal(r.offsets.cpu().numpy(), offs)
+    np.testing.assert_array_equal(r.packed.cpu().numpy()[: offs[-1]], packed)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_largest_k_with_keys(dev, dt):
+    B, K, V = 2, 32, 3001
+    fan = [2] * K + [1]
+    temps = [1.0, 0.0]
+    inp = W.synth(B, K, V, dt, kind="normal", sigma=1.0, draft_sigma=0.1, temperature=temps,
+                  seed=32, device=dev, bonus_row=True)
+    keys_ref = oracle.outcome_predict(_np(inp.draft), inp.tokens.cpu().numpy(), fan,
+                                      _np(inp.draft_bonus))
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, fanout=fan,
+                  draft_bonus=inp.draft_bonus, stats=True, compact=True)
+    np.testing.assert_array_equal(r.keys.cpu().numpy(), keys_ref)
+    o = _oracle_for(inp, keys=keys_ref)
+    _check(*compare_verify(r, o, temps))
+
+
 def test_d3d_key_counts(dev):
     B, K, V = 2, 15, 4096
     inp = W.synth(B, K, V, "bf16", kind="normal", temperature=0.0, seed=9, device=dev,
