@@ -102,7 +102,7 @@ __device__ __forceinline__ uint32_t philox_w0(uint64_t seed, uint32_t row, uint3
                                               uint32_t slot) {
   uint32_t c0 = row, c1 = pos, c2 = slot, c3 = 0u;
   uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
-#pragma unroll
+#pragma unroll 1
   for (int r = 0; r < 10; ++r) {
     const uint32_t m0 = 0xD2511F53u, m1 = 0xCD9E8D57u;
     const uint32_t hi0 = __umulhi(m0, c0), lo0 = m0 * c0;
@@ -183,17 +183,17 @@ __device__ __forceinline__ ff ff_shfl_xor(ff x, int o) {
   return ff{__shfl_xor_sync(0xffffffffu, x.hi, o), __shfl_xor_sync(0xffffffffu, x.lo, o)};
 }
 // inclusive warp scan and warp sum
-__device__ __forceinline__ ff ff_warp_scan(ff x) {
+__device__ __noinline__ ff ff_warp_scan(ff x) {
   const int lane = threadIdx.x & 31;
-#pragma unroll
+#pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
     const ff y = ff_shfl_up(x, o);
     if (lane >= o) x = ff_add(x, y);
   }
   return x;
 }
-__device__ __forceinline__ ff ff_warp_sum(ff x) {
-#pragma unroll
+__device__ __noinline__ ff ff_warp_sum(ff x) {
+#pragma unroll 1
   for (int o = 16; o > 0; o >>= 1) x = ff_add(x, ff_shfl_xor(x, o));
   return x;
 }
@@ -201,7 +201,7 @@ __device__ __forceinline__ ff ff_warp_sum(ff x) {
 // 2^(x.hi + x.lo) without a double-precision transcendental: the integer
 // part of hi scales the result exactly, the fraction (hi - n exact, plus
 // lo) goes through ex2 (relative error about 2^-22).  Below 2^-126: 0.
-__device__ __forceinline__ float exp2_ff(ff x) {
+__device__ __noinline__ float exp2_ff(ff x) {
   if (!(x.hi > -126.f)) return 0.f;
   if (x.hi >= 128.f) return INFINITY;
   const float n = floorf(x.hi);
@@ -368,7 +368,7 @@ __device__ __forceinline__ int elem_index(int v0, int hp, int q, int i, int sz) 
 }
 
 template <int NT>
-__device__ __forceinline__ void row_geometry(RowInfo &R, int v0, int v1, int sz) {
+__device__ __noinline__ void row_geometry(RowInfo &R, int v0, int v1, int sz) {
   constexpr int kStepVec = NT * kU;
   R.gbase = R.g;
   R.hp = R.nvec = R.nsteps = R.qlo = R.qhi = R.sf0 = R.sf1 = 0;
@@ -464,10 +464,10 @@ struct CStat {
 struct Layout {
   int ring, wstat, wsel, cstat, ckeys, cmass, pmass, pw, total;
 };
-// Steps of 32 kU vectors in one warp's share of a slice of `slice` elements.
+// Steps of 64 vectors in one warp's share of a slice of `slice` elements.
 __host__ __device__ inline int pass_steps(int slice, int sz, int NT) {
   const int nvec = (slice * sz + 31) / 16 + 1, nw = NT / 32;
-  return ((nvec + nw - 1) / nw + 32 * kU - 1) / (32 * kU);
+  return ((nvec + nw - 1) / nw + 63) / 64;
 }
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
 __host__ __device__ inline Layout make_layout(int NT, int nrows, int npos, int KF, int cs,
@@ -517,7 +517,6 @@ struct Static {
   ff t_w;
   int red_i[kMaxWarps];
   int tok;
-  int flag_compact;
 };
 
 // Copy-ahead cursor: the next step this thread copies.
@@ -630,6 +629,22 @@ __device__ __forceinline__ void pass_weights(const float *ft, const float *fd, b
     const float pt = ex2(fmaf(ft[k], s, Ct));
     w[k] = residual ? fmaxf(0.f, pt - ex2(fmaf(fd[k], s, Cd)) * R) : pt;
   }
+}
+
+// Mass of one target vector in the sampling pass (sum of its weights).
+template <typename E>
+__device__ __noinline__ float vec_mass(uint4 tv, uint4 dv, bool residual, float Ct, float Cd,
+                                       float s, float R) {
+  constexpr int N = Elt<E>::kPerVec;
+  float ft[N], fd[N], w[N];
+  Elt<E>::unpack(tv, ft);
+  Elt<E>::unpack(dv, fd);
+  pass_weights<E>(ft, fd, residual, Ct, Cd, s, R, w);
+#pragma unroll
+  for (int h = N / 2; h > 0; h >>= 1)
+#pragma unroll
+    for (int i = 0; i < h; ++i) w[i] += w[i + h];
+  return w[0];
 }
 
 // Per-thread state of the row being streamed.
@@ -906,10 +921,11 @@ __device__ __forceinline__ void stream_row(RowAcc<KF> &A, const RowInfo &R, Issu
 // The CTA's best KF elements (value desc, index asc) of key row R from the
 // NW x KF vectors its warps kept, by one warp: the lanes expand the vectors
 // into elements (without the excluded token, -inf and anything outside the
-// slice), then KF rounds of a warp-wide best.  Lane 0 returns them.
+// slice), then KF rounds of a warp-wide best.  Lane 0 writes them to out[]
+// as {value, index bits}; no candidate: {-inf, INT32_MAX}.
 template <typename E, int KF, int NT>
-__device__ __forceinline__ void cta_keys(const RowInfo &R, const int *wsel, int v0, int v1,
-                                         float *outv, int *outi) {
+__device__ __noinline__ void cta_keys(const RowInfo &R, const int *wsel, int v0, int v1,
+                                      float2 *out) {
   constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec, NW = NT / 32;
   constexpr int NC = NW * KF;
   constexpr int PER = (NC + 31) / 32;
@@ -941,7 +957,7 @@ __device__ __forceinline__ void cta_keys(const RowInfo &R, const int *wsel, int 
       }
     }
   }
-#pragma unroll
+#pragma unroll 1
   for (int r = 0; r < KF; ++r) {
     float bv = -INFINITY;
     int bi = INT32_MAX;
@@ -958,10 +974,7 @@ __device__ __forceinline__ void cta_keys(const RowInfo &R, const int *wsel, int 
         cv[t] = -INFINITY;
         ci[t] = INT32_MAX;
       }
-    if (lane == 0) {
-      outv[r] = bi == INT32_MAX ? -INFINITY : bv;
-      outi[r] = bi;
-    }
+    if (lane == 0) out[r] = make_float2(bi == INT32_MAX ? -INFINITY : bv, __int_as_float(bi));
   }
 }
 
@@ -1056,7 +1069,6 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
     if (lane == 0) {
       S.nrows = base + __popc(dm) + (verify ? K : 0);
       S.dvalid = dvalid ? 1 : 0;
-      S.flag_compact = 0;
     }
   } else if (warp == 1 && lane < 2) {
     if (lane == 0 && has_bonus) {
@@ -1146,6 +1158,8 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
     }
     cp_wait<0>();
   }
+  // the packing launch that follows may be scheduled from here on
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 0 && lane < K) {
     S.ld_t[lane] = my_lt;  // lane l holds position K-1-l
     S.ld_d[lane] = my_ld;
@@ -1157,15 +1171,18 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
   if (tid < nrows) {
     const int r = tid;
     float M = -INFINITY;
+#pragma unroll 1
     for (int w = 0; w < NW; ++w) M = fmaxf(M, wstat[r * NW + w].m);
     int I = INT32_MAX;
     float C = INFINITY;
+#pragma unroll 1
     for (int w = 0; w < NW; ++w) {
       const WStat x = wstat[r * NW + w];
       if (x.m == M) I = min(I, x.idx);
       if (x.z > 0.f) C = fminf(C, x.c);
     }
     ff Z{0.f, 0.f};
+#pragma unroll 1
     for (int w = 0; w < NW; ++w) {
       const WStat x = wstat[r * NW + w];
       if (x.z > 0.f) Z = ff_add(Z, two_prod(x.z, ex2(C - x.c)));
@@ -1176,32 +1193,25 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
     cst.c = C;
     cst.zhi = Z.hi;
     cst.zlo = Z.lo;
+#pragma unroll 1
     for (int p = 0; p < cs; ++p) *cluster.map_shared_rank(&cstat[rank * nrows + r], p) = cst;
   }
   if (KF > 0) {
     for (int r = warp; r < nrows; r += NW) {
       const RowInfo &R = S.rows[r];
       if (!(R.type == kRowK || R.type == kRowEK)) continue;
-      float tv[KFm];
-      int ti[KFm];
+      // the CTA's keys staged in the idle ring, then pushed to every CTA
+      float2 *stage = reinterpret_cast<float2 *>(ring) + R.j * KFm;
       if (R.nsteps > 0) {
-        cta_keys<E, KFm, NT>(R, &wsel[R.j * NW * KFm], v0, v1, tv, ti);
-      } else {
-#pragma unroll
-        for (int x = 0; x < KFm; ++x) {
-          tv[x] = -INFINITY;
-          ti[x] = INT32_MAX;
-        }
+        cta_keys<E, KFm, NT>(R, &wsel[R.j * NW * KFm], v0, v1, stage);
+      } else if (lane < KFm) {
+        stage[lane] = make_float2(-INFINITY, __int_as_float(INT32_MAX));
       }
-      // lane 0 holds the CTA's keys; lanes p < cs push them to CTA p
-#pragma unroll
-      for (int x = 0; x < KFm; ++x) {
-        const float vx = __shfl_sync(0xffffffffu, tv[x], 0);
-        const int ix = __shfl_sync(0xffffffffu, ti[x], 0);
-        if (lane < cs)
-          *cluster.map_shared_rank(&ckeys[(rank * npos + R.j) * KFm + x], lane) =
-              make_float2(vx, __int_as_float(ix));
-      }
+      __syncwarp();
+#pragma unroll 1
+      for (int x = lane; x < KFm * cs; x += 32)
+        *cluster.map_shared_rank(&ckeys[(rank * npos + R.j) * KFm + x % KFm], x / KFm) =
+            stage[x % KFm];
     }
   }
   cluster.sync();  // (1) every CTA's statistics are in every CTA
@@ -1210,15 +1220,18 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
   if (tid < nrows) {
     const int r = tid;
     float M = -INFINITY;
+#pragma unroll 1
     for (int p = 0; p < cs; ++p) M = fmaxf(M, cstat[p * nrows + r].m);
     int I = INT32_MAX;
     float C = INFINITY;
+#pragma unroll 1
     for (int p = 0; p < cs; ++p) {
       const CStat &x = cstat[p * nrows + r];
       if (x.m == M) I = min(I, x.idx);
       if (x.zhi > 0.f) C = fminf(C, x.c);
     }
     ff Z{0.f, 0.f};
+#pragma unroll 1
     for (int p = 0; p < cs; ++p) {
       const CStat &x = cstat[p * nrows + r];
       if (x.zhi > 0.f) Z = ff_add(Z, ff_mul_f(ff{x.zhi, x.zlo}, ex2(C - x.c)));
@@ -1333,94 +1346,71 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
     __syncthreads();
 
     // ---- one inverse-CDF draw per sequence (residual at m, or p at K).
-    // Each warp takes a contiguous range of the slice and lane l the four
-    // consecutive vectors 4l..4l+3 of each 128-vector step, so the masses
-    // kept per (step, lane) are in index order.  The CTA holding the crossing
+    // Each warp takes a contiguous range of the slice and lane l the two
+    // consecutive vectors 2l, 2l+1 of each 64-vector step, so the masses kept
+    // per (step, lane) are in index order.  The CTA holding the crossing
     // point finds its warp, step and lane from those masses, and that lane
-    // re-reads only its four vectors.
+    // re-reads only its two vectors.
     for (int attempt = 0; attempt < 2 && S.kind != 0; ++attempt) {
       const int mm = S.m;
       const bool residual = S.kind == 1;
       const RowInfo &Rt = S.rows[S.trow[mm]];
       const RowInfo *Rd = residual ? &S.rows[S.drow[mm]] : nullptr;
       const bool d_vec = residual && Rd->hp == Rt.hp;  // same vector grid
+      RowInfo Rdt;  // otherwise: the draft row read element-wise on the target's grid
+      if (residual && !d_vec) {
+        Rdt = Rt;
+        Rdt.g = Rd->g;
+        Rdt.qlo = 1;
+        Rdt.qhi = 0;
+      }
       const float Ct = S.C[S.trow[mm]];
       const float Cd = residual ? S.C[S.drow[mm]] : 0.f;
       const float Rz =
           residual ? __fdiv_rn(ff_f(S.Z[S.trow[mm]]), ff_f(S.Z[S.drow[mm]])) : 0.f;
       const int wr = (Rt.nvec + NW - 1) / NW;  // vectors per warp
       const int wq0 = min(warp * wr, Rt.nvec), wq1 = min(wq0 + wr, Rt.nvec);
-      const int wsteps = (wq1 - wq0 + 32 * kU - 1) / (32 * kU);
-      // element weights of vector q of the target row (tvec) against the
-      // draft (dvec, or element loads when the draft row's grid differs)
-      auto vec_weights = [&](const uint4 &tvec, const uint4 &dvec, int q, float *w) {
-        float ft[NV], fd[NV];
-        Elt<E>::unpack(tvec, ft);
-        if (residual) {
-          if (d_vec) {
-            Elt<E>::unpack(dvec, fd);
-          } else {
-#pragma unroll
-            for (int i = 0; i < NV; ++i) {
-              const int e = elem_index(v0, Rt.hp, q, i, sz);
-              fd[i] = (e >= v0 && e < v1) ? Elt<E>::load_global(Rd->g + (int64_t)e * sz)
-                                          : -INFINITY;
-            }
-          }
-        }
-        pass_weights<E>(ft, fd, residual, Ct, Cd, s, Rz, w);
-      };
-      auto vec_mass = [&](const uint4 &tvec, const uint4 &dvec, int q) -> float {
-        float w[NV];
-        vec_weights(tvec, dvec, q, w);
-#pragma unroll
-        for (int h = NV / 2; h > 0; h >>= 1)
-#pragma unroll
-          for (int i = 0; i < h; ++i) w[i] += w[i + h];
-        return w[0];
-      };
+      const int wsteps = (wq1 - wq0 + 2 * 32 - 1) / (2 * 32);
       float *pmw = pmass + warp * L.pw * 32;  // [step][lane] masses of this warp
       {
-        // unit u: target step u / per, then (same vector grid) the draft step
         constexpr uint32_t kSlot = kU * NT * 16;
-        const int per = d_vec ? 2 : 1;
-        const int nunits = wsteps * per;
         int i_u = 0;
+        // step u: target vectors into ring vectors 0, 1; draft into 2, 3
         auto issue_pass = [&](int slot) {
-          if (i_u < nunits) {
-            const RowInfo &RR = (i_u % per == 0) ? Rt : *Rd;
-            const int t = i_u / per;
-#pragma unroll
-            for (int k = 0; k < kU; ++k)
-              issue_vec<NT>(RR, wq0 + t * 32 * kU + kU * lane + k, wq1, ring_t + slot * kSlot, k);
+          if (i_u < wsteps) {
+            const int qa = wq0 + i_u * 64 + 2 * lane;
+            const uint32_t sl = ring_t + slot * kSlot;
+            issue_vec<NT>(Rt, qa, wq1, sl, 0);
+            issue_vec<NT>(Rt, qa + 1, wq1, sl, 1);
+            if (d_vec) {
+              issue_vec<NT>(*Rd, qa, wq1, sl, 2);
+              issue_vec<NT>(*Rd, qa + 1, wq1, sl, 3);
+            }
             ++i_u;
           }
           cp_commit();
         };
-#pragma unroll
+#pragma unroll 1
         for (int d = 0; d < kDepth - 1; ++d) issue_pass(d);
         float tsum = 0.f, tcomp = 0.f;
-        uint4 tv4[kU];
-        for (int u = 0; u < nunits; ++u) {
+#pragma unroll 1
+        for (int u = 0; u < wsteps; ++u) {
           issue_pass((u + kDepth - 1) % kDepth);
           cp_wait<kDepth - 1>();
-          const int t = u / per;
           const uint8_t *slot = ring + (u % kDepth) * kSlot + tid * 16;
-          const int q0 = wq0 + t * 32 * kU + kU * lane;
-          if (u % per == 0) {
-#pragma unroll
-            for (int k = 0; k < kU; ++k) tv4[k] = fetch_vec<E, NT>(Rt, q0 + k, wq1, slot, k, v0, v1);
-            if (per == 2) continue;  // the draft unit follows
+          float ms = 0.f;
+#pragma unroll 1
+          for (int k = 0; k < 2; ++k) {
+            const int q = wq0 + u * 64 + 2 * lane + k;
+            if (q >= wq1) break;
+            const uint4 tv = fetch_vec<E, NT>(Rt, q, wq1, slot, k, v0, v1);
+            uint4 dv = tv;
+            if (residual)
+              dv = d_vec ? fetch_vec<E, NT>(*Rd, q, wq1, slot, 2 + k, v0, v1)
+                         : load_vec_slow<E>(Rdt, q, v0, v1);
+            ms += vec_mass<E>(tv, dv, residual, Ct, Cd, s, Rz);
           }
-          float vs[kU];
-#pragma unroll
-          for (int k = 0; k < kU; ++k) {
-            uint4 dvec = tv4[k];
-            if (d_vec) dvec = fetch_vec<E, NT>(*Rd, q0 + k, wq1, slot, k, v0, v1);
-            vs[k] = q0 + k < wq1 ? vec_mass(tv4[k], dvec, q0 + k) : 0.f;
-          }
-          const float ms = (vs[0] + vs[1]) + (vs[2] + vs[3]);
-          pmw[t * 32 + lane] = ms;
+          pmw[u * 32 + lane] = ms;
           kahan_add(tsum, tcomp, ms);
         }
         cp_wait<0>();
@@ -1480,30 +1470,29 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
         if (warp == S.wsel) {
           const ff tw = S.t_w;
           // the crossing step: step masses (lane t sums row t of the warp's
-          // [step][lane] masses pairwise, reading it rotated across the banks)
+          // [step][lane] masses, reading it rotated across the banks)
           int tsel = -1, tlast = -1;
           ff before{0.f, 0.f}, before_last{0.f, 0.f}, cum{0.f, 0.f};
+#pragma unroll 1
           for (int tb = 0; tb < wsteps && tsel < 0; tb += 32) {
             const int t = tb + lane;
-            float row[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) row[i] = t < wsteps ? pmw[t * 32 + ((i + lane) & 31)] : 0.f;
-#pragma unroll
-            for (int h = 16; h > 0; h >>= 1)
-#pragma unroll
-              for (int i = 0; i < h; ++i) row[i] += row[i + h];
-            const float mt = row[0];
-            const ff incl = ff_warp_scan(ff{mt, 0.f});
-            const unsigned cross = __ballot_sync(0xffffffffu, mt > 0.f && ff_gt(ff_add(cum, incl), tw));
-            const unsigned pos = __ballot_sync(0xffffffffu, mt > 0.f);
+            ff mt{0.f, 0.f};
+            if (t < wsteps) {
+#pragma unroll 1
+              for (int i = 0; i < 32; ++i) mt = ff_add_f(mt, pmw[t * 32 + ((i + lane) & 31)]);
+            }
+            const ff incl = ff_warp_scan(mt);
+            const unsigned cross =
+                __ballot_sync(0xffffffffu, ff_pos(mt) && ff_gt(ff_add(cum, incl), tw));
+            const unsigned pos = __ballot_sync(0xffffffffu, ff_pos(mt));
             if (cross) {
               const int l = __ffs(cross) - 1;
               tsel = tb + l;
-              before = ff_add(cum, ff_shfl(ff_add_f(incl, -mt), l));
+              before = ff_add(cum, ff_shfl(ff_sub(incl, mt), l));
             } else if (pos) {
               const int l = 31 - __clz(pos);
               tlast = tb + l;
-              before_last = ff_add(cum, ff_shfl(ff_add_f(incl, -mt), l));
+              before_last = ff_add(cum, ff_shfl(ff_sub(incl, mt), l));
             }
             cum = ff_add(cum, ff_shfl(incl, 31));
           }
@@ -1524,17 +1513,23 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
             if (lsel >= 0) before_l = ff_add(before, ff_shfl(ff_add_f(incl, -ml), lsel));
           }
           if (lsel >= 0 && lane == lsel) {
-            // the crossing lane's four vectors, element by element
-            const int q0 = wq0 + tsel * 32 * kU + kU * lane;
+            // the crossing lane's two vectors, element by element
+            const int q0 = wq0 + tsel * 64 + 2 * lane;
             int tok = -1, klast = -1;
             ff c2 = before_l;
-            for (int k = 0; k < kU && tok < 0; ++k) {
+#pragma unroll 1
+            for (int k = 0; k < 2 && tok < 0; ++k) {
               const int q = q0 + k;
               if (q >= wq1) break;
               const uint4 tvv = load_vec_direct<E>(Rt, q, v0, v1);
-              const uint4 dvv = d_vec ? load_vec_direct<E>(*Rd, q, v0, v1) : tvv;
-              float w[NV];
-              vec_weights(tvv, dvv, q, w);
+              uint4 dvv = tvv;
+              if (residual)
+                dvv = d_vec ? load_vec_direct<E>(*Rd, q, v0, v1) : load_vec_slow<E>(Rdt, q, v0, v1);
+              float ft[NV], fd[NV], w[NV];
+              Elt<E>::unpack(tvv, ft);
+              Elt<E>::unpack(dvv, fd);
+              pass_weights<E>(ft, fd, residual, Ct, Cd, s, Rz, w);
+#pragma unroll 1
               for (int i = 0; i < NV; ++i) {
                 const int e = elem_index(v0, Rt.hp, q, i, sz);
                 if (e < v0 || e >= v1 || !(w[i] > 0.f)) continue;
@@ -1587,19 +1582,6 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
           P.hit[b] = (uint8_t)h;
         }
       }
-      if (P.compact) {
-        // release: this thread's outputs above; acquire: every other
-        // sequence's, for the one that arrives last
-        int done;
-        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
-                     : "=r"(done) : "l"(P.done_counter) : "memory");
-        if (done == P.B - 1) S.flag_compact = 1;
-      }
-    }
-    __syncthreads();
-    if (S.flag_compact) {
-      compact_block(P.B, K, P.out_tokens, P.tau, P.offsets, P.packed, P.status, true, S.red_i);
-      if (tid == 0) *P.done_counter = 0;
     }
   }
   // No CTA touches another's shared memory after barrier (1) or (2), which
@@ -1608,6 +1590,17 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
 
 __global__ void sd_compact_kernel(int B, int K, const int32_t *out_tokens, const int32_t *tau,
                                   int32_t *offsets, int32_t *packed, int32_t *status) {
+  __shared__ int red[32];
+  compact_block(B, K, out_tokens, tau, offsets, packed, status, false, red);
+}
+
+// The packing step launched right behind the verify kernel as its
+// programmatic dependent: it may become resident early and waits here until
+// every verify CTA has finished and its writes are visible.
+__global__ void __launch_bounds__(1024) sd_compact_after_kernel(
+    int B, int K, const int32_t *out_tokens, const int32_t *tau, int32_t *offsets,
+    int32_t *packed, int32_t *status) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ int red[32];
   compact_block(B, K, out_tokens, tau, offsets, packed, status, false, red);
 }
@@ -1654,6 +1647,29 @@ static int rows_per_seq(const Params &P) {
   int n = P.mode == kVerify ? 2 * P.K + 1 : P.K;
   if (P.keys && P.bonus && P.fanout[P.K] > 0) n += 1;
   return std::max(n, 1);
+}
+
+// The packing of all sequences' tokens, as a programmatic dependent of the
+// verify launch just issued on the same stream.
+static sd_status_t launch_compact_after(const Params &P, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(1024, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, sd_compact_after_kernel, (int)P.B, (int)P.K,
+                                           (const int32_t *)P.out_tokens, (const int32_t *)P.tau,
+                                           P.offsets, P.packed, P.status);
+  if (e != cudaSuccess) {
+    fprintf(stderr, "sd_verify packing launch failed: %s\n", cudaGetErrorString(e));
+    return SD_ERR_CUDA;
+  }
+  return SD_OK;
 }
 
 // Vocabulary slice of one CTA for cluster size cs (a multiple of 16 elements).
@@ -1756,6 +1772,7 @@ static sd_status_t launch_nt(Params &P, cudaStream_t stream) {
     fprintf(stderr, "sd_verify launch failed: %s\n", cudaGetErrorString(e));
     return SD_ERR_CUDA;
   }
+  if (P.compact) return launch_compact_after(P, stream);
   return SD_OK;
 }
 
