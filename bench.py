@@ -305,7 +305,7 @@ def run_gpu(args):
                      "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                      "peak_source": pk_kind, "kernel": "sd_verify_kernel",
                      "algorithmic_bytes_per_launch": alg, "formula_bytes_per_launch": formula},
-        "gpu_launches": steps,
+        "gpu_launches": 2 * steps,  # the verify launch and the packing launch per step
         "clocks": clocks,
         "e2e": e2e,
         "hit_rate": hit_rate, "mean_tau": mean_tau, "status_bits": st,

@@ -126,18 +126,17 @@ typedef struct sd_verify_args {
   int32_t *target_argmax;/* [B][K+1]: top target token per position          */
   int32_t *status;       /* one int32, SD_STATUS_* bits OR-ed in             */
 
-  /* Scratch: at least sd_verify_workspace_size(B, K) bytes, 16-byte
-   * aligned, filled with zeros before its first use.  It holds per-row
-   * completion counters and per-position results; every call that returns
-   * SD_OK and whose status has no SD_STATUS_TIMEOUT bit leaves it all zero
-   * again, so the same buffer serves the next call on the same stream (any
-   * B and K that fit) without being cleared.  Calls that overlap on the GPU
-   * need separate workspaces. */
+  /* Scratch, reserved: the current kernels keep all intermediate state in
+   * on-chip memory and need none (sd_verify_workspace_size returns 0), so
+   * workspace may be NULL with workspace_bytes 0.  A non-NULL buffer must
+   * be 16-byte aligned and at least sd_verify_workspace_size(B, K) bytes;
+   * the library does not touch it. */
   void *workspace;
   size_t workspace_bytes;
 } sd_verify_args;
 
-/* Bytes of scratch sd_verify needs for a batch of B rows of K drafts. */
+/* Bytes of scratch sd_verify needs for a batch of B rows of K drafts (0 for
+ * the current kernels); 0 also for arguments out of range. */
 size_t sd_verify_workspace_size(int32_t B, int32_t K);
 
 /*
@@ -146,7 +145,10 @@ size_t sd_verify_workspace_size(int32_t B, int32_t K);
  * correction token from the residual at the first rejection or the bonus
  * token from target row K, tau, the optional hit test, and optionally the
  * outcome-prediction keys and the compaction of all rows' tokens.
- * Each logit row is read from memory once.
+ * Each logit row is streamed from memory once; the target and draft rows at
+ * the first rejection (or target row K) are read a second time for the
+ * draw, mostly from L2.  One kernel launch, plus a one-CTA packing launch
+ * with SD_FLAG_COMPACT (a programmatic dependent of the first, same stream).
  */
 sd_status_t sd_verify(const sd_verify_args *args, void *stream);
 

@@ -141,18 +141,20 @@ def workspace_bytes(B: int, K: int) -> int:
     return int(lib().sd_verify_workspace_size(B, K))
 
 
-def workspace(B: int, K: int, device=None, stream=None) -> torch.Tensor:
-    """A zero-filled scratch buffer for sd_verify, cached per (device,
-    stream).  The library leaves it zeroed after every successful call, so
-    it is cleared only once."""
+def workspace(B: int, K: int, device=None, stream=None):
+    """Scratch for sd_verify: None while the library needs none
+    (sd_verify_workspace_size == 0), else a zero-filled buffer cached per
+    (device, stream)."""
+    need = workspace_bytes(B, K)
+    if need == 0:
+        return None
     device = torch.device(device if device is not None else torch.cuda.current_device())
     s = stream if stream is not None else torch.cuda.current_stream(device)
-    need = workspace_bytes(B, K)
     key = (device.index, s.cuda_stream)
     with _ws_lock:
         buf = _ws.get(key)
         if buf is None or buf.numel() < need:
-            buf = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=device)
+            buf = torch.zeros(need, dtype=torch.uint8, device=device)
             _ws[key] = buf
     return buf
 
@@ -256,7 +258,8 @@ def verify(target, draft, tokens, temperature, seed: int, *, row_base: int = 0,
                                                 r.q_draft.data_ptr())
         a.target_argmax = r.target_argmax.data_ptr()
     a.status = r.status.data_ptr() if r.status is not None else None
-    a.workspace, a.workspace_bytes = w.data_ptr(), w.numel()
+    if w is not None:
+        a.workspace, a.workspace_bytes = w.data_ptr(), w.numel()
     _check(lib().sd_verify(ctypes.byref(a), _stream(dev, stream)), "sd_verify")
     return r
 

@@ -53,7 +53,7 @@ namespace cg = cooperative_groups;
 namespace sdv {
 
 constexpr int kU = 4;                        // 16-byte vectors per thread per step
-constexpr int kDepth = 3;                    // steps in each thread's copy ring
+constexpr int kDepth = 4;                    // steps in each thread's copy ring
 constexpr int kMaxWarps = 16;                // threads per CTA <= 512
 constexpr int kMaxCS = 16;                   // cluster size limit
 constexpr int kMaxRows = 2 * SD_MAX_K + 2;   // K+1 target, K draft, 1 bonus
@@ -80,7 +80,6 @@ struct Params {
   float *ratio_out, *p_out, *q_out;
   int32_t *argmax_out;
   int32_t *status;
-  int32_t *done_counter;   // workspace
   uint64_t seed;
   int64_t row_base;
   int32_t B, K, V;
@@ -174,6 +173,7 @@ __device__ __forceinline__ bool ff_gt(ff x, ff y) {
 __device__ __forceinline__ bool ff_pos(ff x) { return x.hi > 0.f; }
 __device__ __forceinline__ float ff_f(ff x) { return x.hi + x.lo; }
 __device__ __forceinline__ ff ff_shfl(ff x, int src) {
+  __syncwarp();
   return ff{__shfl_sync(0xffffffffu, x.hi, src), __shfl_sync(0xffffffffu, x.lo, src)};
 }
 __device__ __forceinline__ ff ff_shfl_up(ff x, int o) {
@@ -185,14 +185,18 @@ __device__ __forceinline__ ff ff_shfl_xor(ff x, int o) {
 // inclusive warp scan and warp sum
 __device__ __noinline__ ff ff_warp_scan(ff x) {
   const int lane = threadIdx.x & 31;
+  __syncwarp();
 #pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
-    const ff y = ff_shfl_up(x, o);
-    if (lane >= o) x = ff_add(x, y);
+    ff y = ff_shfl_up(x, o);
+    y.hi = lane >= o ? y.hi : 0.f;  // adding (0, 0) leaves x as it is
+    y.lo = lane >= o ? y.lo : 0.f;
+    x = ff_add(x, y);
   }
   return x;
 }
 __device__ __noinline__ ff ff_warp_sum(ff x) {
+  __syncwarp();
 #pragma unroll 1
   for (int o = 16; o > 0; o >>= 1) x = ff_add(x, ff_shfl_xor(x, o));
   return x;
@@ -234,16 +238,19 @@ __device__ __forceinline__ void kahan_add(float &sum, float &comp, float v) {
 }
 
 __device__ __forceinline__ float warp_max(float v) {
+  __syncwarp();
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 __device__ __forceinline__ float warp_sum(float v) {
+  __syncwarp();
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 __device__ __forceinline__ int warp_min_i(int v) {
+  __syncwarp();
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
@@ -277,9 +284,26 @@ __device__ __forceinline__ int ford(float x) {
   return i >= 0 ? i : (i == (int)0x80000000 ? 0 : (i ^ 0x7fffffff));
 }
 __device__ __forceinline__ float fdeord(int i) { return __int_as_float(i >= 0 ? i : (i ^ 0x7fffffff)); }
-__device__ __forceinline__ float rmax_f(float x) { return fdeord(__reduce_max_sync(0xffffffffu, ford(x))); }
-__device__ __forceinline__ float rmin_f(float x) { return fdeord(__reduce_min_sync(0xffffffffu, ford(x))); }
-__device__ __forceinline__ int rmin_i(int x) { return __reduce_min_sync(0xffffffffu, x); }
+// Every warp-collective helper below first reconverges the warp: lanes that
+// took different sides of an earlier branch may otherwise reach the
+// collective separately, and each such collective then costs hundreds of
+// cycles.
+__device__ __forceinline__ float rmax_f(float x) {
+  __syncwarp();
+  return fdeord(__reduce_max_sync(0xffffffffu, ford(x)));
+}
+__device__ __forceinline__ float rmin_f(float x) {
+  __syncwarp();
+  return fdeord(__reduce_min_sync(0xffffffffu, ford(x)));
+}
+__device__ __forceinline__ int rmin_i(int x) {
+  __syncwarp();
+  return __reduce_min_sync(0xffffffffu, x);
+}
+__device__ __forceinline__ unsigned ballot(bool p) {
+  __syncwarp();
+  return __ballot_sync(0xffffffffu, p);
+}
 
 // Warp-wide best (value desc, then index asc) of one candidate per lane.
 __device__ __forceinline__ void warp_best(float &v, int &i) {
@@ -586,19 +610,21 @@ __device__ void compact_block(int B, int K, const int32_t *out_tokens, const int
       }
     }
     int x = t;  // inclusive warp scan
+    __syncwarp();
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+      x += lane >= o ? y : 0;
     }
     if (lane == 31) red[w] = x;
     __syncthreads();
     if (w == 0) {
       int v = lane < nw ? red[lane] : 0;
+      __syncwarp();
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += y;
+        v += lane >= o ? y : 0;
       }
       if (lane < nw) red[lane] = v;  // inclusive warp totals
     }
@@ -775,7 +801,7 @@ __device__ __forceinline__ void step_body(RowAcc<KF> &A, const uint4 (&v)[kU], i
 #pragma unroll
         for (int r = 0; r < KF; ++r) {
           th = rmax_f(x);
-          const unsigned w = __ballot_sync(0xffffffffu, x == th);
+          const unsigned w = ballot(x == th);
           if (lane == __ffs(w) - 1) x = -INFINITY;
         }
         A.theta = th;
@@ -1031,7 +1057,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
     const bool act = l < K;
     const int fj = (act && P.keys) ? P.fanout[j] : 0;
     const bool dpres = act && (sampled || fj > 0);
-    const unsigned dm = __ballot_sync(0xffffffffu, dpres);
+    const unsigned dm = ballot(dpres);
     const int d = d_pre;
     if (act) S.d[j] = d;
     const bool dok = !act || (d >= 0 && d < P.V);
@@ -1326,7 +1352,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
         }
         rej = !a;
       }
-      const unsigned rejects = __ballot_sync(0xffffffffu, rej);
+      const unsigned rejects = ballot(rej);
       if (lane == 0) {
         const int mm = rejects ? __ffs(rejects) - 1 : K;
         S.m = mm;
@@ -1434,8 +1460,8 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
         if (ff_pos(tot) || !residual) {
           const float u = uniform_u(P.seed, P.row_base + b, mm, 1);
           const ff t = ff_mul_f(tot, u);
-          const unsigned cross = __ballot_sync(0xffffffffu, ff_pos(sc) && ff_gt(incl, t));
-          const unsigned pos = __ballot_sync(0xffffffffu, ff_pos(sc));
+          const unsigned cross = ballot(ff_pos(sc) && ff_gt(incl, t));
+          const unsigned pos = ballot(ff_pos(sc));
           // the first CTA whose range passes t; if rounding put t past the
           // total, the last CTA with mass
           const int cstar = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : 0);
@@ -1458,8 +1484,8 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
           const ff m_l = lane < NW ? S.wmass[lane] : ff{0.f, 0.f};
           const ff pre = lane < NW ? S.wpre[lane] : ff{0.f, 0.f};
           const unsigned cross =
-              __ballot_sync(0xffffffffu, ff_pos(m_l) && ff_gt(ff_add(pre, m_l), S.t_loc));
-          const unsigned pos = __ballot_sync(0xffffffffu, ff_pos(m_l));
+              ballot(ff_pos(m_l) && ff_gt(ff_add(pre, m_l), S.t_loc));
+          const unsigned pos = ballot(ff_pos(m_l));
           const int ws = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : 0);
           if (lane == 0) {
             S.wsel = ws;
@@ -1483,8 +1509,8 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
             }
             const ff incl = ff_warp_scan(mt);
             const unsigned cross =
-                __ballot_sync(0xffffffffu, ff_pos(mt) && ff_gt(ff_add(cum, incl), tw));
-            const unsigned pos = __ballot_sync(0xffffffffu, ff_pos(mt));
+                ballot(ff_pos(mt) && ff_gt(ff_add(cum, incl), tw));
+            const unsigned pos = ballot(ff_pos(mt));
             if (cross) {
               const int l = __ffs(cross) - 1;
               tsel = tb + l;
@@ -1507,8 +1533,8 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
             const float ml = pmw[tsel * 32 + lane];
             const ff incl = ff_warp_scan(ff{ml, 0.f});
             const unsigned cross =
-                __ballot_sync(0xffffffffu, ml > 0.f && ff_gt(ff_add(before, incl), tw));
-            const unsigned pos = __ballot_sync(0xffffffffu, ml > 0.f);
+                ballot(ml > 0.f && ff_gt(ff_add(before, incl), tw));
+            const unsigned pos = ballot(ml > 0.f);
             lsel = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : -1);
             if (lsel >= 0) before_l = ff_add(before, ff_shfl(ff_add_f(incl, -ml), lsel));
           }
@@ -1808,8 +1834,9 @@ using namespace sdv;
 extern "C" {
 
 size_t sd_verify_workspace_size(int32_t B, int32_t K) {
-  if (B < 0 || K < 0 || K > SD_MAX_K) return 0;
-  return 256;  // one completion counter, padded
+  (void)B;
+  (void)K;
+  return 0;  // all intermediate state stays on chip
 }
 
 sd_status_t sd_verify(const sd_verify_args *a, void *stream) {
@@ -1832,9 +1859,7 @@ sd_status_t sd_verify(const sd_verify_args *a, void *stream) {
     return SD_ERR_INVALID_ARG;
   if (a->K > 0 && (!a->draft_logits || !a->draft_tokens)) return SD_ERR_INVALID_ARG;
   if (compact && !a->packed) return SD_ERR_INVALID_ARG;
-  if (!a->workspace || !aligned(a->workspace, 16) ||
-      a->workspace_bytes < sd_verify_workspace_size(a->B, a->K))
-    return SD_ERR_INVALID_ARG;
+  if (a->workspace && !aligned(a->workspace, 16)) return SD_ERR_INVALID_ARG;
   if (a->cache_keys && a->n_keys < 0) return SD_ERR_INVALID_ARG;
   const size_t esz = a->dtype == SD_BF16 ? 2 : 4;
   if (!aligned(a->target_logits, esz) || (a->draft_logits && !aligned(a->draft_logits, esz)))
@@ -1864,7 +1889,6 @@ sd_status_t sd_verify(const sd_verify_args *a, void *stream) {
   P.K = a->K;
   P.V = a->V;
   P.compact = compact ? 1 : 0;
-  P.done_counter = (int32_t *)a->workspace;
   if (predict) {
     if (!a->fanout_host || !a->keys_out) return SD_ERR_INVALID_ARG;
     if (a->draft_bonus_logits && !aligned(a->draft_bonus_logits, esz)) return SD_ERR_INVALID_ARG;

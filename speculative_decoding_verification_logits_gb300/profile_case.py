@@ -1,0 +1,36 @@
+"""Run a few verify rounds of one synthetic workload (for profilers).
+
+    python -m speculative_decoding_verification_logits_gb300.profile_case WORKLOAD [ROUNDS]
+
+Two input sets of the workload alternate; every round is one fused verify
+launch (plus the packing launch).  Prints the mean tau of the last round.
+"""
+import os
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+import torch  # noqa: E402
+
+import sd_workloads as W  # noqa: E402
+import speculative_decoding_verification_logits_gb300 as sd  # noqa: E402
+
+
+def main():
+    name = sys.argv[1] if len(sys.argv) > 1 else "saguaro"
+    n = int(sys.argv[2]) if len(sys.argv) > 2 else 4
+    dev = torch.device("cuda:0")
+    spec = W.WORKLOADS[name]
+    fan = spec.get("fanout")
+    pool = [W.workload(name, round_idx=i, device=dev) for i in range(2)]
+    r = None
+    for i in range(n):
+        p = pool[i % 2]
+        r = sd.verify(p.target, p.draft, p.tokens, p.temperature, p.seed + i, fanout=fan,
+                      draft_bonus=p.draft_bonus, compact=True)
+    torch.cuda.synchronize()
+    print("ok", r.tau.float().mean().item())
+
+
+if __name__ == "__main__":
+    main()

@@ -227,26 +227,24 @@ def test_invalid_rows_set_status_and_empty_batch(dev):
     assert r0.offsets.tolist() == [0]
 
 
-def test_workspace_is_left_zeroed_and_reusable(dev):
+def test_repeated_calls_and_optional_scratch(dev):
+    # back-to-back calls on one stream give identical results; an unused
+    # scratch buffer, if passed, is left untouched
     B, K, V = 8, 5, 5000
     inp = W.synth(B, K, V, "bf16", kind="peaked", peaks=4, temperature=0.8, seed=21, device=dev)
-    ws = torch.zeros(sd.workspace_bytes(B, K), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
     a = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, ws=ws,
                   compact=True)
+    b = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, compact=True)
     torch.cuda.synchronize()
-    b = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, ws=ws,
-                  compact=True)
     n = int(a.offsets[-1])
     assert torch.equal(a.out_tokens, b.out_tokens) and torch.equal(a.packed[:n], b.packed[:n])
-    torch.cuda.synchronize()
     assert int(ws.count_nonzero().item()) == 0
-    # a smaller batch with another K reuses the same buffer
+    # then a smaller batch with another K and dtype
     inp2 = W.synth(3, 2, 777, "f32", temperature=[0.0, 1.0, 0.5], seed=2, device=dev)
-    c = sd.verify(inp2.target, inp2.draft, inp2.tokens, inp2.temperature, inp2.seed, ws=ws)
+    c = sd.verify(inp2.target, inp2.draft, inp2.tokens, inp2.temperature, inp2.seed)
     o = _oracle_for(inp2)
     _check(*compare_verify(c, o, inp2.temperature.cpu().numpy(), check_stats=False))
-    torch.cuda.synchronize()
-    assert int(ws.count_nonzero().item()) == 0
 
 
 def test_row_base_splits_batch_identically(dev):
