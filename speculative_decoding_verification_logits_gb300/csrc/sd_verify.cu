@@ -643,34 +643,54 @@ __device__ void compact_block(int B, int K, const int32_t *out_tokens, const int
 
 
 // ------------------------------------------------------------ streaming --
-// Weights of the sampling pass for the elements of one target vector:
-// residual Zt (p - q)+ = max(0, 2^(l s + Ct) - 2^(l' s + Cd) R), R = Zt / Zd,
-// or Zt p = 2^(l s + Ct) for a draw from p.
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Weights of the sampling pass for the elements of one target vector, two
+// lanes per instruction: the residual Zt (p - q)+ =
+// max(0, 2^(l s + Ct) - 2^(l' s + Cd + log2 R)) with R = Zt / Zd (cd2 holds
+// Cd + log2 R), or Zt p = 2^(l s + Ct) for a draw from p.
 template <typename E>
-__device__ __forceinline__ void pass_weights(const float *ft, const float *fd, bool residual,
-                                             float Ct, float Cd, float s, float R, float *w) {
+__device__ __forceinline__ void pass_weights(const uint4 &tv, const uint4 &dv, bool residual,
+                                             uint64_t s2, uint64_t ct2, uint64_t cd2, float *w) {
   constexpr int N = Elt<E>::kPerVec;
+  float ft[N], fd[N];
+  Elt<E>::unpack(tv, ft);
+  Elt<E>::unpack(dv, fd);
 #pragma unroll
-  for (int k = 0; k < N; ++k) {
-    const float pt = ex2(fmaf(ft[k], s, Ct));
-    w[k] = residual ? fmaxf(0.f, pt - ex2(fmaf(fd[k], s, Cd)) * R) : pt;
+  for (int i = 0; i < N; i += 2) {
+    float a, b;
+    upk2(fma2(pk2(ft[i], ft[i + 1]), s2, ct2), a, b);
+    uint64_t p = pk2(ex2(a), ex2(b));
+    if (residual) {
+      float c, d;
+      upk2(fma2(pk2(fd[i], fd[i + 1]), s2, cd2), c, d);
+      p = sub2(p, pk2(ex2(c), ex2(d)));
+    }
+    upk2(p, w[i], w[i + 1]);
+    if (residual) {
+      w[i] = fmaxf(0.f, w[i]);
+      w[i + 1] = fmaxf(0.f, w[i + 1]);
+    }
   }
 }
 
 // Mass of one target vector in the sampling pass (sum of its weights).
 template <typename E>
-__device__ __noinline__ float vec_mass(uint4 tv, uint4 dv, bool residual, float Ct, float Cd,
-                                       float s, float R) {
+__device__ __forceinline__ float vec_mass(const uint4 &tv, const uint4 &dv, bool residual,
+                                          uint64_t s2, uint64_t ct2, uint64_t cd2) {
   constexpr int N = Elt<E>::kPerVec;
-  float ft[N], fd[N], w[N];
-  Elt<E>::unpack(tv, ft);
-  Elt<E>::unpack(dv, fd);
-  pass_weights<E>(ft, fd, residual, Ct, Cd, s, R, w);
+  float w[N];
+  pass_weights<E>(tv, dv, residual, s2, ct2, cd2, w);
+  uint64_t acc = pk2(w[0], w[1]);
 #pragma unroll
-  for (int h = N / 2; h > 0; h >>= 1)
-#pragma unroll
-    for (int i = 0; i < h; ++i) w[i] += w[i + h];
-  return w[0];
+  for (int i = 2; i < N; i += 2) acc = add2(acc, pk2(w[i], w[i + 1]));
+  float lo, hi;
+  upk2(acc, lo, hi);
+  return lo + hi;
 }
 
 // Per-thread state of the row being streamed.
@@ -1394,6 +1414,9 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       const float Cd = residual ? S.C[S.drow[mm]] : 0.f;
       const float Rz =
           residual ? __fdiv_rn(ff_f(S.Z[S.trow[mm]]), ff_f(S.Z[S.drow[mm]])) : 0.f;
+      const uint64_t s2 = pk2(s, s), ct2 = pk2(Ct, Ct);
+      const float cdr = residual ? Cd + __log2f(Rz) : 0.f;  // the draft weight scaled by R
+      const uint64_t cd2 = pk2(cdr, cdr);
       const int wr = (Rt.nvec + NW - 1) / NW;  // vectors per warp
       const int wq0 = min(warp * wr, Rt.nvec), wq1 = min(wq0 + wr, Rt.nvec);
       const int wsteps = (wq1 - wq0 + 2 * 32 - 1) / (2 * 32);
@@ -1434,7 +1457,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
             if (residual)
               dv = d_vec ? fetch_vec<E, NT>(*Rd, q, wq1, slot, 2 + k, v0, v1)
                          : load_vec_slow<E>(Rdt, q, v0, v1);
-            ms += vec_mass<E>(tv, dv, residual, Ct, Cd, s, Rz);
+            ms += vec_mass<E>(tv, dv, residual, s2, ct2, cd2);
           }
           pmw[u * 32 + lane] = ms;
           kahan_add(tsum, tcomp, ms);
@@ -1551,10 +1574,8 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
               uint4 dvv = tvv;
               if (residual)
                 dvv = d_vec ? load_vec_direct<E>(*Rd, q, v0, v1) : load_vec_slow<E>(Rdt, q, v0, v1);
-              float ft[NV], fd[NV], w[NV];
-              Elt<E>::unpack(tvv, ft);
-              Elt<E>::unpack(dvv, fd);
-              pass_weights<E>(ft, fd, residual, Ct, Cd, s, Rz, w);
+              float w[NV];
+              pass_weights<E>(tvv, dvv, residual, s2, ct2, cd2, w);
 #pragma unroll 1
               for (int i = 0; i < NV; ++i) {
                 const int e = elem_index(v0, Rt.hp, q, i, sz);
@@ -1699,11 +1720,21 @@ static sd_status_t launch_compact_after(const Params &P, cudaStream_t stream) {
 }
 
 // Vocabulary slice of one CTA for cluster size cs (a multiple of 16 elements).
-static int slice_for(int V, int cs) { return (int)((((int64_t)V + cs - 1) / cs + 15) / 16 * 16); }
+// Whole streaming steps (NT kU vectors) per slice where that still leaves
+// every CTA some vocabulary, so only the last CTA of a cluster meets a
+// partial step; otherwise a multiple of 16 elements.
+static int slice_for(int V, int cs, int sz, int NT) {
+  const int64_t even = ((int64_t)V + cs - 1) / cs;
+  const int64_t step = (int64_t)NT * kU * 16 / sz;
+  const int64_t whole = (even + step - 1) / step * step;
+  if ((cs - 1) * whole < V) return (int)whole;
+  return (int)((even + 15) / 16 * 16);
+}
 
 template <typename E, int KF, int NT>
 static int smem_bytes(const Params &P, int cs) {
-  return make_layout(NT, rows_per_seq(P), P.K + 1, KF, cs, slice_for(P.V, cs), Elt<E>::kSize)
+  return make_layout(NT, rows_per_seq(P), P.K + 1, KF, cs, slice_for(P.V, cs, Elt<E>::kSize, NT),
+                     Elt<E>::kSize)
       .total;
 }
 
@@ -1774,7 +1805,7 @@ static sd_status_t launch_nt(Params &P, cudaStream_t stream) {
   const int cs = choose_cs<E, KF, NT>(P);
   if (cs < 1 || cs > kMaxCS) return SD_ERR_INVALID_ARG;
   P.cs = cs;
-  P.slice = slice_for(P.V, cs);
+  P.slice = slice_for(P.V, cs, sz, NT);
   const Layout L = make_layout(NT, rows_per_seq(P), P.K + 1, KF, cs, P.slice, sz);
   if (L.total > kDynSmemCap) return SD_ERR_UNSUPPORTED;
   void *fn = kernel_fn<E, KF, NT>();
