@@ -53,7 +53,7 @@ namespace cg = cooperative_groups;
 namespace sdv {
 
 constexpr int kU = 4;                        // 16-byte vectors per thread per step
-constexpr int kDepth = 4;                    // steps in each thread's copy ring
+constexpr int kDepth = 3;                    // steps in each thread's copy ring
 constexpr int kMaxWarps = 16;                // threads per CTA <= 512
 constexpr int kMaxCS = 16;                   // cluster size limit
 constexpr int kMaxRows = 2 * SD_MAX_K + 2;   // K+1 target, K draft, 1 bonus
@@ -1423,17 +1423,24 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       float *pmw = pmass + warp * L.pw * 32;  // [step][lane] masses of this warp
       {
         constexpr uint32_t kSlot = kU * NT * 16;
+        // step u: target vectors into ring vectors 0, 1; draft into 2, 3.  The
+        // rows' fields are kept in registers: the copy instructions clobber
+        // memory, so fields read through a reference would be reloaded.
+        const uint8_t *const tg = Rt.gbase;
+        const uint8_t *const dg = d_vec ? Rd->gbase : Rt.gbase;
+        const int tlo = max(Rt.qlo, wq0), thi = min(Rt.qhi, wq1);  // vectors copied whole
         int i_u = 0;
-        // step u: target vectors into ring vectors 0, 1; draft into 2, 3
         auto issue_pass = [&](int slot) {
           if (i_u < wsteps) {
             const int qa = wq0 + i_u * 64 + 2 * lane;
             const uint32_t sl = ring_t + slot * kSlot;
-            issue_vec<NT>(Rt, qa, wq1, sl, 0);
-            issue_vec<NT>(Rt, qa + 1, wq1, sl, 1);
-            if (d_vec) {
-              issue_vec<NT>(*Rd, qa, wq1, sl, 2);
-              issue_vec<NT>(*Rd, qa + 1, wq1, sl, 3);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int q = qa + k;
+              if (q >= tlo && q < thi) {
+                cp_async16(sl + k * NT * 16, tg + 16 * q);
+                if (d_vec) cp_async16(sl + (2 + k) * NT * 16, dg + 16 * q);
+              }
             }
             ++i_u;
           }
@@ -1448,16 +1455,21 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
           cp_wait<kDepth - 1>();
           const uint8_t *slot = ring + (u % kDepth) * kSlot + tid * 16;
           float ms = 0.f;
-#pragma unroll 1
+#pragma unroll
           for (int k = 0; k < 2; ++k) {
             const int q = wq0 + u * 64 + 2 * lane + k;
-            if (q >= wq1) break;
-            const uint4 tv = fetch_vec<E, NT>(Rt, q, wq1, slot, k, v0, v1);
-            uint4 dv = tv;
-            if (residual)
-              dv = d_vec ? fetch_vec<E, NT>(*Rd, q, wq1, slot, 2 + k, v0, v1)
-                         : load_vec_slow<E>(Rdt, q, v0, v1);
-            ms += vec_mass<E>(tv, dv, residual, s2, ct2, cd2);
+            if (q < wq1) {
+              uint4 tv, dv;
+              if (q >= tlo && q < thi) {
+                tv = *reinterpret_cast<const uint4 *>(slot + k * NT * 16);
+                dv = d_vec ? *reinterpret_cast<const uint4 *>(slot + (2 + k) * NT * 16) : tv;
+              } else {
+                tv = load_vec_slow<E>(Rt, q, v0, v1);
+                dv = d_vec ? load_vec_slow<E>(*Rd, q, v0, v1) : tv;
+              }
+              if (residual && !d_vec) dv = load_vec_slow<E>(Rdt, q, v0, v1);
+              ms += vec_mass<E>(tv, dv, residual, s2, ct2, cd2);
+            }
           }
           pmw[u * 32 + lane] = ms;
           kahan_add(tsum, tcomp, ms);
