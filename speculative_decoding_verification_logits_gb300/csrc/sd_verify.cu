@@ -826,20 +826,23 @@ __device__ __forceinline__ void step_body(RowAcc<KF> &A, const uint4 (&v)[kU], i
         }
         A.theta = th;
       }
+      const float vbest = fmaxf(fmaxf(vm[0], vm[1]), fmaxf(vm[2], vm[3]));
+      if (vbest > A.kv[KF - 1] && vbest >= A.theta) {  // rare once the row is under way
 #pragma unroll
-      for (int k = 0; k < kU; ++k) {
-        if (vm[k] > A.kv[KF - 1] && vm[k] >= A.theta) {
-          A.kv[KF - 1] = vm[k];
-          A.kq[KF - 1] = qbase + k * NT;
+        for (int k = 0; k < kU; ++k) {
+          if (vm[k] > A.kv[KF - 1] && vm[k] >= A.theta) {
+            A.kv[KF - 1] = vm[k];
+            A.kq[KF - 1] = qbase + k * NT;
 #pragma unroll
-          for (int x = KF - 1; x > 0; --x) {
-            if (A.kv[x] > A.kv[x - 1]) {  // later vectors lose ties
-              const float t1 = A.kv[x];
-              A.kv[x] = A.kv[x - 1];
-              A.kv[x - 1] = t1;
-              const int t2 = A.kq[x];
-              A.kq[x] = A.kq[x - 1];
-              A.kq[x - 1] = t2;
+            for (int x = KF - 1; x > 0; --x) {
+              if (A.kv[x] > A.kv[x - 1]) {  // later vectors lose ties
+                const float t1 = A.kv[x];
+                A.kv[x] = A.kv[x - 1];
+                A.kv[x - 1] = t1;
+                const int t2 = A.kq[x];
+                A.kq[x] = A.kq[x - 1];
+                A.kq[x - 1] = t2;
+              }
             }
           }
         }
