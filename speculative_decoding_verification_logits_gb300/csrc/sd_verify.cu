@@ -87,7 +87,8 @@ struct Params {
   int32_t keys;            // build keys in this pass
   int32_t compact;
   int32_t n_keys_in, n_keys_out;
-  int32_t cs, slice;       // cluster size, vocabulary slice per CTA
+  int32_t cs, slice;       // cluster size, vocabulary slice per CTA (draw pass)
+  int32_t rowsplit;        // stream split: 1 row-major over the sequence, 0 by slice
   int32_t fanout[SD_MAX_K + 1];
   int32_t fan_off[SD_MAX_K + 2];
 };
@@ -380,6 +381,7 @@ enum RowType : int { kRowE = 0, kRowEA = 1, kRowA = 2, kRowK = 3, kRowEK = 4 };
 struct RowInfo {
   const uint8_t *g;      // element 0 of the row
   const uint8_t *gbase;  // 16-byte boundary at or below element v0
+  int v0, v1;            // the elements [v0, v1) of the row this CTA covers
   int kind, j, type;     // RowKind, position, RowType
   int excl;              // token excluded from the keys (-1: none)
   int fan;               // keys wanted from this row
@@ -395,6 +397,8 @@ template <int NT>
 __device__ __noinline__ void row_geometry(RowInfo &R, int v0, int v1, int sz) {
   constexpr int kStepVec = NT * kU;
   R.gbase = R.g;
+  R.v0 = v0;
+  R.v1 = v1;
   R.hp = R.nvec = R.nsteps = R.qlo = R.qhi = R.sf0 = R.sf1 = 0;
   R.qd = R.qd_step = -1;
   if (v1 <= v0) return;
@@ -532,6 +536,7 @@ struct Static {
   ff Z[kMaxRows];
   int amax[kMaxRows];      //   lowest index of the max
   int2 keys[(SD_MAX_K + 1) * SD_MAX_FANOUT];  // this sequence's keys (fused prediction)
+  RowInfo dt, dd;             // draw: target and draft row at m on the vocabulary slice
   int m, kind, owner, valid;  // kind: 0 none, 1 residual at m, 2 from p at m
   ff t_loc;
   int cstar;
@@ -1095,7 +1100,6 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       R.type = sampled ? (fj > 0 ? kRowEK : kRowE) : kRowK;
       R.excl = d;
       R.fan = fj;
-      row_geometry<NT>(R, v0, v1, sz);
       S.drow[j] = r_d;
     } else if (act) {
       S.drow[j] = -1;
@@ -1108,7 +1112,6 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       R.type = sampled ? (P.argmax_out ? kRowEA : kRowE) : kRowA;
       R.excl = -1;
       R.fan = 0;
-      row_geometry<NT>(R, v0, v1, sz);
       S.trow[j] = r_t;
     }
     if (act && sampled && dvalid) {
@@ -1128,7 +1131,6 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       R.type = kRowK;
       R.excl = -1;
       R.fan = P.fanout[K];
-      row_geometry<NT>(R, v0, v1, sz);
       S.drow[K] = 0;
     } else if (lane == 0) {
       S.drow[K] = -1;
@@ -1141,13 +1143,35 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       R.type = sampled ? (P.argmax_out ? kRowEA : kRowE) : kRowA;
       R.excl = -1;
       R.fan = 0;
-      row_geometry<NT>(R, v0, v1, sz);
       S.trow[K] = has_bonus ? 1 : 0;
     }
   }
   __syncthreads();
 
   const int nrows = S.nrows;
+  // ---- the part of each row this CTA streams: either the vocabulary slice
+  // [v0, v1) of every row, or an equal share of the sequence's rows laid end
+  // to end in stream order, cut at whole streaming steps of a row (a few row
+  // pieces per CTA instead of a piece of every row)
+  if (tid < nrows) {
+    RowInfo &R = S.rows[tid];
+    if (P.rowsplit) {
+      constexpr int ue = NT * kU * 16 / sz;  // elements per streaming step
+      const int spr = (P.V + ue - 1) / ue;   // steps per row
+      const int64_t U = (int64_t)nrows * spr;
+      const int64_t u_lo = U * rank / cs, u_hi = U * (rank + 1) / cs;
+      const int64_t r0 = (int64_t)tid * spr;
+      const int64_t a = (u_lo > r0 ? u_lo : r0) - r0;
+      const int64_t e = (u_hi < r0 + spr ? u_hi : r0 + spr) - r0;
+      R.v0 = e > a ? (int)(a * ue) : 0;
+      R.v1 = e > a ? (int)(e * ue < P.V ? e * ue : (int64_t)P.V) : 0;
+    } else {
+      R.v0 = v0;
+      R.v1 = v1;
+    }
+    row_geometry<NT>(R, R.v0, R.v1, sz);
+  }
+  __syncthreads();
   const int npos = K + 1;
   const Layout L = make_layout(NT, nrows, npos, KF, cs, P.slice, sz);
   uint8_t *ring = dyn + L.ring;
@@ -1182,25 +1206,25 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       }
       switch (R.type) {
         case kRowE:
-          stream_row<E, KF, NT, true, false, false>(A, R, I, S, nrows, ring, ring_t, c_off, v0, v1,
+          stream_row<E, KF, NT, true, false, false>(A, R, I, S, nrows, ring, ring_t, c_off, R.v0, R.v1,
                                                    s, s2, ws, wk);
           break;
         case kRowEA:
-          stream_row<E, KF, NT, true, true, false>(A, R, I, S, nrows, ring, ring_t, c_off, v0, v1,
+          stream_row<E, KF, NT, true, true, false>(A, R, I, S, nrows, ring, ring_t, c_off, R.v0, R.v1,
                                                   s, s2, ws, wk);
           break;
         case kRowA:
-          stream_row<E, KF, NT, false, true, false>(A, R, I, S, nrows, ring, ring_t, c_off, v0,
-                                                   v1, s, s2, ws, wk);
+          stream_row<E, KF, NT, false, true, false>(A, R, I, S, nrows, ring, ring_t, c_off, R.v0,
+                                                   R.v1, s, s2, ws, wk);
           break;
         default:
           if (KF > 0) {
             if (R.type == kRowK)
               stream_row<E, KF, NT, false, false, (KF > 0)>(A, R, I, S, nrows, ring, ring_t, c_off,
-                                                            v0, v1, s, s2, ws, wk);
+                                                            R.v0, R.v1, s, s2, ws, wk);
             else
               stream_row<E, KF, NT, true, false, (KF > 0)>(A, R, I, S, nrows, ring, ring_t, c_off,
-                                                           v0, v1, s, s2, ws, wk);
+                                                           R.v0, R.v1, s, s2, ws, wk);
           }
           break;
       }
@@ -1252,7 +1276,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       // the CTA's keys staged in the idle ring, then pushed to every CTA
       float2 *stage = reinterpret_cast<float2 *>(ring) + R.j * KFm;
       if (R.nsteps > 0) {
-        cta_keys<E, KFm, NT>(R, &wsel[R.j * NW * KFm], v0, v1, stage);
+        cta_keys<E, KFm, NT>(R, &wsel[R.j * NW * KFm], R.v0, R.v1, stage);
       } else if (lane < KFm) {
         stage[lane] = make_float2(-INFINITY, __int_as_float(INT32_MAX));
       }
@@ -1376,6 +1400,16 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
         rej = !a;
       }
       const unsigned rejects = ballot(rej);
+      if (sampled && tvalid && dvalid && lane < 2) {  // the rows the draw reads
+        const int mm = rejects ? __ffs(rejects) - 1 : K;
+        if (lane == 0) {
+          S.dt = S.rows[S.trow[mm]];
+          row_geometry<NT>(S.dt, v0, v1, sz);
+        } else if (mm < K) {
+          S.dd = S.rows[S.drow[mm]];
+          row_geometry<NT>(S.dd, v0, v1, sz);
+        }
+      }
       if (lane == 0) {
         const int mm = rejects ? __ffs(rejects) - 1 : K;
         S.m = mm;
@@ -1403,8 +1437,8 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
     for (int attempt = 0; attempt < 2 && S.kind != 0; ++attempt) {
       const int mm = S.m;
       const bool residual = S.kind == 1;
-      const RowInfo &Rt = S.rows[S.trow[mm]];
-      const RowInfo *Rd = residual ? &S.rows[S.drow[mm]] : nullptr;
+      const RowInfo &Rt = S.dt;
+      const RowInfo *Rd = residual ? &S.dd : nullptr;
       const bool d_vec = residual && Rd->hp == Rt.hp;  // same vector grid
       RowInfo Rdt;  // otherwise: the draft row read element-wise on the target's grid
       if (residual && !d_vec) {
@@ -1821,6 +1855,13 @@ static sd_status_t launch_nt(Params &P, cudaStream_t stream) {
   if (cs < 1 || cs > kMaxCS) return SD_ERR_INVALID_ARG;
   P.cs = cs;
   P.slice = slice_for(P.V, cs, sz, NT);
+  // Row-major split where a slice of every row would leave each CTA at most
+  // two streaming steps per row (per-row work then outweighs the steps);
+  // SDV_ROWSPLIT=0/1 forces either.
+  {
+    const int rs = env_int("SDV_ROWSPLIT", -1);
+    P.rowsplit = rs >= 0 ? (rs ? 1 : 0) : (P.slice <= 2 * (NT * kU * 16 / sz) ? 1 : 0);
+  }
   const Layout L = make_layout(NT, rows_per_seq(P), P.K + 1, KF, cs, P.slice, sz);
   if (L.total > kDynSmemCap) return SD_ERR_UNSUPPORTED;
   void *fn = kernel_fn<E, KF, NT>();
@@ -1837,8 +1878,9 @@ static sd_status_t launch_nt(Params &P, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (env_int("SDV_VERBOSE", 0))
-    fprintf(stderr, "sd_verify: mode=%d B=%d K=%d V=%d cs=%d NT=%d slice=%d KF=%d smem=%d\n",
-            P.mode, P.B, P.K, P.V, cs, NT, P.slice, KF, L.total);
+    fprintf(stderr,
+            "sd_verify: mode=%d B=%d K=%d V=%d cs=%d NT=%d slice=%d rowsplit=%d KF=%d smem=%d\n",
+            P.mode, P.B, P.K, P.V, cs, NT, P.slice, P.rowsplit, KF, L.total);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, (void (*)(const Params))fn, P);
   if (e != cudaSuccess) {
     fprintf(stderr, "sd_verify launch failed: %s\n", cudaGetErrorString(e));

@@ -178,6 +178,34 @@ def test_forced_cluster_sizes(dev, cs, monkeypatch):
     np.testing.assert_array_equal(r.packed.cpu().numpy()[: offs[-1]], packed)
 
 
+@pytest.mark.parametrize("rs,cs,V,dt", [(0, 5, 50021, "bf16"), (1, 5, 50021, "bf16"),
+                                        (1, 2, 50021, "f32"), (1, 16, 3001, "bf16"),
+                                        (1, 16, 3001, "f32"), (1, 7, 131072, "bf16")])
+def test_stream_split_modes(dev, rs, cs, V, dt, monkeypatch):
+    # both ways of dividing a sequence's rows among the cluster's CTAs: a
+    # vocabulary slice of every row, or row pieces cut at whole streaming
+    # steps (pieces that start mid-row, rows off the 16-byte grid for odd V,
+    # and CTAs left with no piece at all when the rows hold fewer steps than
+    # the cluster has CTAs)
+    monkeypatch.setenv("SDV_CS", str(cs))
+    monkeypatch.setenv("SDV_ROWSPLIT", str(rs))
+    B, K = 3, 5
+    fan = [4, 3, 2, 1, 1, 2]
+    temps = [0.9, 0.0, 0.6]
+    inp = W.synth(B, K, V, dt, kind="peaked", sigma=3.0, draft_sigma=1.0, peaks=20,
+                  temperature=temps, seed=70 + cs + rs, device=dev, bonus_row=True)
+    keys_ref = oracle.outcome_predict(_np(inp.draft), inp.tokens.cpu().numpy(), fan,
+                                      _np(inp.draft_bonus))
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, fanout=fan,
+                  draft_bonus=inp.draft_bonus, stats=True, compact=True)
+    np.testing.assert_array_equal(r.keys.cpu().numpy(), keys_ref)
+    o = _oracle_for(inp, keys=keys_ref)
+    _check(*compare_verify(r, o, temps))
+    # the same without keys: greedy rows stream the target only
+    r2 = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, stats=True)
+    _check(*compare_verify(r2, _oracle_for(inp), temps))
+
+
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
 def test_largest_k_with_keys(dev, dt):
     B, K, V = 2, 32, 3001
