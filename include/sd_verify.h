@@ -126,17 +126,21 @@ typedef struct sd_verify_args {
   int32_t *target_argmax;/* [B][K+1]: top target token per position          */
   int32_t *status;       /* one int32, SD_STATUS_* bits OR-ed in             */
 
-  /* Scratch, reserved: the current kernels keep all intermediate state in
-   * on-chip memory and need none (sd_verify_workspace_size returns 0), so
-   * workspace may be NULL with workspace_bytes 0.  A non-NULL buffer must
-   * be 16-byte aligned and at least sd_verify_workspace_size(B, K) bytes;
-   * the library does not touch it. */
+  /* Scratch for the split launch (optional): at least
+   * sd_verify_workspace_size(B, K) bytes, 16-byte aligned, caller-owned.
+   * With it, the rows of all sequences are streamed by one flat grid that
+   * writes per-piece statistics here, and a per-sequence finish reads them
+   * back; without it (NULL), one cluster kernel does both on chip.  The
+   * contents need no clearing (every record is written before it is read in
+   * the same call); calls that share a workspace must not overlap on the GPU
+   * (one stream orders them).  Smaller than required: SD_ERR_INVALID_ARG. */
   void *workspace;
   size_t workspace_bytes;
 } sd_verify_args;
 
-/* Bytes of scratch sd_verify needs for a batch of B rows of K drafts (0 for
- * the current kernels); 0 also for arguments out of range. */
+/* Bytes of scratch the split launch of sd_verify needs for a batch of B rows
+ * of K drafts: (1024 + B (2K + 2)) records of 96 bytes; 0 for arguments out
+ * of range. */
 size_t sd_verify_workspace_size(int32_t B, int32_t K);
 
 /*
@@ -147,8 +151,12 @@ size_t sd_verify_workspace_size(int32_t B, int32_t K);
  * outcome-prediction keys and the compaction of all rows' tokens.
  * Each logit row is streamed from memory once; the target and draft rows at
  * the first rejection (or target row K) are read a second time for the
- * draw, mostly from L2.  One kernel launch, plus a one-CTA packing launch
- * with SD_FLAG_COMPACT (a programmatic dependent of the first, same stream).
+ * draw, mostly from L2.  With a workspace: a streaming launch and a finish
+ * launch (its programmatic dependent); without one: a single launch; plus,
+ * with SD_FLAG_COMPACT, a one-CTA packing launch (a programmatic dependent
+ * of the last, same stream).  Requests outside the split launch's limits
+ * (a streaming CTA's share touching more than 2 SD_MAX_K + 2 rows, or B too
+ * large for its shared-memory list of sampled rows) take the single launch.
  */
 sd_status_t sd_verify(const sd_verify_args *args, void *stream);
 

@@ -36,12 +36,32 @@ def stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Each translation unit is compiled to an object in parallel, then the
+    objects are linked into the shared library."""
     if not force and not stale():
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), *SOURCES, "-o", tmp]
-    if verbose:
-        print(" ".join(cmd), flush=True)
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    tag = f".tmp{os.getpid()}"
+    base = [nvc := nvcc(), *NVCC_FLAGS[:-1], "-I", os.path.join(ROOT, "include")]
+    objs, procs = [], []
+    for src in SOURCES:
+        obj = os.path.join(PKG, os.path.basename(src) + tag + ".o")
+        cmd = [*[a for a in base if a != "-shared"], "-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        objs.append(obj)
+        procs.append(subprocess.Popen(cmd))
+    try:
+        rcs = [p.wait() for p in procs]
+        if any(rcs):
+            raise subprocess.CalledProcessError(next(r for r in rcs if r), "nvcc -c")
+        tmp = LIB + tag
+        link = [nvc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", *objs, "-o", tmp]
+        if verbose:
+            print(" ".join(link), flush=True)
+        subprocess.run(link, check=True)
+        os.replace(tmp, LIB)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB

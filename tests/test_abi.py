@@ -37,10 +37,15 @@ def test_struct_layout_and_strings():
 
 
 def test_workspace_size():
-    # all intermediate state stays on chip: no scratch for any size
-    for B, K in [(8, 5), (256, 5), (1, 0), (4, sd.SD_MAX_K), (4, sd.SD_MAX_K + 1)]:
-        assert sd.lib().sd_verify_workspace_size(B, K) == 0
-    assert sd.workspace(8, 5) is None
+    # the split launch keeps one 96-byte record per row piece: at most one per
+    # logit row of the batch (2K+2 per sequence) plus one per streaming CTA
+    # (at most 1024); 0 for arguments out of range
+    L = sd.lib()
+    for B, K in [(8, 5), (256, 5), (1, 0), (4, sd.SD_MAX_K), (0, 3)]:
+        assert L.sd_verify_workspace_size(B, K) == (1024 + B * (2 * K + 2)) * 96
+    assert L.sd_verify_workspace_size(4, sd.SD_MAX_K + 1) == 0
+    assert L.sd_verify_workspace_size(-1, 5) == 0
+    assert L.sd_verify_workspace_size(3, -1) == 0
 
 
 def test_host_argument_checks_reject_bad_requests():

@@ -26,6 +26,14 @@ def dev():
     return torch.device("cuda:0")
 
 
+@pytest.fixture(params=["split", "cluster"])
+def path(request, monkeypatch):
+    """Both launch paths: the flat streaming grid + per-sequence finish (the
+    default when scratch is given), and the single cluster kernel."""
+    monkeypatch.setenv("SDV_SPLIT", "1" if request.param == "split" else "0")
+    return request.param
+
+
 def _np(t):
     return W.to_numpy_logits(t)
 
@@ -95,7 +103,7 @@ SHAPES = [
 
 @pytest.mark.parametrize("B,K,V,dt", SHAPES)
 @pytest.mark.parametrize("kind", ["normal", "peaked"])
-def test_small_shapes_full_parity(dev, B, K, V, dt, kind):
+def test_small_shapes_full_parity(dev, path, B, K, V, dt, kind):
     temps = [0.0, 0.6, 1.0, 1.7, 0.3, 1.0][:B]
     inp = W.synth(B, K, V, dt, kind=kind, sigma=2.0, draft_sigma=0.7, peaks=3 if V > 8 else 0,
                   temperature=temps, seed=B * 1000 + K * 10 + V, device=dev)
@@ -111,7 +119,7 @@ def test_small_shapes_full_parity(dev, B, K, V, dt, kind):
     assert int(r.status.item()) == 0
 
 
-def test_zipf_and_ties_and_neg_inf(dev):
+def test_zipf_and_ties_and_neg_inf(dev, path):
     B, K, V = 4, 3, 3001
     inp = W.synth(B, K, V, "bf16", kind="zipf", temperature=[1.0, 0.0, 0.6, 1.0], seed=77,
                   device=dev)
@@ -130,7 +138,7 @@ def test_zipf_and_ties_and_neg_inf(dev):
 
 # ------------------------------------------------------ outcome prediction ----
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
-def test_outcome_keys_standalone_and_fused(dev, dt):
+def test_outcome_keys_standalone_and_fused(dev, path, dt):
     B, K, V = 5, 6, 12007
     fan = [4, 3, 2, 1, 1, 1, 1]
     inp = W.synth(B, K, V, dt, kind="peaked", sigma=3.0, draft_sigma=1.0, peaks=20,
@@ -157,9 +165,10 @@ def test_outcome_keys_standalone_and_fused(dev, dt):
 
 
 @pytest.mark.parametrize("cs", [1, 3, 7, 16])
-def test_forced_cluster_sizes(dev, cs, monkeypatch):
+def test_forced_cluster_sizes(dev, path, cs, monkeypatch):
     # every cluster size streams the same rows: slices off the 16-byte grid
-    # (odd V, bf16), fan-outs up to the largest key count, greedy and sampled
+    # (odd V, bf16), fan-outs up to the largest key count, greedy and sampled;
+    # on the split path the size is the finish's (the draw's slices)
     monkeypatch.setenv("SDV_CS", str(cs))
     B, K, V = 3, 5, 50021
     fan = [8, 2, 1, 0, 3, 1]
@@ -187,6 +196,7 @@ def test_stream_split_modes(dev, rs, cs, V, dt, monkeypatch):
     # steps (pieces that start mid-row, rows off the 16-byte grid for odd V,
     # and CTAs left with no piece at all when the rows hold fewer steps than
     # the cluster has CTAs)
+    monkeypatch.setenv("SDV_SPLIT", "0")
     monkeypatch.setenv("SDV_CS", str(cs))
     monkeypatch.setenv("SDV_ROWSPLIT", str(rs))
     B, K = 3, 5
@@ -206,8 +216,35 @@ def test_stream_split_modes(dev, rs, cs, V, dt, monkeypatch):
     _check(*compare_verify(r2, _oracle_for(inp), temps))
 
 
+@pytest.mark.parametrize("G,V,dt", [(1, 50021, "bf16"), (5, 50021, "bf16"), (37, 50021, "f32"),
+                                    (300, 50021, "bf16"), (64, 3001, "bf16"),
+                                    (300, 131072, "f32")])
+def test_split_grid_sizes(dev, G, V, dt, monkeypatch):
+    # the flat streaming grid at several sizes: one CTA streaming every row,
+    # ranges that cut rows at arbitrary steps, rows spread over many CTAs
+    # (up to the limit of pieces per row), rows of a single step (V = 3001)
+    monkeypatch.setenv("SDV_SPLIT", "1")
+    monkeypatch.setenv("SDV_GRID", str(G))
+    B, K = 4, 5
+    fan = [4, 3, 2, 1, 0, 2]
+    temps = [0.9, 0.0, 0.6, 1.4]
+    inp = W.synth(B, K, V, dt, kind="peaked", sigma=3.0, draft_sigma=1.0, peaks=20,
+                  temperature=temps, seed=90 + G, device=dev, bonus_row=True)
+    keys_ref = oracle.outcome_predict(_np(inp.draft), inp.tokens.cpu().numpy(), fan,
+                                      _np(inp.draft_bonus))
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, fanout=fan,
+                  draft_bonus=inp.draft_bonus, stats=True, compact=True)
+    np.testing.assert_array_equal(r.keys.cpu().numpy(), keys_ref)
+    _check(*compare_verify(r, _oracle_for(inp, keys=keys_ref), temps))
+    offs, packed = oracle.compact(r.out_tokens.cpu().numpy(), r.tau.cpu().numpy())
+    np.testing.assert_array_equal(r.offsets.cpu().numpy(), offs)
+    np.testing.assert_array_equal(r.packed.cpu().numpy()[: offs[-1]], packed)
+    r2 = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, stats=True)
+    _check(*compare_verify(r2, _oracle_for(inp), temps))
+
+
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
-def test_largest_k_with_keys(dev, dt):
+def test_largest_k_with_keys(dev, path, dt):
     B, K, V = 2, 32, 3001
     fan = [2] * K + [1]
     temps = [1.0, 0.0]
@@ -222,7 +259,7 @@ def test_largest_k_with_keys(dev, dt):
     _check(*compare_verify(r, o, temps))
 
 
-def test_d3d_key_counts(dev):
+def test_d3d_key_counts(dev, path):
     B, K, V = 2, 15, 4096
     inp = W.synth(B, K, V, "bf16", kind="normal", temperature=0.0, seed=9, device=dev,
                   bonus_row=True)
@@ -236,7 +273,7 @@ def test_d3d_key_counts(dev):
 
 
 # --------------------------------------------------------------- edge cases ----
-def test_invalid_rows_set_status_and_empty_batch(dev):
+def test_invalid_rows_set_status_and_empty_batch(dev, path):
     B, K, V = 4, 3, 999
     inp = W.synth(B, K, V, "f32", temperature=[1.0, 1.0, 1.0, 0.0], seed=3, device=dev)
     inp.tokens[1, 2] = V
@@ -255,19 +292,38 @@ def test_invalid_rows_set_status_and_empty_batch(dev):
     assert r0.offsets.tolist() == [0]
 
 
-def test_repeated_calls_and_optional_scratch(dev):
-    # back-to-back calls on one stream give identical results; an unused
-    # scratch buffer, if passed, is left untouched
+def test_repeated_calls_and_scratch(dev, monkeypatch, capfd):
+    # back-to-back calls on one stream give identical results on both paths;
+    # the split path runs when scratch is given (SDV_VERBOSE names the path);
+    # scratch is never read before it is written in the same call (it starts
+    # filled with garbage here); scratch below sd_verify_workspace_size is
+    # refused
     B, K, V = 8, 5, 5000
     inp = W.synth(B, K, V, "bf16", kind="peaked", peaks=4, temperature=0.8, seed=21, device=dev)
-    ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+    ws = torch.full((sd.workspace_bytes(B, K),), 0xAB, dtype=torch.uint8, device=dev)
+    monkeypatch.setenv("SDV_VERBOSE", "1")
     a = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, ws=ws,
                   compact=True)
-    b = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, compact=True)
     torch.cuda.synchronize()
+    assert "sd_verify split:" in capfd.readouterr().err
+    b = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, ws=ws,
+                  compact=True)
+    monkeypatch.setenv("SDV_SPLIT", "0")
+    c = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, compact=True)
+    torch.cuda.synchronize()
+    assert "sd_verify: mode=0" in capfd.readouterr().err
     n = int(a.offsets[-1])
-    assert torch.equal(a.out_tokens, b.out_tokens) and torch.equal(a.packed[:n], b.packed[:n])
-    assert int(ws.count_nonzero().item()) == 0
+    assert torch.equal(a.out_tokens, b.out_tokens) and torch.equal(a.tau, b.tau)
+    assert torch.equal(a.packed[:n], b.packed[:n])
+    # the two paths group the sums differently: both against the oracle
+    o = _oracle_for(inp)
+    for x in (a, c):
+        _check(*compare_verify(x, o, inp.temperature.cpu().numpy(), check_stats=False))
+    monkeypatch.setenv("SDV_SPLIT", "1")
+    with pytest.raises(sd.SDError):
+        sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed,
+                  ws=torch.zeros(64, dtype=torch.uint8, device=dev))
+    monkeypatch.delenv("SDV_VERBOSE")
     # then a smaller batch with another K and dtype
     inp2 = W.synth(3, 2, 777, "f32", temperature=[0.0, 1.0, 0.5], seed=2, device=dev)
     c = sd.verify(inp2.target, inp2.draft, inp2.tokens, inp2.temperature, inp2.seed)
@@ -275,7 +331,7 @@ def test_repeated_calls_and_optional_scratch(dev):
     _check(*compare_verify(c, o, inp2.temperature.cpu().numpy(), check_stats=False))
 
 
-def test_row_base_splits_batch_identically(dev):
+def test_row_base_splits_batch_identically(dev, path):
     B, K, V = 10, 4, 9000
     inp = W.synth(B, K, V, "bf16", kind="normal", temperature=0.9, seed=31, device=dev)
     full = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed)
@@ -303,7 +359,7 @@ def test_compact_standalone(dev):
 
 # ------------------------------------------- workloads at full size, sampled --
 @pytest.mark.parametrize("name", W.ORDER)
-def test_workload_full_size_sampled_rows(dev, name):
+def test_workload_full_size_sampled_rows(dev, path, name):
     inp = W.workload(name, round_idx=3, device=dev)
     spec = W.WORKLOADS[name]
     fan = spec.get("fanout")
@@ -343,7 +399,7 @@ def test_workload_full_size_sampled_rows(dev, name):
 
 
 @pytest.mark.parametrize("name,rounds", [("small", 200), ("peaked", 40)])
-def test_many_rounds_mismatch_count(dev, name, rounds):
+def test_many_rounds_mismatch_count(dev, path, name, rounds):
     """Every sampled row compared in full over many rounds: no difference
     outside the guard band; guarded rows counted."""
     tot = dict(rows=0, positions=0, guarded=0, guarded_mismatch=0, mismatch_outside_guard=0)
