@@ -161,6 +161,31 @@ size_t sd_verify_workspace_size(int32_t B, int32_t K);
 sd_status_t sd_verify(const sd_verify_args *args, void *stream);
 
 /*
+ * sd_verify without caller scratch (the pages have no counterpart: this is
+ * an interface for callers that cannot allocate device memory when they
+ * verify -- a serving runtime whose memory is all handed to its own pool
+ * up front, a plugin given only the tensors it works on, a step that must
+ * not call an allocator).  Same arguments and results as sd_verify; the
+ * workspace fields must be NULL / 0 (else SD_ERR_INVALID_ARG).  The split
+ * launch keeps its piece records in a 2 MiB array inside the library
+ * (a file-scope __device__ array that every GPU which loads the library
+ * holds until the process exits), so sd_verify_workspace_size(B, K) may be
+ * at most 2 MiB: 1024 + B (2K + 2) <= 21845 (e.g. B = 256 at K = 32);
+ * larger batches return SD_ERR_UNSUPPORTED with a message on stderr.  The
+ * call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current); make that
+ * first call before capturing a stream into a CUDA graph.  All calls share
+ * the one array per device: calls that may overlap on the GPU (other
+ * streams, other threads) race on it, so order them on one stream.  The
+ * array keeps the last call's records; nothing in it needs clearing, as
+ * every record is written before it is read within a call.  Requests
+ * outside the split launch's limits run the single cluster kernel, which
+ * needs no scratch.
+ */
+sd_status_t sd_verify_noalloc(const sd_verify_args *args, void *stream);
+
+/*
  * Outcome prediction: for each row b and position k < K, the fanout[k]
  * tokens with the highest draft logit at k other than the drafted token
  * d_k (ties to the lowest index, -inf logits never chosen), keyed (k, token):

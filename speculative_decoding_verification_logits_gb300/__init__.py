@@ -72,6 +72,8 @@ def lib():
             L.sd_verify_workspace_size.restype = sz
             L.sd_verify.argtypes = [ctypes.POINTER(VerifyArgs), _P]
             L.sd_verify.restype = ctypes.c_int
+            L.sd_verify_noalloc.argtypes = [ctypes.POINTER(VerifyArgs), _P]
+            L.sd_verify_noalloc.restype = ctypes.c_int
             L.sd_outcome_predict.argtypes = [i32, i32, i32, ctypes.c_int, _P, _P, _P, _P, _P, _P,
                                              _P, _P]
             L.sd_outcome_predict.restype = ctypes.c_int
