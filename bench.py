@@ -22,6 +22,7 @@ cores instead (the reference arm).
 from __future__ import annotations
 
 import argparse
+import glob
 import hashlib
 import json
 import os
@@ -46,8 +47,7 @@ METRIC = "verify rounds/s"
 UNIT = "rounds/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_logits_gb300", "csrc",
-                          "sd_verify.cu")
+KERNEL_DIR = os.path.join(ROOT, "speculative_decoding_verification_logits_gb300", "csrc")
 
 
 def describe(name):
@@ -129,7 +129,12 @@ def peaks():
 
 
 def kernel_src_hash():
-    return hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    """Hash of every CUDA source of the library (csrc/*.cu, *.cuh, sorted)."""
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(KERNEL_DIR, "*.cu")) +
+                    glob.glob(os.path.join(KERNEL_DIR, "*.cuh"))):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload):
@@ -144,6 +149,23 @@ def profiled_traffic(workload):
     if not m or not h or h.group(1) != kernel_src_hash():
         return None
     return float(m.group(1))
+
+
+def launches_per_step(B, K):
+    """Kernel launches of one verify round: the split launch (streaming grid,
+    finish, packing) where the library takes it -- with scratch, when the
+    cluster kernel would leave SMs idle or run one CTA per sequence -- else
+    the cluster kernel and the packing launch.  Mirrors the library's rule
+    with the cluster size it would pick (SDV_VERBOSE=1 prints the launch)."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mode = int(os.environ.get("SDV_SPLIT", "-1") or -1)
+    if mode == 0:
+        return 2
+    if mode == 1:
+        return 3
+    cs = max(1, min(16, (2 * sms) // max(B, 1)))
+    return 3 if (cs <= 1 or B * cs < sms) else 2
 
 
 def algorithmic_bytes(inp: W.Inputs) -> int:
@@ -303,9 +325,12 @@ def run_gpu(args):
                          f"> 4x L2 {l2 / 1e6:.0f} MB)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                     "peak_source": pk_kind, "kernel": "sd_verify_kernel",
+                     "peak_source": pk_kind,
+                     "kernel": "verify step: all launches of one round (duration = step time)",
                      "algorithmic_bytes_per_launch": alg, "formula_bytes_per_launch": formula},
-        "gpu_launches": 2 * steps,  # the verify launch and the packing launch per step
+        # per step: the cluster kernel and the packing launch, or the streaming
+        # grid, the finish and the packing launch (split launch)
+        "gpu_launches": launches_per_step(B, K) * steps,
         "clocks": clocks,
         "e2e": e2e,
         "hit_rate": hit_rate, "mean_tau": mean_tau, "status_bits": st,

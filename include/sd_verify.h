@@ -151,8 +151,13 @@ size_t sd_verify_workspace_size(int32_t B, int32_t K);
  * outcome-prediction keys and the compaction of all rows' tokens.
  * Each logit row is streamed from memory once; the target and draft rows at
  * the first rejection (or target row K) are read a second time for the
- * draw, mostly from L2.  With a workspace: a streaming launch and a finish
- * launch (its programmatic dependent); without one: a single launch; plus,
+ * draw, mostly from L2.  Two ways to run: a split launch (a streaming
+ * launch over the rows of all sequences, then a finish launch as its
+ * programmatic dependent; needs the workspace) and a single cluster kernel.
+ * With a workspace the split launch is taken where the cluster kernel would
+ * leave SMs without work (B times its cluster size below the SM count) or
+ * would give each sequence one CTA; else, and without a workspace, the
+ * single launch; plus,
  * with SD_FLAG_COMPACT, a one-CTA packing launch (a programmatic dependent
  * of the last, same stream).  Requests outside the split launch's limits
  * (a streaming CTA's share touching more than 2 SD_MAX_K + 2 rows, or B too
@@ -179,9 +184,10 @@ sd_status_t sd_verify(const sd_verify_args *args, void *stream);
  * the one array per device: calls that may overlap on the GPU (other
  * streams, other threads) race on it, so order them on one stream.  The
  * array keeps the last call's records; nothing in it needs clearing, as
- * every record is written before it is read within a call.  Requests
- * outside the split launch's limits run the single cluster kernel, which
- * needs no scratch.
+ * every record is written before it is read within a call.  Like
+ * sd_verify, it takes the split launch only where that is the faster one
+ * (see sd_verify) and the single cluster kernel, which needs no scratch,
+ * otherwise.
  */
 sd_status_t sd_verify_noalloc(const sd_verify_args *args, void *stream);
 

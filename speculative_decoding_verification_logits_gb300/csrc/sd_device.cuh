@@ -542,6 +542,8 @@ struct Static {
   int wsel;                   //   the warp holding the crossing point
   ff t_w;
   int red_i[kMaxWarps];
+  float u_acc[SD_MAX_K];      // accept uniforms u(b, j, 0)
+  float u_draw[SD_MAX_K + 1]; // draw uniforms u(b, m, 1) for every m
   int rflat[kMaxRows];        // split finish: the row's index in the flat stream
   int pc0[kMaxRows], pc1[kMaxRows];  //   and the streaming CTAs that covered it
   int tok;
@@ -1059,6 +1061,15 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
 
   // every CTA of the cluster has started before any pushes into its memory
   cluster_arrive_relaxed();
+  if (SPLIT && warp == 0) {
+    // Run the out-of-line helpers of the accept scan and the draw once, on
+    // values the compiler cannot fold, before anything else: the first jump
+    // into a helper late in the chain otherwise costs microseconds.
+    const ff w0 = ff_warp_scan(ff{(float)(lane * P.V), (float)P.K});
+    const ff w1 = ff_warp_sum(w0);
+    const float w2 = exp2_ff(ff{w1.lo, 0.f});
+    if (w2 == -1.f) S.tok = -2;  // never true: keeps the calls
+  }
 
   const int v0 = min(rank * P.slice, P.V);
   const int v1 = min(v0 + P.slice, P.V);
@@ -1120,6 +1131,13 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       S.nrows = base + __popc(dm) + (verify ? K : 0);
       S.dvalid = dvalid ? 1 : 0;
     }
+    // the uniforms of the accept test at every position and of the draw at
+    // every possible outcome position, ahead of the chain that uses them
+    if (sampled)
+      for (int q = lane; q <= K; q += 32) {
+        if (q < K) S.u_acc[q] = uniform_u(P.seed, P.row_base + b, q, 0);
+        S.u_draw[q] = uniform_u(P.seed, P.row_base + b, q, 1);
+      }
   } else if (warp == 1 && lane < 2) {
     if (lane == 0 && has_bonus) {
       RowInfo &R = S.rows[0];
@@ -1268,19 +1286,6 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
   __syncthreads();
 
   if constexpr (SPLIT) {
-    // While the streaming grid may still run: run the out-of-line helpers of
-    // the accept scan and the draw once on dummy values, so that their code
-    // is resident when the latency-bound chain below reaches them (a cold
-    // jump into a helper costs microseconds there; here it overlaps the
-    // stream's tail).
-    if (warp == 0) {
-      const ff w0 = ff_warp_scan(ff{(float)lane, 0.f});
-      const ff w1 = ff_warp_sum(w0);
-      const float w2 = exp2_ff(w1);
-      RowInfo Rw = S.rows[0];
-      row_geometry<NT>(Rw, 0, 16, sz);
-      if (w2 == -1.f || Rw.nvec < 0) S.tok = -2;  // never true: keeps the calls
-    }
     // the streaming grid has finished and its records are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
     cluster_wait();  // pairs with the arrive at the top
@@ -1337,41 +1342,30 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
   }
 
   // ---- combine the cluster's statistics (same arithmetic in every CTA)
-  if (SPLIT && tid < nrows) {
-    // the same combine over the streaming CTAs' piece records of the row
-    // (at most kMaxParts of them), all loads in flight at once
-    const int r = tid, np = S.pc1[r] - S.pc0[r] + 1;
-    const uint8_t *rec0 = P.ws + (int64_t)(S.pc0[r] + S.rflat[r]) * kRecBytes;
-    CStat pt[kMaxParts];
-#pragma unroll
-    for (int p = 0; p < kMaxParts; ++p) {
-      if (p < np) {
-        const float *x = reinterpret_cast<const float *>(rec0 + p * kRecBytes);
-        const float4 a = __ldcg(reinterpret_cast<const float4 *>(x));
-        pt[p] = CStat{a.x, __float_as_int(a.y), a.z, a.w, __ldcg(x + 4)};
+  if constexpr (SPLIT) {
+    // the same combine over the row's piece records (at most kMaxParts):
+    // one warp per row, lane p holding piece p, all records loaded at once
+    for (int r = warp; r < nrows; r += NW) {
+      const int np = S.pc1[r] - S.pc0[r] + 1;
+      CStat x{-INFINITY, INT32_MAX, INFINITY, 0.f, 0.f};
+      if (lane < np) {
+        const float *rp = reinterpret_cast<const float *>(
+            P.ws + (int64_t)(S.pc0[r] + lane + S.rflat[r]) * kRecBytes);
+        const float4 a4 = __ldcg(reinterpret_cast<const float4 *>(rp));
+        x = CStat{a4.x, __float_as_int(a4.y), a4.z, a4.w, __ldcg(rp + 4)};
+      }
+      const float M = rmax_f(x.m);
+      const int I = rmin_i(x.m == M ? x.idx : INT32_MAX);
+      const float C = rmin_f(x.zhi > 0.f ? x.c : INFINITY);
+      const ff zt = x.zhi > 0.f ? ff_mul_f(ff{x.zhi, x.zlo}, ex2(C - x.c)) : ff{0.f, 0.f};
+      const ff Z = ff_warp_sum(zt);
+      if (lane == 0) {
+        S.M[r] = M;
+        S.C[r] = C;
+        S.Z[r] = Z;
+        S.amax[r] = I == INT32_MAX ? 0 : I;
       }
     }
-    float M = -INFINITY;
-#pragma unroll
-    for (int p = 0; p < kMaxParts; ++p)
-      if (p < np) M = fmaxf(M, pt[p].m);
-    int I = INT32_MAX;
-    float C = INFINITY;
-#pragma unroll
-    for (int p = 0; p < kMaxParts; ++p) {
-      if (p < np) {
-        if (pt[p].m == M) I = min(I, pt[p].idx);
-        if (pt[p].zhi > 0.f) C = fminf(C, pt[p].c);
-      }
-    }
-    ff Z{0.f, 0.f};
-#pragma unroll
-    for (int p = 0; p < kMaxParts; ++p)
-      if (p < np && pt[p].zhi > 0.f) Z = ff_add(Z, ff_mul_f(ff{pt[p].zhi, pt[p].zlo}, ex2(C - pt[p].c)));
-    S.M[r] = M;
-    S.C[r] = C;
-    S.Z[r] = Z;
-    S.amax[r] = I == INT32_MAX ? 0 : I;
   } else if (!SPLIT && tid < nrows) {
     const int r = tid;
     float M = -INFINITY;
@@ -1480,7 +1474,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
           const float r = (ldr == -INFINITY)
                               ? INFINITY  // q(d) = 0
                               : exp2_ff(ff_sub(xt, xd)) * __fdiv_rn(zd, zt);
-          const float u = uniform_u(P.seed, P.row_base + b, j, 0);
+          const float u = S.u_acc[j];
           a = (u <= r) ? 1 : 0;
           if (rank == 0) {
             const int64_t pj = (int64_t)b * K + j;
@@ -1622,7 +1616,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
         const ff incl = ff_warp_scan(sc);
         const ff tot = ff_shfl(incl, 31);
         if (ff_pos(tot) || !residual) {
-          const float u = uniform_u(P.seed, P.row_base + b, mm, 1);
+          const float u = S.u_draw[mm];
           const ff t = ff_mul_f(tot, u);
           const unsigned cross = ballot(ff_pos(sc) && ff_gt(incl, t));
           const unsigned pos = ballot(ff_pos(sc));
@@ -1667,9 +1661,17 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
           for (int tb = 0; tb < wsteps && tsel < 0; tb += 32) {
             const int t = tb + lane;
             ff mt{0.f, 0.f};
-            if (t < wsteps) {
-#pragma unroll 1
-              for (int i = 0; i < 32; ++i) mt = ff_add_f(mt, pmw[t * 32 + ((i + lane) & 31)]);
+            if (t < wsteps) {  // pairwise: five dependent levels instead of 32
+              ff v[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                v[i] = two_sum(pmw[t * 32 + ((2 * i + lane) & 31)],
+                               pmw[t * 32 + ((2 * i + 1 + lane) & 31)]);
+#pragma unroll
+              for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+                for (int i = 0; i < w2; ++i) v[i] = ff_add(v[i], v[i + w2]);
+              mt = v[0];
             }
             const ff incl = ff_warp_scan(mt);
             const unsigned cross =
@@ -1707,16 +1709,24 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
             const int q0 = wq0 + tsel * 64 + 2 * lane;
             int tok = -1, klast = -1;
             ff c2 = before_l;
+            uint4 tv2[2], dv2[2];  // both vectors requested before either is used
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int q = q0 + k;
+              if (q < wq1) {
+                tv2[k] = load_vec_direct<E>(Rt, q, v0, v1);
+                dv2[k] = tv2[k];
+                if (residual)
+                  dv2[k] = d_vec ? load_vec_direct<E>(*Rd, q, v0, v1)
+                                 : load_vec_slow<E>(Rdt, q, v0, v1);
+              }
+            }
 #pragma unroll 1
             for (int k = 0; k < 2 && tok < 0; ++k) {
               const int q = q0 + k;
               if (q >= wq1) break;
-              const uint4 tvv = load_vec_direct<E>(Rt, q, v0, v1);
-              uint4 dvv = tvv;
-              if (residual)
-                dvv = d_vec ? load_vec_direct<E>(*Rd, q, v0, v1) : load_vec_slow<E>(Rdt, q, v0, v1);
               float w[NV];
-              pass_weights<E>(tvv, dvv, residual, s2, ct2, cd2, w);
+              pass_weights<E>(k ? tv2[1] : tv2[0], k ? dv2[1] : dv2[0], residual, s2, ct2, cd2, w);
 #pragma unroll 1
               for (int i = 0; i < NV; ++i) {
                 const int e = elem_index(v0, Rt.hp, q, i, sz);
@@ -1739,36 +1749,33 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       break;
     }
 
-    // ---- the sequence's outputs (owning CTA)
-    if (rank == S.owner && tid == 0) {
+    // ---- the sequence's outputs (owning CTA, one warp: lane j writes token
+    // j, the lanes test the keys together)
+    if (rank == S.owner && warp == 0) {
       int32_t *out = P.out_tokens + (int64_t)b * (K + 1);
-      if (!S.valid) {
-        for (int j = 0; j <= K; ++j) out[j] = -1;
-        P.num_accepted[b] = 0;
-        P.tau[b] = 0;
-        if (P.hit) P.hit[b] = 0;
-        if (P.status)
+      const bool valid = S.valid != 0;
+      const int mm = valid ? S.m : -1, tok = S.tok;
+      for (int j = lane; j <= K; j += 32)
+        out[j] = !valid ? -1 : (j < mm ? S.d[j] : (j == mm ? tok : -1));
+      bool h = false;
+      if (valid && P.hit) {
+        if (P.keys) {
+          for (int k2 = lane; k2 < P.n_keys_out; k2 += 32)
+            h |= S.keys[k2].x == mm && S.keys[k2].y == tok;
+        } else if (P.keys_in) {
+          const int32_t *kb = P.keys_in + (int64_t)b * P.n_keys_in * 2;
+          for (int k2 = lane; k2 < P.n_keys_in; k2 += 32)
+            h |= kb[2 * k2] == mm && kb[2 * k2 + 1] == tok;
+        }
+      }
+      const bool hit = ballot(h) != 0u;
+      if (lane == 0) {
+        P.num_accepted[b] = valid ? mm : 0;
+        P.tau[b] = valid ? mm + 1 : 0;
+        if (P.hit) P.hit[b] = (uint8_t)(hit ? 1 : 0);
+        if (!valid && P.status)
           atomicOr(P.status, (tvalid ? 0 : (int)SD_STATUS_BAD_TEMP) |
                                  (S.dvalid ? 0 : (int)SD_STATUS_BAD_TOKEN));
-      } else {
-        const int mm = S.m, tok = S.tok;
-        for (int j = 0; j < mm; ++j) out[j] = S.d[j];
-        out[mm] = tok;
-        for (int j = mm + 1; j <= K; ++j) out[j] = -1;
-        P.num_accepted[b] = mm;
-        P.tau[b] = mm + 1;
-        if (P.hit) {
-          int h = 0;
-          if (P.keys) {
-            for (int k2 = 0; k2 < P.n_keys_out; ++k2)
-              if (S.keys[k2].x == mm && S.keys[k2].y == tok) h = 1;
-          } else if (P.keys_in) {
-            const int32_t *kb = P.keys_in + (int64_t)b * P.n_keys_in * 2;
-            for (int k2 = 0; k2 < P.n_keys_in; ++k2)
-              if (kb[2 * k2] == mm && kb[2 * k2 + 1] == tok) h = 1;
-          }
-          P.hit[b] = (uint8_t)h;
-        }
       }
     }
   }

@@ -95,11 +95,21 @@ static sd_status_t launch_nt(Params &P, cudaStream_t stream) {
   return SD_OK;
 }
 
-// The split launch when the caller gave scratch for it (SDV_SPLIT=0 turns it
-// off), else, or when the request is outside its limits, the cluster kernel.
+// With scratch from the caller, the split launch where it pays: where the
+// cluster kernel would leave SMs without a CTA (B cs < SMs) or would give
+// each sequence a single CTA (cs = 1), so that one SM streams a whole
+// sequence.  Otherwise -- or without scratch, or when the request is
+// outside the split launch's limits -- the cluster kernel.  SDV_SPLIT=1 / 0
+// forces either.
 template <typename E, int KF>
 static sd_status_t launch_kf(Params &P, cudaStream_t s) {
-  if (P.ws && env_int("SDV_SPLIT", 1)) {
+  const int mode = env_int("SDV_SPLIT", -1);
+  bool split = P.ws != nullptr && mode != 0;
+  if (split && mode < 0 && P.mode == kVerify) {
+    const int cs = choose_cs<E, KF, 256>(P);
+    split = cs <= 1 || (int64_t)P.B * cs < sm_count();
+  }
+  if (split) {
     const sd_status_t st = launch_split<E, KF>(P, P.ws_bytes, s);
     if (st != SD_ERR_UNSUPPORTED) return st;
   }

@@ -294,13 +294,14 @@ def test_invalid_rows_set_status_and_empty_batch(dev, path):
 
 def test_repeated_calls_and_scratch(dev, monkeypatch, capfd):
     # back-to-back calls on one stream give identical results on both paths;
-    # the split path runs when scratch is given (SDV_VERBOSE names the path);
+    # with scratch and SDV_SPLIT=1 the split path runs (SDV_VERBOSE names it);
     # scratch is never read before it is written in the same call (it starts
     # filled with garbage here); scratch below sd_verify_workspace_size is
     # refused
     B, K, V = 8, 5, 5000
     inp = W.synth(B, K, V, "bf16", kind="peaked", peaks=4, temperature=0.8, seed=21, device=dev)
     ws = torch.full((sd.workspace_bytes(B, K),), 0xAB, dtype=torch.uint8, device=dev)
+    monkeypatch.setenv("SDV_SPLIT", "1")
     monkeypatch.setenv("SDV_VERBOSE", "1")
     a = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, ws=ws,
                   compact=True)

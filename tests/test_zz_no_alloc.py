@@ -63,9 +63,14 @@ def _same(r, ref):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_sd_verify_on_two_calls():
+def test_noalloc_matches_sd_verify_on_two_calls(monkeypatch, capfd):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    # both batches are small enough (B times the cluster size below the SM
+    # count) that the split launch, the one that keeps records in the static
+    # array, is the one chosen; SDV_VERBOSE names the launch taken
+    monkeypatch.delenv("SDV_SPLIT", raising=False)
+    monkeypatch.setenv("SDV_VERBOSE", "1")
     dev = torch.device("cuda:0")
     L = sd.lib()
     stream = torch.cuda.current_stream(dev)
@@ -86,9 +91,11 @@ def test_noalloc_matches_sd_verify_on_two_calls():
         r = sd.alloc_outputs(inp.B, inp.K, dev, hit=bool(fan), compact=True, stats=True,
                              n_keys=n_keys)
         a, keep = _noalloc_args(inp, r, fan, n_keys)
+        capfd.readouterr()
         rc = L.sd_verify_noalloc(ctypes.byref(a), ctypes.c_void_p(stream.cuda_stream))
         assert rc == sd.SD_OK, L.sd_status_string(rc)
         torch.cuda.synchronize(dev)
+        assert "sd_verify split:" in capfd.readouterr().err
         _same(r, ref)
         del keep
 
