@@ -1041,6 +1041,40 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
+// The sequence's outputs, by one warp: lane j writes token j, the lanes
+// test the keys together.
+static __device__ __forceinline__ void seq_outputs(const Params &P, const Static &S, int b,
+                                                   bool tvalid) {
+  const int lane = threadIdx.x & 31, K = P.K;
+  int32_t *out = P.out_tokens + (int64_t)b * (K + 1);
+  const bool valid = S.valid != 0;
+  const int mm = valid ? S.m : -1, tok = S.tok;
+  for (int j = lane; j <= K; j += 32) {
+    const int v = !valid ? -1 : (j < mm ? S.d[j] : (j == mm ? tok : -1));
+    out[j] = v;
+  }
+  bool h = false;
+  if (valid && P.hit) {
+    if (P.keys) {
+      for (int k2 = lane; k2 < P.n_keys_out; k2 += 32)
+        h |= S.keys[k2].x == mm && S.keys[k2].y == tok;
+    } else if (P.keys_in) {
+      const int32_t *kb = P.keys_in + (int64_t)b * P.n_keys_in * 2;
+      for (int k2 = lane; k2 < P.n_keys_in; k2 += 32)
+        h |= kb[2 * k2] == mm && kb[2 * k2 + 1] == tok;
+    }
+  }
+  const bool hit = ballot(h) != 0u;
+  if (lane == 0) {
+    P.num_accepted[b] = valid ? mm : 0;
+    P.tau[b] = valid ? mm + 1 : 0;
+    if (P.hit) P.hit[b] = (uint8_t)(hit ? 1 : 0);
+    if (!valid && P.status)
+      atomicOr(P.status, (tvalid ? 0 : (int)SD_STATUS_BAD_TEMP) |
+                             (S.dvalid ? 0 : (int)SD_STATUS_BAD_TOKEN));
+  }
+}
+
 // SPLIT: the finish of the split launch -- the rows were streamed by
 // sd_flat_stream_kernel, whose piece records replace this kernel's stream and
 // its first cluster exchange; everything from the combine on is shared.
@@ -1704,43 +1738,38 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
             lsel = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : -1);
             if (lsel >= 0) before_l = ff_add(before, ff_shfl(ff_add_f(incl, -ml), lsel));
           }
-          if (lsel >= 0 && lane == lsel) {
-            // the crossing lane's two vectors, element by element
-            const int q0 = wq0 + tsel * 64 + 2 * lane;
-            int tok = -1, klast = -1;
-            ff c2 = before_l;
-            uint4 tv2[2], dv2[2];  // both vectors requested before either is used
+          if (lsel >= 0) {
+            // the crossing lane's two vectors, one element per lane (lane
+            // k NV + i: element i of vector k, i.e. index order), a scan of
+            // the weights from before_l, the first element past tw; if
+            // rounding leaves none, the last element with weight
+            const int k = lane / NV, i = lane % NV;
+            const int q = wq0 + tsel * 64 + 2 * lsel + k;
+            float w = 0.f;
+            int e = -1;
+            if (lane < 2 * NV && q < wq1) {
+              const uint4 tvv = load_vec_direct<E>(Rt, q, v0, v1);
+              uint4 dvv = tvv;
+              if (residual)
+                dvv = d_vec ? load_vec_direct<E>(*Rd, q, v0, v1) : load_vec_slow<E>(Rdt, q, v0, v1);
+              float ww[NV];
+              pass_weights<E>(tvv, dvv, residual, s2, ct2, cd2, ww);
+              float wi = 0.f;
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int q = q0 + k;
-              if (q < wq1) {
-                tv2[k] = load_vec_direct<E>(Rt, q, v0, v1);
-                dv2[k] = tv2[k];
-                if (residual)
-                  dv2[k] = d_vec ? load_vec_direct<E>(*Rd, q, v0, v1)
-                                 : load_vec_slow<E>(Rdt, q, v0, v1);
+              for (int ii = 0; ii < NV; ++ii)
+                if (ii == i) wi = ww[ii];
+              const int ei = elem_index(v0, Rt.hp, q, i, sz);
+              if (ei >= v0 && ei < v1 && wi > 0.f) {
+                w = wi;
+                e = ei;
               }
             }
-#pragma unroll 1
-            for (int k = 0; k < 2 && tok < 0; ++k) {
-              const int q = q0 + k;
-              if (q >= wq1) break;
-              float w[NV];
-              pass_weights<E>(k ? tv2[1] : tv2[0], k ? dv2[1] : dv2[0], residual, s2, ct2, cd2, w);
-#pragma unroll 1
-              for (int i = 0; i < NV; ++i) {
-                const int e = elem_index(v0, Rt.hp, q, i, sz);
-                if (e < v0 || e >= v1 || !(w[i] > 0.f)) continue;
-                klast = e;
-                const ff c3 = ff_add_f(c2, w[i]);
-                if (ff_gt(c3, tw)) {
-                  tok = e;
-                  break;
-                }
-                c2 = c3;
-              }
-            }
-            S.tok = tok >= 0 ? tok : klast;
+            const ff cw = ff_add(before_l, ff_warp_scan(ff{w, 0.f}));
+            const unsigned cross = ballot(e >= 0 && ff_gt(cw, tw));
+            const unsigned pos = ballot(e >= 0);
+            const int ls = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : 0);
+            const int tok = __shfl_sync(0xffffffffu, e, ls);
+            if (lane == 0) S.tok = tok >= 0 ? tok : S.amax[S.trow[mm]];
           }
           if (lsel < 0 && lane == 0) S.tok = S.amax[S.trow[mm]];  // no mass in this warp
         }
@@ -1749,35 +1778,8 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       break;
     }
 
-    // ---- the sequence's outputs (owning CTA, one warp: lane j writes token
-    // j, the lanes test the keys together)
-    if (rank == S.owner && warp == 0) {
-      int32_t *out = P.out_tokens + (int64_t)b * (K + 1);
-      const bool valid = S.valid != 0;
-      const int mm = valid ? S.m : -1, tok = S.tok;
-      for (int j = lane; j <= K; j += 32)
-        out[j] = !valid ? -1 : (j < mm ? S.d[j] : (j == mm ? tok : -1));
-      bool h = false;
-      if (valid && P.hit) {
-        if (P.keys) {
-          for (int k2 = lane; k2 < P.n_keys_out; k2 += 32)
-            h |= S.keys[k2].x == mm && S.keys[k2].y == tok;
-        } else if (P.keys_in) {
-          const int32_t *kb = P.keys_in + (int64_t)b * P.n_keys_in * 2;
-          for (int k2 = lane; k2 < P.n_keys_in; k2 += 32)
-            h |= kb[2 * k2] == mm && kb[2 * k2 + 1] == tok;
-        }
-      }
-      const bool hit = ballot(h) != 0u;
-      if (lane == 0) {
-        P.num_accepted[b] = valid ? mm : 0;
-        P.tau[b] = valid ? mm + 1 : 0;
-        if (P.hit) P.hit[b] = (uint8_t)(hit ? 1 : 0);
-        if (!valid && P.status)
-          atomicOr(P.status, (tvalid ? 0 : (int)SD_STATUS_BAD_TEMP) |
-                                 (S.dvalid ? 0 : (int)SD_STATUS_BAD_TOKEN));
-      }
-    }
+    // ---- the sequence's outputs (owning CTA, one warp)
+    if (rank == S.owner && warp == 0) seq_outputs(P, S, b, tvalid);
   }
   // No CTA touches another's shared memory after barrier (1) or (2), which
   // every CTA passes, so the CTAs may leave independently.
