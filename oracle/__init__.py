@@ -79,6 +79,8 @@ def _bind(L):
     L.oracle_outcome_predict.argtypes = [i32, i32, i32, i32, P, P, P, P, P]
     L.oracle_outcome_predict.restype = i32
     L.oracle_compact.argtypes = [i32, i32, P, P, P, P]
+    L.oracle_d3d_pack.argtypes = [i32, i32, i32, P, P, P, P, i32, P, P, P]
+    L.oracle_d3d_pack.restype = None
     L.oracle_compact.restype = None
     return L
 
@@ -204,3 +206,22 @@ def compact(out_tokens, tau):
     packed = np.full(max(int(tau.sum()), 1), -1, np.int32)
     lib().oracle_compact(B, K1 - 1, _ptr(out_tokens), _ptr(tau), _ptr(offsets), _ptr(packed))
     return offsets, packed[: int(tau.sum())]
+
+
+def d3d_pack(keys, draft_tokens, anchor, anchor_pos, mask_token: int):
+    """The drafter's packed next pass: (tokens, positions) [B][1+n_keys][K+1]
+    and ctx [B][1+n_keys] (block-0 tokens each block sees)."""
+    keys = np.ascontiguousarray(keys, dtype=np.int32)
+    B, n_keys, _ = keys.shape
+    draft_tokens = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    K = draft_tokens.shape[1]
+    anchor = np.ascontiguousarray(anchor, dtype=np.int32).reshape(B)
+    anchor_pos = np.ascontiguousarray(anchor_pos, dtype=np.int32).reshape(B)
+    nb = 1 + n_keys
+    tokens = np.zeros((B, nb, K + 1), np.int32)
+    positions = np.zeros((B, nb, K + 1), np.int32)
+    ctx = np.zeros((B, nb), np.int32)
+    lib().oracle_d3d_pack(B, K, n_keys, _ptr(keys), _ptr(draft_tokens), _ptr(anchor),
+                          _ptr(anchor_pos), int(mask_token), _ptr(tokens), _ptr(positions),
+                          _ptr(ctx))
+    return tokens, positions, ctx

@@ -393,4 +393,52 @@ void oracle_compact(int B, int K, const int32_t *out_tokens, const int32_t *tau,
   offsets[B] = acc;
 }
 
+// Packing of the drafter's next pass ([D3D] パック:24ブロックを1回の計算で
+// and the list of continuations before it).  One block is K+1 tokens: an
+// anchor (already confirmed) and K drafted tokens.  The pack holds the block
+// under verification (block 0) and one continuation block per outcome key:
+//  * block 0: anchor[b], then d_0..d_{K-1}, at positions anchor_pos[b] + i;
+//  * key (k, c), 0 <= k <= K: a rejection at k (or, k == K, all accepted)
+//    confirms the anchor and d_0..d_{k-1}, and c takes position
+//    anchor_pos[b] + 1 + k; its block is c followed by K mask tokens at the
+//    next K positions;
+//  * an empty key (or k outside [0, K]) leaves its block empty: tokens,
+//    positions and ctx all -1.
+// ctx[b][i]: how many tokens of block 0 block i sees besides the shared
+// prefix ("each block sees the text before it and itself"): 0 for block 0
+// (it sees itself), k + 1 for the continuation of key (k, c).
+// tokens / positions: [B][1 + n_keys][K + 1]; ctx: [B][1 + n_keys].
+void oracle_d3d_pack(int B, int K, int n_keys, const int32_t *keys, const int32_t *draft_tokens,
+                     const int32_t *anchor, const int32_t *anchor_pos, int32_t mask_token,
+                     int32_t *tokens, int32_t *positions, int32_t *ctx) {
+  const int L = K + 1, nb = 1 + n_keys;
+  for (int b = 0; b < B; ++b) {
+    for (int blk = 0; blk < nb; ++blk) {
+      int32_t *t = tokens + ((size_t)b * nb + blk) * L;
+      int32_t *p = positions + ((size_t)b * nb + blk) * L;
+      int32_t &c = ctx[(size_t)b * nb + blk];
+      if (blk == 0) {
+        for (int i = 0; i < L; ++i) {
+          t[i] = i == 0 ? anchor[b] : draft_tokens[(size_t)b * K + (i - 1)];
+          p[i] = anchor_pos[b] + i;
+        }
+        c = 0;
+        continue;
+      }
+      const int32_t *key = keys + ((size_t)b * n_keys + (blk - 1)) * 2;
+      const int k = key[0];
+      if (k < 0 || k > K || key[1] < 0) {
+        for (int i = 0; i < L; ++i) t[i] = p[i] = -1;
+        c = -1;
+        continue;
+      }
+      for (int i = 0; i < L; ++i) {
+        t[i] = i == 0 ? key[1] : mask_token;
+        p[i] = anchor_pos[b] + 1 + k + i;
+      }
+      c = k + 1;
+    }
+  }
+}
+
 }  // extern "C"

@@ -35,6 +35,9 @@ MUTANTS = {
                         "if (l[(size_t)i] >= l[(size_t)best]) best = i;"),
     "accept_uses_sample_slot": ("uniform_from_philox(seed, row, (uint32_t)j, 0u)",
                                 "uniform_from_philox(seed, row, (uint32_t)j, 1u)"),
+    "pack_position_off_by_one": ("p[i] = anchor_pos[b] + 1 + k + i;",
+                                 "p[i] = anchor_pos[b] + k + i;"),
+    "pack_ctx_off_by_one": ("      c = k + 1;", "      c = k;"),
 }
 
 FAST_PINS = [
@@ -46,6 +49,8 @@ FAST_PINS = [
     pins.test_probabilities_match_torch_softmax_float64,
     pins.test_outcome_keys_match_stable_sort_brute_force,
     pins.test_key_counts_from_d3d_preparation_table,
+    pins.test_d3d_pack_worked_example,
+    pins.test_d3d_pack_hit_block_continues_confirmed_text,
     pins.test_hit_test_brute_force,
     pins.test_compaction_brute_force,
     pins.test_invalid_rows_and_degenerate_K0,

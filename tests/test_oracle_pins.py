@@ -524,3 +524,81 @@ def test_uniforms_are_uniform_and_exact(oracle_lib):
     assert a != oracle_lib.uniform(2, 2, 3, 0) and a != oracle_lib.uniform(1, 3, 3, 0)
     assert a != oracle_lib.uniform(1, 2, 4, 0) and a != oracle_lib.uniform(1, 2, 3, 1)
     assert a != oracle_lib.uniform(1 << 32, 2, 3, 0)
+
+
+# ------------------------------------------------------------ D3D packing --
+def test_d3d_pack_worked_example(oracle_lib):
+    """[D3D] worked example: the round confirms 今日 は いい 天気 and です
+    replaces だ.  The continuation keyed (3, です) must start right after
+    the confirmed text: block 0's first ctx tokens plus its anchor give
+    exactly the anchor and the round's emitted tokens."""
+    g, ids, target, draftl, tokens = _worked_example_inputs()
+    K = tokens.size
+    r = oracle_lib.verify(target[None], draftl[None], tokens[None], [0.0], seed=1)
+    anchor, pos0, mask = ids[g["anchor"][0]], 40, -7
+    keys = np.array([[[3, ids["です"]], [1, ids["ね"]], [-1, -1]]], np.int32)
+    t, p, c = oracle_lib.d3d_pack(keys, tokens[None], [anchor], [pos0], mask)
+    assert list(t[0, 0]) == [anchor] + list(tokens) and list(p[0, 0]) == list(range(40, 46))
+    assert list(t[0, 1]) == [ids["です"]] + [mask] * K
+    assert list(p[0, 1]) == list(range(44, 50)) and c[0, 1] == 4 == int(r["tau"][0])
+    confirmed = list(t[0, 0, :c[0, 1]]) + [t[0, 1, 0]]
+    assert confirmed == [anchor] + list(r["out_tokens"][0, :int(r["tau"][0])])
+    assert [ids[w] for w in g["expect_packed"]] == confirmed[1:]
+    assert c[0, 0] == 0 and c[0, 2] == 2 and list(p[0, 2]) == list(range(42, 48))
+    assert list(t[0, 3]) == [-1] * (K + 1) and list(p[0, 3]) == [-1] * (K + 1) and c[0, 3] == -1
+
+
+def test_d3d_pack_sizes_from_preparation_table(oracle_lib):
+    """[D3D] パック: 23 continuations plus the block under verification are
+    24 blocks of 16 = 384 tokens; the table's 512 and 912 likewise."""
+    K, V, B = 15, 64, 2
+    rng = np.random.default_rng(47)
+    draft = rng.normal(size=(B, K, V)).astype(np.float32)
+    bonus = rng.normal(size=(B, V)).astype(np.float32)
+    tokens = draft.argmax(-1).astype(np.int32)
+    for line in open(os.path.join(GOLDEN, "d3d_prep_table.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        positions, cands, prepared = map(int, line.split())
+        fanout = [cands] * positions + [0] * (K - positions) + [1]
+        keys = oracle_lib.outcome_predict(draft, tokens, fanout, bonus)
+        t, p, c = oracle_lib.d3d_pack(keys, tokens, [5, 6], [100, 200], -1)
+        assert t.shape[1:] == (prepared // 16, 16) and t[0].size == prepared
+        assert (c >= 0).all()          # every key found a candidate: no empty block
+
+
+def test_d3d_pack_hit_block_continues_confirmed_text(oracle_lib):
+    """Over random rounds with keys: the block keyed by the real outcome (a
+    hit) sees exactly tau tokens of block 0 and continues at the position
+    after them; every block's positions are consecutive and start ctx after
+    the anchor's."""
+    rng = np.random.default_rng(53)
+    B, K, V = 64, 6, 24
+    target = rng.normal(0, 2, size=(B, K + 1, V)).astype(np.float32)
+    draft = (target[:, :K] + rng.normal(0, 0.5, size=(B, K, V))).astype(np.float32)
+    temps = rng.choice([0.0, 0.8], size=B).astype(np.float32)
+    tokens = np.where(temps[:, None] == 0, draft.argmax(-1),
+                      rng.integers(0, V, size=(B, K))).astype(np.int32)
+    fanout = [3] * K + [2]
+    keys = oracle_lib.outcome_predict(draft, tokens, fanout, target[:, K])
+    r = oracle_lib.verify(target, draft, tokens, temps, seed=9, keys=keys)
+    anchor = rng.integers(0, V, size=B).astype(np.int32)
+    pos0 = rng.integers(0, 1000, size=B).astype(np.int32)
+    t, p, c = oracle_lib.d3d_pack(keys, tokens, anchor, pos0, -3)
+    hits = 0
+    for b in range(B):
+        assert c[b, 0] == 0
+        for i in range(1, t.shape[1]):
+            if c[b, i] < 0:
+                continue
+            assert list(p[b, i]) == list(range(p[b, i, 0], p[b, i, 0] + K + 1))
+            assert p[b, i, 0] - pos0[b] == c[b, i]
+        tau, tok = int(r["tau"][b]), int(r["out_tokens"][b, int(r["num_accepted"][b])])
+        hit_blocks = [i for i in range(1, t.shape[1])
+                      if c[b, i] == tau and t[b, i, 0] == tok]
+        assert bool(hit_blocks) == bool(r["hit"][b])
+        for i in hit_blocks:
+            hits += 1
+            confirmed = list(t[b, 0, :c[b, i]]) + [t[b, i, 0]]
+            assert confirmed == [anchor[b]] + list(r["out_tokens"][b, :tau])
+    assert hits > 0
