@@ -55,6 +55,8 @@ def describe(name):
     d = f"{name}: B={s['B']} K={s['K']} V={s['V']} {s['dtype']} {s['kind']} T={s['temperature']}"
     if s.get("fanout"):
         d += f" fanout={','.join(map(str, s['fanout']))} + draft bonus row"
+    if s.get("pack"):
+        d += " + drafter pack of (1 + keys) blocks of K+1 tokens"
     return d
 
 
@@ -200,12 +202,22 @@ def run_gpu(args):
             for _ in range(n_sets)]
     stream = torch.cuda.Stream(dev)
     wss = sd.workspace(B, K, dev, stream)
+    pack = "anchor" in one.meta   # the D3D workload also packs the drafter's next pass
+    n_keys = sum(fan) if fan else 0
+    packs = [(torch.empty((B, 1 + n_keys, K + 1), dtype=torch.int32, device=dev),
+              torch.empty((B, 1 + n_keys, K + 1), dtype=torch.int32, device=dev),
+              torch.empty((B, 1 + n_keys), dtype=torch.int32, device=dev))
+             for _ in range(n_sets)] if pack else None
 
     def step(i):
         p = pool[i % n_sets]
+        o = outs[i % n_sets]
         sd.verify(p.target, p.draft, p.tokens, p.temperature, p.seed + i // n_sets,
                   row_base=p.meta["row_base"], fanout=fan, draft_bonus=p.draft_bonus,
-                  compact=True, out=outs[i % n_sets], ws=wss, stream=stream)
+                  compact=True, out=o, ws=wss, stream=stream)
+        if pack:
+            sd.d3d_pack(o.keys, p.tokens, p.meta["anchor"], p.meta["anchor_pos"],
+                        p.meta["mask_token"], out=packs[i % n_sets], stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
@@ -272,8 +284,11 @@ def run_gpu(args):
                 t = getattr(p, k)
                 if t is not None:
                     hp[k] = t.cpu().pin_memory()
+            if pack:
+                hp["anchor"] = p.meta["anchor"].cpu().pin_memory()
+                hp["anchor_pos"] = p.meta["anchor_pos"].cpu().pin_memory()
             host.append(hp)
-        dbuf = {k: torch.empty_like(getattr(pool[0], k)) for k in host[0]}
+        dbuf = {k: torch.empty_like(v, device=dev) for k, v in host[0].items()}
         r_host = {"out_tokens": torch.empty((B, K + 1), dtype=torch.int32).pin_memory(),
                   "tau": torch.empty(B, dtype=torch.int32).pin_memory(),
                   "hit": torch.empty(B, dtype=torch.uint8).pin_memory(),
@@ -293,6 +308,9 @@ def run_gpu(args):
                           pool[0].seed + i, row_base=rank * B, fanout=fan,
                           draft_bonus=dbuf.get("draft_bonus"), compact=True, out=out0, ws=wss,
                           stream=stream)
+                if pack:
+                    sd.d3d_pack(out0.keys, dbuf["tokens"], dbuf["anchor"], dbuf["anchor_pos"],
+                                pool[0].meta["mask_token"], out=packs[0], stream=stream)
                 for k, t in r_host.items():
                     t.copy_(getattr(out0, k), non_blocking=True)
 
@@ -330,7 +348,7 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": alg, "formula_bytes_per_launch": formula},
         # per step: the cluster kernel and the packing launch, or the streaming
         # grid, the finish and the packing launch (split launch)
-        "gpu_launches": launches_per_step(B, K) * steps,
+        "gpu_launches": (launches_per_step(B, K) + (1 if pack else 0)) * steps,
         "clocks": clocks,
         "e2e": e2e,
         "hit_rate": hit_rate, "mean_tau": mean_tau, "status_bits": st,
@@ -360,13 +378,19 @@ def _oracle_round(inp: W.Inputs, rows, threads):
             keys = oracle.outcome_predict(d[b:b + 1], tok[b:b + 1], fan,
                                           None if bonus is None else bonus[b:b + 1])
         return oracle.verify(t[b:b + 1], d[b:b + 1], tok[b:b + 1], temps[b:b + 1], inp.seed,
-                             row_base=int(b), keys=keys)
+                             row_base=int(b), keys=keys), keys
 
     with ThreadPoolExecutor(threads) as ex:
-        res = list(ex.map(one, rows))
+        pairs = list(ex.map(one, rows))
+    res = [r for r, _ in pairs]
     out = np.concatenate([r["out_tokens"] for r in res])
     tau = np.concatenate([r["tau"] for r in res])
     oracle.compact(out, tau)
+    if "anchor" in inp.meta:   # the D3D workload also packs the drafter's next pass
+        idx = np.asarray(rows)
+        oracle.d3d_pack(np.concatenate([k for _, k in pairs]), tok[idx],
+                        inp.meta["anchor"].cpu().numpy()[idx],
+                        inp.meta["anchor_pos"].cpu().numpy()[idx], inp.meta["mask_token"])
     return res
 
 

@@ -208,6 +208,28 @@ sd_status_t sd_outcome_predict(int32_t B, int32_t K, int32_t V, sd_dtype_t dtype
                                void *stream);
 
 /*
+ * The drafter's next pass, packed from the outcome keys ("LLMの生成を5倍速く
+ * する「D3D」を図で読む" (animemo.app), sections 答え:ありうる結果すべてに、
+ * 先回りして下書きする and パック:24ブロックを1回の計算で).  A block is K+1
+ * tokens.  Block 0 is the block under verification: anchor[b] (the last
+ * settled token) and the K drafts, at positions anchor_pos[b] + i.  Block
+ * 1 + s is the continuation of key s = (k, c) of keys [B][n_keys][2] (as
+ * sd_outcome_predict writes them): c at position anchor_pos[b] + 1 + k (the
+ * place of the rejected draft k, or the bonus place when k == K), then K
+ * copies of mask_token at the following positions; an empty key (-1, -1)
+ * or k outside [0, K] gives an empty block (tokens, positions, ctx all -1).
+ * ctx[b][blk]: tokens of block 0 that block blk sees besides the shared
+ * prefix -- 0 for block 0 (it sees itself), k + 1 for a continuation.
+ * Outputs tokens, positions [B][1 + n_keys][K + 1] and ctx [B][1 + n_keys],
+ * caller-owned device memory; keys must be 8-byte aligned.  With K = 15
+ * and fanout 2 x 11 + 1 this is the pages' 24 blocks x 16 = 384 tokens.
+ */
+sd_status_t sd_d3d_pack(int32_t B, int32_t K, int32_t n_keys, const int32_t *keys,
+                        const int32_t *draft_tokens, const int32_t *anchor,
+                        const int32_t *anchor_pos, int32_t mask_token, int32_t *tokens,
+                        int32_t *positions, int32_t *ctx, void *stream);
+
+/*
  * Compaction: offsets[b] = sum of tau over rows before b (B+1 entries) and
  * packed[offsets[b] + i] = out_tokens[b][i] for i < tau[b].  packed needs
  * room for B*(K+1) tokens.  Entries of tau outside [0, K+1] set

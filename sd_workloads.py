@@ -22,6 +22,12 @@ Workloads (logit layouts: target [B][K+1][V], draft [B][K][V], row-major):
             fan-out 4,3,2,1,1,1,1 (F=4).
   mix       B=256, K=4, V=128256, bf16 as "zipf"; per-row temperature drawn
             uniformly from {0, 0.6, 1.0}.
+  d3d       B=16, K=15, V=151936, bf16 as "zipf", greedy (T=0); a block of
+            16 tokens (anchor + 15 drafts), keys for rejection positions
+            1..11 with two candidates each plus the all-accepted bonus key
+            (fan-out 2 x 11, 0 x 4, 1: 23 keys, a 24-block pack of 384
+            tokens), a bonus draft row, a seeded anchor token and anchor
+            position per row for the pack, mask token id V.
 
 The per-round uniforms of the verify step are keyed by ``seed`` (one per
 round), which the generator returns with the inputs.
@@ -45,9 +51,12 @@ WORKLOADS = {
                     bonus_row=True, fanout=[4, 3, 2, 1, 1, 1, 1]),
     "mix": dict(B=256, K=4, V=128256, dtype="bf16", kind="zipf", temperature="mix",
                 rounds=1000, base_seed=1239),
+    "d3d": dict(B=16, K=15, V=151936, dtype="bf16", kind="zipf", temperature=0.0,
+                rounds=2000, base_seed=1240, bonus_row=True,
+                fanout=[2] * 11 + [0] * 4 + [1], pack=True),
 }
 # the workloads in the order they are usually listed (1..5)
-ORDER = ["small", "peaked", "zipf", "saguaro", "mix"]
+ORDER = ["small", "peaked", "zipf", "saguaro", "mix", "d3d"]
 
 
 @dataclass
@@ -171,7 +180,16 @@ def workload(name: str, round_idx: int = 0, device="cpu", **override) -> Inputs:
     spec.update(override)
     spec.pop("rounds")
     base = spec.pop("base_seed")
-    return synth(seed=base, round_idx=round_idx, device=device, **spec)
+    pack = spec.pop("pack", False)
+    inp = synth(seed=base, round_idx=round_idx, device=device, **spec)
+    if pack:  # the settled token before each block and its position
+        g = _gen(base * 7919 + round_idx, "cpu")
+        inp.meta["anchor"] = torch.randint(0, inp.V, (inp.B,), generator=g,
+                                           dtype=torch.int32).to(device)
+        inp.meta["anchor_pos"] = torch.randint(0, 8192, (inp.B,), generator=g,
+                                               dtype=torch.int32).to(device)
+        inp.meta["mask_token"] = inp.V
+    return inp
 
 
 def logit_bytes(inp: Inputs, algorithmic: bool = True, with_bonus: bool = True) -> int:
@@ -181,8 +199,11 @@ def logit_bytes(inp: Inputs, algorithmic: bool = True, with_bonus: bool = True) 
     B, K, V = inp.B, inp.K, inp.V
     es = inp.target.element_size()
     if algorithmic:
+        # sampled rows read every draft row; greedy rows only those with keys
         n_sampled = int((inp.temperature > 0).sum().item())
-        n = B * (K + 1) * V + n_sampled * K * V
+        fan = inp.fanout or [0] * (K + 1)
+        n_keyed = sum(1 for j in range(K) if fan[j] > 0)
+        n = B * (K + 1) * V + n_sampled * K * V + (B - n_sampled) * n_keyed * V
     else:
         n = (2 * K + 1) * V * B
     if with_bonus and inp.draft_bonus is not None:

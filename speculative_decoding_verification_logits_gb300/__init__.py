@@ -79,6 +79,8 @@ def lib():
             L.sd_outcome_predict.restype = ctypes.c_int
             L.sd_compact.argtypes = [i32, i32, _P, _P, _P, _P, _P, _P]
             L.sd_compact.restype = ctypes.c_int
+            L.sd_d3d_pack.argtypes = [i32, i32, i32, _P, _P, _P, _P, i32, _P, _P, _P, _P]
+            L.sd_d3d_pack.restype = ctypes.c_int
             L.sd_uniforms.argtypes = [u64, i32, _P, _P, _P, _P, _P]
             L.sd_uniforms.restype = ctypes.c_int
             L.sd_verify_args_size.argtypes = []
@@ -290,6 +292,33 @@ def outcome_predict(draft, tokens, fanout, draft_bonus=None, *, keys=None, statu
                                     _ptr(status), _stream(dev, stream)), "sd_outcome_predict")
     assert n_out.value == n
     return keys
+
+
+def d3d_pack(keys, draft_tokens, anchor, anchor_pos, mask_token: int, *, out=None,
+             stream=None):
+    """The drafter's packed next pass: (tokens, positions) [B][1+n_keys][K+1]
+    and ctx [B][1+n_keys] from keys [B][n_keys][2], draft_tokens [B][K],
+    anchor [B] and anchor_pos [B] (int32, CUDA)."""
+    _need(keys, "keys", torch.int32)
+    B, n_keys, two = keys.shape
+    if two != 2:
+        raise ValueError("keys must be [B][n_keys][2]")
+    dev = keys.device
+    _need(draft_tokens, "draft_tokens", torch.int32, None, dev)
+    if draft_tokens.dim() != 2 or draft_tokens.shape[0] != B:
+        raise ValueError("draft_tokens must be [B][K]")
+    K = draft_tokens.shape[1]
+    _need(anchor, "anchor", torch.int32, (B,), dev)
+    _need(anchor_pos, "anchor_pos", torch.int32, (B,), dev)
+    if out is None:
+        out = (torch.empty((B, 1 + n_keys, K + 1), dtype=torch.int32, device=dev),
+               torch.empty((B, 1 + n_keys, K + 1), dtype=torch.int32, device=dev),
+               torch.empty((B, 1 + n_keys), dtype=torch.int32, device=dev))
+    t, p, c = out
+    _check(lib().sd_d3d_pack(B, K, n_keys, _ptr(keys), _ptr(draft_tokens), _ptr(anchor),
+                             _ptr(anchor_pos), int(mask_token), _ptr(t), _ptr(p), _ptr(c),
+                             _stream(dev, stream)), "sd_d3d_pack")
+    return t, p, c
 
 
 def compact(out_tokens, tau, *, offsets=None, packed=None, status=None, stream=None):

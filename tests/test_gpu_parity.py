@@ -415,3 +415,53 @@ def test_many_rounds_mismatch_count(dev, path, name, rounds):
     print(f"{name}: {tot}")
     assert tot["mismatch_outside_guard"] == 0
     assert tot["guarded_mismatch"] <= max(1, 1e-4 * tot["positions"])
+
+
+# ------------------------------------------------------------ D3D packing --
+@pytest.mark.parametrize("B,K,n_keys", [(1, 15, 23), (16, 15, 23), (300, 7, 13), (5, 32, 40),
+                                        (3, 0, 2), (4, 5, 0), (7, 15, 56)])
+def test_d3d_pack_matches_oracle(dev, B, K, n_keys):
+    # keys as sd_outcome_predict writes them, plus empty slots and positions
+    # outside [0, K]; integer layout work: exact
+    rng = np.random.default_rng(1000 + B + K + n_keys)
+    keys = np.stack([rng.integers(-1, K + 2, size=(B, n_keys)),
+                     rng.integers(0, 50000, size=(B, n_keys))], -1).astype(np.int32)
+    keys[rng.random((B, n_keys)) < 0.2] = -1
+    tok = rng.integers(0, 50000, size=(B, K)).astype(np.int32)
+    anchor = rng.integers(0, 50000, size=B).astype(np.int32)
+    pos = rng.integers(0, 100000, size=B).astype(np.int32)
+    t_ref, p_ref, c_ref = oracle.d3d_pack(keys, tok, anchor, pos, 50001)
+    g = lambda a: torch.from_numpy(a).to(dev)
+    t, p, c = sd.d3d_pack(g(keys), g(tok), g(anchor), g(pos), 50001)
+    np.testing.assert_array_equal(t.cpu().numpy(), t_ref)
+    np.testing.assert_array_equal(p.cpu().numpy(), p_ref)
+    np.testing.assert_array_equal(c.cpu().numpy(), c_ref)
+
+
+def test_d3d_workload_pack_after_verify(dev, path):
+    # the D3D round at full size: verify with fused keys, then the pack from
+    # the kernel's own keys; the pack equals the oracle's for those keys, and
+    # on every hit row the block of the real outcome continues the confirmed
+    # text exactly
+    inp = W.workload("d3d", round_idx=2, device=dev)
+    m = inp.meta
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed,
+                  fanout=inp.fanout, draft_bonus=inp.draft_bonus, compact=True)
+    t, p, c = sd.d3d_pack(r.keys, inp.tokens, m["anchor"], m["anchor_pos"], m["mask_token"])
+    torch.cuda.synchronize()
+    keys = r.keys.cpu().numpy()
+    assert keys.shape[1] == 23 and t.shape[1:] == (24, 16)     # 24 blocks x 16 = 384 tokens
+    t_ref, p_ref, c_ref = oracle.d3d_pack(keys, inp.tokens.cpu().numpy(),
+                                          m["anchor"].cpu().numpy(),
+                                          m["anchor_pos"].cpu().numpy(), m["mask_token"])
+    np.testing.assert_array_equal(t.cpu().numpy(), t_ref)
+    np.testing.assert_array_equal(p.cpu().numpy(), p_ref)
+    np.testing.assert_array_equal(c.cpu().numpy(), c_ref)
+    tau, na, out = r.tau.cpu().numpy(), r.num_accepted.cpu().numpy(), r.out_tokens.cpu().numpy()
+    hit = r.hit.cpu().numpy()
+    anchor = m["anchor"].cpu().numpy()
+    for b in range(inp.B):
+        blocks = [i for i in range(1, 24) if c_ref[b, i] == tau[b] and t_ref[b, i, 0] == out[b, na[b]]]
+        assert bool(blocks) == bool(hit[b])
+        for i in blocks:
+            assert list(t_ref[b, 0, :tau[b]]) + [t_ref[b, i, 0]] == [anchor[b]] + list(out[b, :tau[b]])
