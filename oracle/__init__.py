@@ -81,6 +81,8 @@ def _bind(L):
     L.oracle_compact.argtypes = [i32, i32, P, P, P, P]
     L.oracle_d3d_pack.argtypes = [i32, i32, i32, P, P, P, P, i32, P, P, P]
     L.oracle_d3d_pack.restype = None
+    L.oracle_ngram_draft.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P]
+    L.oracle_ngram_draft.restype = None
     L.oracle_compact.restype = None
     return L
 
@@ -225,3 +227,16 @@ def d3d_pack(keys, draft_tokens, anchor, anchor_pos, mask_token: int):
                           _ptr(anchor_pos), int(mask_token), _ptr(tokens), _ptr(positions),
                           _ptr(ctx))
     return tokens, positions, ctx
+
+
+def ngram_draft(history, lengths, K: int, n_max: int, n_min: int):
+    """Prompt-lookup drafts: (drafts [B][K], count [B], match_pos [B],
+    match_n [B]) from history [B][L] int32 and lengths [B]."""
+    history = np.ascontiguousarray(history, dtype=np.int32)
+    B, L = history.shape
+    lengths = np.ascontiguousarray(lengths, dtype=np.int32).reshape(B)
+    drafts = np.zeros((B, K), np.int32)
+    count, pos, n = (np.zeros(B, np.int32) for _ in range(3))
+    lib().oracle_ngram_draft(B, L, K, n_max, n_min, _ptr(history), _ptr(lengths), _ptr(drafts),
+                             _ptr(count), _ptr(pos), _ptr(n))
+    return drafts, count, pos, n

@@ -441,4 +441,49 @@ void oracle_d3d_pack(int B, int K, int n_keys, const int32_t *keys, const int32_
   }
 }
 
+// N-gram / prompt-lookup drafting ([SD] FAQ "is a separate draft model
+// always needed?": the engine finds a matching span in the prompt and recent
+// output and copies the tokens that follow it as drafts; [SSD] Saguaro
+// fallback: an n-gram model as the light fallback drafter at large batch).
+// For each row b with history h[0..len): for n = n_max down to n_min, the
+// last n tokens h[len-n..len) are searched for at earlier places: the
+// latest i with i + n < len (the span must be followed by at least one
+// token) and h[i..i+n) == h[len-n..len).  The first n that has such an i
+// wins; the drafts are h[i+n .. min(i+n+K, len)), the remaining slots -1.
+// No match: count 0, all -1, match_pos and match_n -1.
+// history: [B][L] (row b uses its first len[b] tokens); drafts: [B][K].
+void oracle_ngram_draft(int B, int L, int K, int n_max, int n_min, const int32_t *history,
+                        const int32_t *len, int32_t *drafts, int32_t *count, int32_t *match_pos,
+                        int32_t *match_n) {
+  for (int b = 0; b < B; ++b) {
+    const int32_t *h = history + (size_t)b * L;
+    const int n_tok = len[b];
+    int best_i = -1, best_n = -1;
+    for (int n = n_max; n >= n_min && best_i < 0; --n) {
+      if (n > n_tok) continue;
+      for (int i = n_tok - n - 1; i >= 0; --i) {  // latest first; i + n < n_tok
+        bool same = true;
+        for (int t = 0; t < n && same; ++t) same = h[i + t] == h[n_tok - n + t];
+        if (same) {
+          best_i = i;
+          best_n = n;
+          break;
+        }
+      }
+    }
+    int c = 0;
+    for (int j = 0; j < K; ++j) {
+      int v = -1;
+      if (best_i >= 0 && best_i + best_n + j < n_tok) {
+        v = h[best_i + best_n + j];
+        ++c;
+      }
+      drafts[(size_t)b * K + j] = v;
+    }
+    count[b] = c;
+    match_pos[b] = best_i;
+    match_n[b] = best_n;
+  }
+}
+
 }  // extern "C"

@@ -38,6 +38,10 @@ MUTANTS = {
     "pack_position_off_by_one": ("p[i] = anchor_pos[b] + 1 + k + i;",
                                  "p[i] = anchor_pos[b] + k + i;"),
     "pack_ctx_off_by_one": ("      c = k + 1;", "      c = k;"),
+    "ngram_earliest_match": ("for (int i = n_tok - n - 1; i >= 0; --i) {",
+                             "for (int i = 0; i <= n_tok - n - 1; ++i) {"),
+    "ngram_matches_itself": ("for (int i = n_tok - n - 1; i >= 0; --i) {",
+                             "for (int i = n_tok - n; i >= 0; --i) {"),
 }
 
 FAST_PINS = [
@@ -51,6 +55,8 @@ FAST_PINS = [
     pins.test_key_counts_from_d3d_preparation_table,
     pins.test_d3d_pack_worked_example,
     pins.test_d3d_pack_hit_block_continues_confirmed_text,
+    pins.test_ngram_draft_worked_example,
+    pins.test_ngram_draft_matches_substring_search,
     pins.test_hit_test_brute_force,
     pins.test_compaction_brute_force,
     pins.test_invalid_rows_and_degenerate_K0,

@@ -602,3 +602,47 @@ def test_d3d_pack_hit_block_continues_confirmed_text(oracle_lib):
             confirmed = list(t[b, 0, :c[b, i]]) + [t[b, i, 0]]
             assert confirmed == [anchor[b]] + list(r["out_tokens"][b, :tau])
     assert hits > 0
+
+
+# -------------------------------------------------- n-gram / prompt lookup --
+def test_ngram_draft_worked_example(oracle_lib):
+    """[SD] prompt-lookup drafting: the text ends with 1 2 3; its latest
+    earlier occurrence (positions 6..8) is followed by 7 4 1 2, which become
+    the drafts.  With n_max = 4 the 4-gram 4 1 2 3 has no earlier occurrence
+    and the 3-gram is used."""
+    h = np.array([[5, 1, 2, 3, 9, 9, 1, 2, 3, 7, 4, 1, 2, 3]], np.int32)
+    d, c, pos, n = oracle_lib.ngram_draft(h, [14], 4, 4, 1)
+    assert list(d[0]) == [7, 4, 1, 2] and c[0] == 4 and pos[0] == 6 and n[0] == 3
+    # K beyond the copied span: truncated, the rest -1
+    d, c, pos, n = oracle_lib.ngram_draft(h, [14], 8, 3, 1)
+    assert list(d[0]) == [7, 4, 1, 2, 3, -1, -1, -1] and c[0] == 5
+    # a history too short for any n-gram, and one with no repeat at all
+    d, c, pos, n = oracle_lib.ngram_draft(np.array([[1, 2, 3, 4]], np.int32), [4], 3, 2, 1)
+    assert c[0] == 0 and pos[0] == -1 and n[0] == -1 and list(d[0]) == [-1] * 3
+
+
+def _ngram_by_rfind(h, n_tok, K, n_max, n_min):
+    # independent restatement with Python's substring search: tokens become
+    # characters, the pattern is searched in the text minus its last token
+    s = "".join(chr(0x4E00 + int(t)) for t in h[:n_tok])
+    for n in range(n_max, n_min - 1, -1):
+        if n > n_tok:
+            continue
+        i = s.rfind(s[n_tok - n:], 0, n_tok - 1)
+        if i >= 0:
+            d = [int(t) for t in h[i + n:min(i + n + K, n_tok)]]
+            return d + [-1] * (K - len(d)), len(d), i, n
+    return [-1] * K, 0, -1, -1
+
+
+def test_ngram_draft_matches_substring_search(oracle_lib):
+    rng = np.random.default_rng(59)
+    B, L = 300, 80
+    h = rng.integers(0, 6, size=(B, L)).astype(np.int32)     # small vocabulary: many repeats
+    h[::7] = rng.integers(0, 1000, size=(len(h[::7]), L))     # and rows with almost none
+    lens = rng.integers(0, L + 1, size=B).astype(np.int32)
+    for K, n_max, n_min in [(5, 4, 1), (8, 3, 3), (3, 6, 2)]:
+        d, c, pos, n = oracle_lib.ngram_draft(h, lens, K, n_max, n_min)
+        for b in range(B):
+            want = _ngram_by_rfind(h[b], int(lens[b]), K, n_max, n_min)
+            assert (list(d[b]), int(c[b]), int(pos[b]), int(n[b])) == want, (b, K, n_max, n_min)
