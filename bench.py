@@ -130,12 +130,14 @@ def peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
+VERIFY_SOURCES = ("sd_device.cuh", "sd_split.cu", "sd_verify.cu")
+
+
 def kernel_src_hash():
-    """Hash of every CUDA source of the library (csrc/*.cu, *.cuh, sorted)."""
+    """Hash of the CUDA sources of the verify launches (the profiled kernels)."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(KERNEL_DIR, "*.cu")) +
-                    glob.glob(os.path.join(KERNEL_DIR, "*.cuh"))):
-        h.update(open(p, "rb").read())
+    for name in VERIFY_SOURCES:
+        h.update(open(os.path.join(KERNEL_DIR, name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -358,6 +360,126 @@ def run_gpu(args):
     return line
 
 
+# ------------------------------------------------ n-gram drafting workload ---
+def run_ngram(args):
+    """Prompt-lookup drafting rounds (one sd_ngram_draft launch per round)
+    over seeded histories; same timing rules as the verify workloads."""
+    import speculative_decoding_verification_logits_gb300 as sd
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sd.lib()
+    h0, lens, s = W.ngram_inputs(0, device=dev)
+    B, L, K, V = s["B"], s["L"], s["K"], s["V"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = h0.numel() * 4
+    n_sets = max(2, int(np.ceil(4 * l2 / set_bytes)) + 1)
+    pool = [h0] + [((h0.to(torch.int64) + 7919 * r) % V).to(torch.int32) for r in range(1, n_sets)]
+    e = lambda *sh: torch.empty(sh, dtype=torch.int32, device=dev)
+    outs = [(e(B, K), e(B), e(B), e(B)) for _ in range(n_sets)]
+    stream = torch.cuda.Stream(dev)
+
+    def step(i):
+        sd.ngram_draft(pool[i % n_sets], lens, K, s["n_max"], s["n_min"], out=outs[i % n_sets],
+                       stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize(dev)
+    G = min(args.steps, max(n_sets, (256 // n_sets) * n_sets))
+    graphs = {}
+    full, rem = divmod(args.steps, G)
+    plan = [G] * full + ([rem] if rem else [])
+    for n in set(plan):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i)
+        graphs[n] = g
+    with torch.cuda.stream(stream):
+        for n in set(plan):
+            graphs[n].replay()
+    torch.cuda.synchronize(dev)
+
+    def timed(fn):
+        if ws_n > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1)
+        if ws_n > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    def replay_all():
+        with torch.cuda.stream(stream):
+            for n in plan:
+                graphs[n].replay()
+
+    with ClockSampler(local) as clk:
+        ms = timed(replay_all)
+    clocks = clk.summary()
+    # history bytes the backward scan must read: from each row's end back to
+    # its match, or the whole row when nothing matches
+    mp = outs[0][2].cpu().numpy()
+    ln = lens.cpu().numpy()
+    alg = int(4 * np.where(mp >= 0, ln - mp, ln).sum())
+    e2e = None
+    if not args.no_e2e:
+        hh = [pool[0].cpu().pin_memory(), pool[1].cpu().pin_memory()]
+        dh = torch.empty_like(pool[0])
+        rh = [torch.empty((B, K), dtype=torch.int32).pin_memory(),
+              torch.empty(B, dtype=torch.int32).pin_memory()]
+        n_e2e = max(1, min(args.steps, args.e2e_steps))
+
+        def e2e_steps():
+            for i in range(n_e2e):
+                dh.copy_(hh[i % 2], non_blocking=True)
+                sd.ngram_draft(dh, lens, K, s["n_max"], s["n_min"], out=outs[0], stream=stream)
+                rh[0].copy_(outs[0][0], non_blocking=True)
+                rh[1].copy_(outs[0][1], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            e2e_steps()
+            ms_e2e = timed(e2e_steps)
+        e2e = {"value": ws_n * n_e2e / (ms_e2e / 1e3), "unit": UNIT, "steps": n_e2e,
+               "h2d_bytes_per_step": hh[0].numel() * 4, "d2h_bytes_per_step": B * (K + 1) * 4}
+    if ws_n > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    achieved = alg / (ms / args.steps / 1e3) / 1e9
+    return {
+        "metric": "n-gram drafting rounds/s", "value": ws_n * args.steps / (ms / 1e3),
+        "unit": UNIT, "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic (seeded phrase-book token histories)",
+        "config": {"workload": f"ngram: B={B} L={L} (lengths {L // 4}..{L}) K={K} "
+                               f"n={s['n_max']}..{s['n_min']}", "global_batch": B * ws_n,
+                   "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU",
+                   "l2": f"rotating {n_sets} history sets ({n_sets * set_bytes / 1e6:.0f} MB, "
+                         f"> 4x L2 {l2 / 1e6:.0f} MB)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk_kind,
+                     "kernel": "sd_ngram_kernel (duration = step time)",
+                     "algorithmic_bytes_per_launch": alg},
+        "gpu_launches": args.steps, "clocks": clocks, "e2e": e2e,
+        "match_rate": float((mp >= 0).mean()),
+    }
+
+
 # ------------------------------------------------------------- oracle arm ---
 def _oracle_round(inp: W.Inputs, rows, threads):
     """The oracle on the given rows of one round: outcome prediction, verify
@@ -422,6 +544,25 @@ def run_reference(args):
     oracle.build()
     name = args.workload
     cores = os.cpu_count() or 1
+    if name == "ngram":   # the oracle's drafter over whole rounds, one thread
+        h, lens, s = W.ngram_inputs(0)
+        hn, ln = h.numpy(), lens.numpy()
+        for _ in range(args.warmup):
+            oracle.ngram_draft(hn, ln, s["K"], s["n_max"], s["n_min"])
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle.ngram_draft(hn, ln, s["K"], s["n_max"], s["n_min"])
+        dt = time.perf_counter() - t0
+        v = args.steps / dt
+        return {"impl": "reference", "metric": "n-gram drafting rounds/s", "value": v,
+                "unit": UNIT, "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+                "config": {"workload": "ngram", "global_batch": s["B"]},
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                 "sample": "whole rounds, one thread"},
+                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
     inp = W.workload(name, round_idx=0, device="cpu")
     B = inp.B
     t0 = time.perf_counter()
@@ -454,14 +595,19 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=HEADLINE, choices=W.ORDER)
+    ap.add_argument("--workload", default=HEADLINE, choices=W.ORDER + ["ngram"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=400)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if args.impl == "reference":
+        line = run_reference(args)
+    elif args.workload == "ngram":
+        line = run_ngram(args)
+    else:
+        line = run_gpu(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

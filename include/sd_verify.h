@@ -230,6 +230,25 @@ sd_status_t sd_d3d_pack(int32_t B, int32_t K, int32_t n_keys, const int32_t *key
                         int32_t *positions, int32_t *ctx, void *stream);
 
 /*
+ * N-gram / prompt-lookup drafting ("What is speculative decoding" explainer
+ * (lotook.com), FAQ on drafting without a separate model: copy the tokens
+ * that follow a span of the prompt and recent output matching the text's
+ * ending; "Speculative Speculative Decoding" blog (jiwasawa.github.io),
+ * Saguaro fallback: an n-gram model as the light drafter at large batch).
+ * Row b's history is history[b][0..lengths[b]) of history [B][L] (int32
+ * tokens >= 0, lengths clamped to [0, L]).  For n = n_max down to n_min
+ * (1 <= n_min <= n_max <= 16), the last n tokens are looked up at earlier
+ * places followed by at least one token; the first n that occurs wins, at
+ * its latest occurrence i.  drafts[b][0..K) = the tokens from i + n on (at
+ * most up to the end of the history, then -1); count[b] = how many are
+ * real; match_pos[b] = i and match_n[b] = n, or -1 / -1 and count 0 when
+ * nothing matches.  One CTA per row; L < 2^26.
+ */
+sd_status_t sd_ngram_draft(int32_t B, int32_t L, int32_t K, int32_t n_max, int32_t n_min,
+                           const int32_t *history, const int32_t *lengths, int32_t *drafts,
+                           int32_t *count, int32_t *match_pos, int32_t *match_n, void *stream);
+
+/*
  * Compaction: offsets[b] = sum of tau over rows before b (B+1 entries) and
  * packed[offsets[b] + i] = out_tokens[b][i] for i < tau[b].  packed needs
  * room for B*(K+1) tokens.  Entries of tau outside [0, K+1] set

@@ -218,3 +218,44 @@ def to_numpy_logits(t: torch.Tensor):
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view("uint16")
     return t.numpy()
+
+
+# ------------------------------------------------------- n-gram drafting --
+# Token histories for the prompt-lookup drafter: each row is its prompt and
+# output so far, built from a per-row phrase book (48 phrases of 8-32 random
+# tokens, drawn with replacement) mixed with fresh random text (30 % of the
+# pieces, 1-7 tokens), so that the text's ending usually recurs earlier, as
+# in the summarising, editing and quoting the pages name.  One seeded base
+# set is drawn on the host; round r maps every token t to (t + 7919 r) mod V
+# (a bijection: every match stays where it was, the bytes differ).
+NGRAM = dict(B=256, L=16384, V=128256, K=4, n_max=4, n_min=1, base_seed=1241)
+
+
+def ngram_base(B, L, V, seed):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(L // 4, L + 1, size=B).astype(np.int32)
+    h = rng.integers(0, V, size=(B, L)).astype(np.int32)   # padding past the length: random
+    for b in range(B):
+        book = [rng.integers(0, V, size=int(rng.integers(8, 33))) for _ in range(48)]
+        pieces, total = [], 0
+        while total < lens[b]:
+            if rng.random() < 0.3:
+                p = rng.integers(0, V, size=int(rng.integers(1, 8)))
+            else:
+                p = book[int(rng.integers(0, 48))]
+            pieces.append(p)
+            total += len(p)
+        h[b, :lens[b]] = np.concatenate(pieces)[:lens[b]]
+    return h, lens
+
+
+def ngram_inputs(round_idx=0, device="cpu", **override):
+    """(history [B][L] int32, lengths [B] int32, spec) of one drafting round."""
+    spec = dict(NGRAM)
+    spec.update(override)
+    h, lens = ngram_base(spec["B"], spec["L"], spec["V"], spec["base_seed"])
+    h = torch.from_numpy(h).to(device)
+    if round_idx:
+        h = ((h.to(torch.int64) + 7919 * round_idx) % spec["V"]).to(torch.int32)
+    return h.contiguous(), torch.from_numpy(lens).to(device), spec

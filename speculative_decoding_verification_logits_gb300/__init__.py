@@ -81,6 +81,8 @@ def lib():
             L.sd_compact.restype = ctypes.c_int
             L.sd_d3d_pack.argtypes = [i32, i32, i32, _P, _P, _P, _P, i32, _P, _P, _P, _P]
             L.sd_d3d_pack.restype = ctypes.c_int
+            L.sd_ngram_draft.argtypes = [i32, i32, i32, i32, i32, _P, _P, _P, _P, _P, _P, _P]
+            L.sd_ngram_draft.restype = ctypes.c_int
             L.sd_uniforms.argtypes = [u64, i32, _P, _P, _P, _P, _P]
             L.sd_uniforms.restype = ctypes.c_int
             L.sd_verify_args_size.argtypes = []
@@ -319,6 +321,23 @@ def d3d_pack(keys, draft_tokens, anchor, anchor_pos, mask_token: int, *, out=Non
                              _ptr(anchor_pos), int(mask_token), _ptr(t), _ptr(p), _ptr(c),
                              _stream(dev, stream)), "sd_d3d_pack")
     return t, p, c
+
+
+def ngram_draft(history, lengths, K: int, n_max: int, n_min: int, *, out=None, stream=None):
+    """Prompt-lookup drafts (drafts [B][K], count, match_pos, match_n [B])
+    from history [B][L] and lengths [B] (int32, CUDA)."""
+    _need(history, "history", torch.int32)
+    B, L = history.shape
+    dev = history.device
+    _need(lengths, "lengths", torch.int32, (B,), dev)
+    if out is None:
+        e = lambda *s: torch.empty(s, dtype=torch.int32, device=dev)
+        out = (e(B, K), e(B), e(B), e(B))
+    d, c, p, n = out
+    _check(lib().sd_ngram_draft(B, L, K, n_max, n_min, _ptr(history), _ptr(lengths), _ptr(d),
+                                _ptr(c), _ptr(p), _ptr(n), _stream(dev, stream)),
+           "sd_ngram_draft")
+    return d, c, p, n
 
 
 def compact(out_tokens, tau, *, offsets=None, packed=None, status=None, stream=None):

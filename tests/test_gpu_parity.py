@@ -465,3 +465,33 @@ def test_d3d_workload_pack_after_verify(dev, path):
         assert bool(blocks) == bool(hit[b])
         for i in blocks:
             assert list(t_ref[b, 0, :tau[b]]) + [t_ref[b, i, 0]] == [anchor[b]] + list(out[b, :tau[b]])
+
+
+# ------------------------------------------------ n-gram / prompt lookup --
+@pytest.mark.parametrize("B,L,K,n_max,n_min,vocab", [(300, 80, 5, 4, 1, 6), (7, 1000, 8, 3, 3, 4),
+                                                     (64, 513, 0, 6, 2, 3), (5, 1, 4, 2, 1, 2),
+                                                     (40, 2048, 32, 16, 1, 2), (33, 300, 4, 4, 1, 50000)])
+def test_ngram_draft_matches_oracle(dev, B, L, K, n_max, n_min, vocab):
+    # small vocabularies give many and long matches, a large one almost none;
+    # lengths cover 0, 1 and the full row; exact
+    rng = np.random.default_rng(7 * B + L + K)
+    h = rng.integers(0, vocab, size=(B, L)).astype(np.int32)
+    lens = rng.integers(0, L + 1, size=B).astype(np.int32)
+    lens[0], lens[-1] = L, min(1, L)
+    ref = oracle.ngram_draft(h, lens, K, n_max, n_min)
+    out = sd.ngram_draft(torch.from_numpy(h).to(dev), torch.from_numpy(lens).to(dev), K, n_max,
+                         n_min)
+    for x, y in zip(out, ref):
+        np.testing.assert_array_equal(x.cpu().numpy(), y)
+
+
+def test_ngram_workload_full_size(dev):
+    # the benchmark's histories (256 rows up to 16384 tokens): every row exact
+    for rd in (0, 3):
+        h, lens, s = W.ngram_inputs(rd, device=dev)
+        ref = oracle.ngram_draft(h.cpu().numpy(), lens.cpu().numpy(), s["K"], s["n_max"],
+                                 s["n_min"])
+        out = sd.ngram_draft(h, lens, s["K"], s["n_max"], s["n_min"])
+        for x, y in zip(out, ref):
+            np.testing.assert_array_equal(x.cpu().numpy(), y)
+        assert (ref[3] >= 0).mean() > 0.8      # the histories repeat themselves
