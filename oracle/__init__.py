@@ -83,6 +83,8 @@ def _bind(L):
     L.oracle_d3d_pack.restype = None
     L.oracle_ngram_draft.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P]
     L.oracle_ngram_draft.restype = None
+    L.oracle_kv_rollback.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P]
+    L.oracle_kv_rollback.restype = None
     L.oracle_compact.restype = None
     return L
 
@@ -240,3 +242,17 @@ def ngram_draft(history, lengths, K: int, n_max: int, n_min: int):
     lib().oracle_ngram_draft(B, L, K, n_max, n_min, _ptr(history), _ptr(lengths), _ptr(drafts),
                              _ptr(count), _ptr(pos), _ptr(n))
     return drafts, count, pos, n
+
+
+def kv_rollback(block_table, kv_len, tau, page_size: int, appended: int):
+    """(block_table after, new_len [B], freed page ids, free_offsets [B+1])."""
+    bt = np.array(block_table, dtype=np.int32, copy=True)
+    B, max_pages = bt.shape
+    kv_len = np.ascontiguousarray(kv_len, dtype=np.int32).reshape(B)
+    tau = np.ascontiguousarray(tau, dtype=np.int32).reshape(B)
+    new_len = np.zeros(B, np.int32)
+    freed = np.full(max(B * max_pages, 1), -1, np.int32)
+    offs = np.zeros(B + 1, np.int32)
+    lib().oracle_kv_rollback(B, page_size, max_pages, appended, _ptr(kv_len), _ptr(tau), _ptr(bt),
+                             _ptr(new_len), _ptr(freed), _ptr(offs))
+    return bt, new_len, freed[: int(offs[-1])], offs

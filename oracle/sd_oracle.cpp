@@ -486,4 +486,37 @@ void oracle_ngram_draft(int B, int L, int K, int n_max, int n_min, const int32_t
   }
 }
 
+// KV-cache rollback after a round ([SD] FAQ on speculative decoding and the
+// KV cache: when the target rejects the drafts after some position, the
+// engine rolls both models' KV caches back and truncates them, dropping the
+// rejected entries before the next cycle).  Row b's cache holds kv_len[b]
+// entries in pages of page_size entries listed in block_table[b][0..); the
+// round appended `appended` of them (the verify pass: the anchor and the K
+// drafts, K + 1) and confirms the first tau[b] (the anchor and the accepted
+// drafts; the correction or bonus token has no entry yet; 0 for an invalid
+// row).  new_len = kv_len - appended + min(tau, appended) (appended and the
+// kept entries clamped to the entries the row holds).  The pages past
+// ceil(new_len / page_size), up to ceil(kv_len / page_size), are freed: their
+// ids go, row after row, to freed[free_offsets[b] ...] and their table
+// slots become -1.  free_offsets has B + 1 entries.
+void oracle_kv_rollback(int B, int page_size, int max_pages, int appended, const int32_t *kv_len,
+                        const int32_t *tau, int32_t *block_table, int32_t *new_len,
+                        int32_t *freed, int32_t *free_offsets) {
+  int32_t acc = 0;
+  for (int b = 0; b < B; ++b) {
+    const int before = std::max(kv_len[b] - appended, 0);    // entries older than the round
+    const int keep = std::min(std::min(std::max(tau[b], 0), appended), kv_len[b] - before);
+    const int n_new = before + keep;
+    const int used = (kv_len[b] + page_size - 1) / page_size;
+    const int still = (n_new + page_size - 1) / page_size;
+    new_len[b] = n_new;
+    free_offsets[b] = acc;
+    for (int p = still; p < used && p < max_pages; ++p) {
+      freed[acc++] = block_table[(size_t)b * max_pages + p];
+      block_table[(size_t)b * max_pages + p] = -1;
+    }
+  }
+  free_offsets[B] = acc;
+}
+
 }  // extern "C"

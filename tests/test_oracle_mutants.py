@@ -42,6 +42,10 @@ MUTANTS = {
                              "for (int i = 0; i <= n_tok - n - 1; ++i) {"),
     "ngram_matches_itself": ("for (int i = n_tok - n - 1; i >= 0; --i) {",
                              "for (int i = n_tok - n; i >= 0; --i) {"),
+    "rollback_keeps_tau_plus_one": ("std::min(std::max(tau[b], 0), appended)",
+                                    "std::min(std::max(tau[b] + 1, 0), appended)"),
+    "rollback_floor_pages": ("const int still = (n_new + page_size - 1) / page_size;",
+                             "const int still = n_new / page_size;"),
 }
 
 FAST_PINS = [
@@ -57,6 +61,8 @@ FAST_PINS = [
     pins.test_d3d_pack_hit_block_continues_confirmed_text,
     pins.test_ngram_draft_worked_example,
     pins.test_ngram_draft_matches_substring_search,
+    pins.test_kv_rollback_worked_example,
+    pins.test_kv_rollback_matches_entry_sets,
     pins.test_hit_test_brute_force,
     pins.test_compaction_brute_force,
     pins.test_invalid_rows_and_degenerate_K0,

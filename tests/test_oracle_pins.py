@@ -646,3 +646,45 @@ def test_ngram_draft_matches_substring_search(oracle_lib):
         for b in range(B):
             want = _ngram_by_rfind(h[b], int(lens[b]), K, n_max, n_min)
             assert (list(d[b]), int(c[b]), int(pos[b]), int(n[b])) == want, (b, K, n_max, n_min)
+
+
+# ------------------------------------------------------- KV-cache rollback --
+def test_kv_rollback_worked_example(oracle_lib):
+    """[D3D] worked example + [SD] rollback: the verify pass appended the
+    anchor 今日 and the five drafts (entries 64..69 after a 64-entry
+    prefix); the round confirms 今日 は いい 天気 (tau = 4), so entries 68
+    and 69 (だ, よ) go and with them the last 4-entry page."""
+    g, ids, target, draftl, tokens = _worked_example_inputs()
+    r = oracle_lib.verify(target[None], draftl[None], tokens[None], [0.0], seed=1)
+    tau = int(r["tau"][0])
+    bt = np.arange(100, 120, dtype=np.int32)[None]          # page ids of the row
+    bt2, new_len, freed, offs = oracle_lib.kv_rollback(bt, [70], [tau], 4, tokens.size + 1)
+    assert tau == 4 and new_len[0] == 68
+    assert list(freed) == [117] and list(offs) == [0, 1]
+    assert bt2[0, 17] == -1 and (bt2[0, :17] == bt[0, :17]).all() and (bt2[0, 18:] == bt[0, 18:]).all()
+
+
+def test_kv_rollback_matches_entry_sets(oracle_lib):
+    """Restated with sets of entries and pages: the cache keeps the entries
+    before the round plus the first min(tau, appended) appended ones; a page
+    stays while it holds a kept entry."""
+    rng = np.random.default_rng(61)
+    for page, appended in [(16, 6), (1, 3), (7, 9), (32, 33)]:
+        B, maxp = 50, 40
+        bt = rng.permutation(B * maxp).astype(np.int32).reshape(B, maxp)
+        kv = rng.integers(0, page * maxp + 1, size=B).astype(np.int32)
+        tau = rng.integers(0, appended + 3, size=B).astype(np.int32)   # some past appended
+        bt2, new_len, freed, offs = oracle_lib.kv_rollback(bt, kv, tau, page, appended)
+        want_free = []
+        for b in range(B):
+            before = max(int(kv[b]) - appended, 0)
+            kept = list(range(before)) + list(range(before, int(kv[b])))[:min(int(tau[b]), appended)]
+            assert new_len[b] == len(kept)
+            pages_kept = {e // page for e in kept}
+            pages_all = {e // page for e in range(int(kv[b]))}
+            gone = sorted(pages_all - pages_kept)
+            assert list(freed[offs[b]:offs[b + 1]]) == [int(bt[b, p]) for p in gone]
+            want_free += gone
+            for p in range(maxp):
+                assert bt2[b, p] == (-1 if p in gone else bt[b, p])
+        assert offs[-1] == len(want_free)
