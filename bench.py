@@ -56,7 +56,7 @@ def describe(name):
     if s.get("fanout"):
         d += f" fanout={','.join(map(str, s['fanout']))} + draft bonus row"
     if s.get("pack"):
-        d += " + drafter pack of (1 + keys) blocks of K+1 tokens"
+        d += " + drafter pack of (1 + keys) blocks of K+1 tokens + KV rollback"
     return d
 
 
@@ -210,6 +210,10 @@ def run_gpu(args):
               torch.empty((B, 1 + n_keys, K + 1), dtype=torch.int32, device=dev),
               torch.empty((B, 1 + n_keys), dtype=torch.int32, device=dev))
              for _ in range(n_sets)] if pack else None
+    rolls = [(torch.empty(B, dtype=torch.int32, device=dev),
+              torch.empty(p_.meta["block_table"].numel(), dtype=torch.int32, device=dev),
+              torch.empty(B + 1, dtype=torch.int32, device=dev))
+             for p_ in pool] if pack else None
 
     def step(i):
         p = pool[i % n_sets]
@@ -220,6 +224,10 @@ def run_gpu(args):
         if pack:
             sd.d3d_pack(o.keys, p.tokens, p.meta["anchor"], p.meta["anchor_pos"],
                         p.meta["mask_token"], out=packs[i % n_sets], stream=stream)
+            # roll the target's KV cache back to the confirmed tokens (the
+            # page table is reused from round to round: timing only)
+            sd.kv_rollback(p.meta["block_table"], p.meta["kv_len"], o.tau, p.meta["page_size"],
+                           K + 1, out=rolls[i % n_sets], stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
@@ -350,7 +358,7 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": alg, "formula_bytes_per_launch": formula},
         # per step: the cluster kernel and the packing launch, or the streaming
         # grid, the finish and the packing launch (split launch)
-        "gpu_launches": (launches_per_step(B, K) + (1 if pack else 0)) * steps,
+        "gpu_launches": (launches_per_step(B, K) + (2 if pack else 0)) * steps,
         "clocks": clocks,
         "e2e": e2e,
         "hit_rate": hit_rate, "mean_tau": mean_tau, "status_bits": st,
@@ -513,6 +521,9 @@ def _oracle_round(inp: W.Inputs, rows, threads):
         oracle.d3d_pack(np.concatenate([k for _, k in pairs]), tok[idx],
                         inp.meta["anchor"].cpu().numpy()[idx],
                         inp.meta["anchor_pos"].cpu().numpy()[idx], inp.meta["mask_token"])
+        oracle.kv_rollback(inp.meta["block_table"].cpu().numpy()[idx],
+                           inp.meta["kv_len"].cpu().numpy()[idx], tau,
+                           inp.meta["page_size"], inp.K + 1)
     return res
 
 

@@ -249,6 +249,26 @@ sd_status_t sd_ngram_draft(int32_t B, int32_t L, int32_t K, int32_t n_max, int32
                            int32_t *count, int32_t *match_pos, int32_t *match_n, void *stream);
 
 /*
+ * KV-cache rollback after a round ("What is speculative decoding" explainer
+ * (lotook.com), FAQ on speculative decoding and the KV cache: both caches
+ * are rolled back and truncated, dropping the rejected drafts' entries).
+ * Row b holds kv_len[b] entries in pages of page_size entries listed in
+ * block_table [B][max_pages] (in/out); the round appended `appended` of them
+ * (K + 1 for the target's verify pass: the anchor and the drafts) and
+ * confirms the first tau[b] (as sd_verify writes it; the correction or bonus
+ * token has no entry yet).  new_len[b] = before + min(tau, appended, held),
+ * before = max(kv_len - appended, 0), held = kv_len - before.  The pages
+ * from ceil(new_len / page_size) up to min(ceil(kv_len / page_size),
+ * max_pages) are freed: their ids go, row after row, to freed[] (room for
+ * B * max_pages ids) at free_offsets[b] (B + 1 entries, the last the total),
+ * and their table slots become -1.  One CTA.
+ */
+sd_status_t sd_kv_rollback(int32_t B, int32_t page_size, int32_t max_pages, int32_t appended,
+                           const int32_t *kv_len, const int32_t *tau, int32_t *block_table,
+                           int32_t *new_len, int32_t *freed, int32_t *free_offsets,
+                           void *stream);
+
+/*
  * Compaction: offsets[b] = sum of tau over rows before b (B+1 entries) and
  * packed[offsets[b] + i] = out_tokens[b][i] for i < tau[b].  packed needs
  * room for B*(K+1) tokens.  Entries of tau outside [0, K+1] set

@@ -27,7 +27,9 @@ Workloads (logit layouts: target [B][K+1][V], draft [B][K][V], row-major):
             1..11 with two candidates each plus the all-accepted bonus key
             (fan-out 2 x 11, 0 x 4, 1: 23 keys, a 24-block pack of 384
             tokens), a bonus draft row, a seeded anchor token and anchor
-            position per row for the pack, mask token id V.
+            position per row for the pack, mask token id V, and the target's
+            paged KV cache for the rollback (anchor position + K + 1 entries,
+            16-entry pages, a random page table).
 
 The per-round uniforms of the verify step are keyed by ``seed`` (one per
 round), which the generator returns with the inputs.
@@ -189,6 +191,14 @@ def workload(name: str, round_idx: int = 0, device="cpu", **override) -> Inputs:
         inp.meta["anchor_pos"] = torch.randint(0, 8192, (inp.B,), generator=g,
                                                dtype=torch.int32).to(device)
         inp.meta["mask_token"] = inp.V
+        # the target's paged KV cache: entries up to the anchor, plus the
+        # anchor and the K drafts the verify pass appended; 16-entry pages
+        page = 16
+        max_pages = (8192 + inp.K + 1 + page - 1) // page
+        inp.meta["page_size"] = page
+        inp.meta["kv_len"] = (inp.meta["anchor_pos"] + inp.K + 1).contiguous()
+        inp.meta["block_table"] = torch.randperm(inp.B * max_pages, generator=g).to(
+            torch.int32).reshape(inp.B, max_pages).to(device)
     return inp
 
 

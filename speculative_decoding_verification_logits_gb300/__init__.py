@@ -83,6 +83,8 @@ def lib():
             L.sd_d3d_pack.restype = ctypes.c_int
             L.sd_ngram_draft.argtypes = [i32, i32, i32, i32, i32, _P, _P, _P, _P, _P, _P, _P]
             L.sd_ngram_draft.restype = ctypes.c_int
+            L.sd_kv_rollback.argtypes = [i32, i32, i32, i32, _P, _P, _P, _P, _P, _P, _P]
+            L.sd_kv_rollback.restype = ctypes.c_int
             L.sd_uniforms.argtypes = [u64, i32, _P, _P, _P, _P, _P]
             L.sd_uniforms.restype = ctypes.c_int
             L.sd_verify_args_size.argtypes = []
@@ -338,6 +340,26 @@ def ngram_draft(history, lengths, K: int, n_max: int, n_min: int, *, out=None, s
                                 _ptr(c), _ptr(p), _ptr(n), _stream(dev, stream)),
            "sd_ngram_draft")
     return d, c, p, n
+
+
+def kv_rollback(block_table, kv_len, tau, page_size: int, appended: int, *, out=None,
+                stream=None):
+    """Roll row caches back after a round: block_table [B][max_pages] is
+    updated in place; returns (new_len [B], freed [B*max_pages], free_offsets
+    [B+1]) -- freed[:free_offsets[-1]] are the freed page ids."""
+    _need(block_table, "block_table", torch.int32)
+    B, max_pages = block_table.shape
+    dev = block_table.device
+    _need(kv_len, "kv_len", torch.int32, (B,), dev)
+    _need(tau, "tau", torch.int32, (B,), dev)
+    if out is None:
+        e = lambda *s: torch.empty(s, dtype=torch.int32, device=dev)
+        out = (e(B), e(max(B * max_pages, 1)), e(B + 1))
+    n, f, o = out
+    _check(lib().sd_kv_rollback(B, page_size, max_pages, appended, _ptr(kv_len), _ptr(tau),
+                                _ptr(block_table), _ptr(n), _ptr(f), _ptr(o),
+                                _stream(dev, stream)), "sd_kv_rollback")
+    return n, f, o
 
 
 def compact(out_tokens, tau, *, offsets=None, packed=None, status=None, stream=None):

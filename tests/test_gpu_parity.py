@@ -465,6 +465,16 @@ def test_d3d_workload_pack_after_verify(dev, path):
         assert bool(blocks) == bool(hit[b])
         for i in blocks:
             assert list(t_ref[b, 0, :tau[b]]) + [t_ref[b, i, 0]] == [anchor[b]] + list(out[b, :tau[b]])
+    # then the target's KV cache rolled back to the round's tau
+    bt = m["block_table"].clone()
+    n, f, o = sd.kv_rollback(bt, m["kv_len"], r.tau, m["page_size"], inp.K + 1)
+    bt_ref, n_ref, f_ref, o_ref = oracle.kv_rollback(m["block_table"].cpu().numpy(),
+                                                     m["kv_len"].cpu().numpy(), tau,
+                                                     m["page_size"], inp.K + 1)
+    np.testing.assert_array_equal(bt.cpu().numpy(), bt_ref)
+    np.testing.assert_array_equal(n.cpu().numpy(), n_ref)
+    np.testing.assert_array_equal(f.cpu().numpy()[: o_ref[-1]], f_ref)
+    assert (n_ref == m["anchor_pos"].cpu().numpy() + tau).all()   # the prefix plus tau
 
 
 # ------------------------------------------------ n-gram / prompt lookup --
@@ -495,3 +505,21 @@ def test_ngram_workload_full_size(dev):
         for x, y in zip(out, ref):
             np.testing.assert_array_equal(x.cpu().numpy(), y)
         assert (ref[3] >= 0).mean() > 0.8      # the histories repeat themselves
+
+
+# ------------------------------------------------------- KV-cache rollback --
+@pytest.mark.parametrize("B,page,maxp,appended", [(50, 16, 40, 6), (3000, 16, 8, 16), (7, 1, 64, 9),
+                                                  (1, 32, 3, 33), (1100, 7, 20, 5)])
+def test_kv_rollback_matches_oracle(dev, B, page, maxp, appended):
+    rng = np.random.default_rng(B + page + maxp)
+    bt = rng.permutation(B * maxp).astype(np.int32).reshape(B, maxp)
+    kv = rng.integers(0, page * maxp + page, size=B).astype(np.int32)   # some past the table
+    tau = rng.integers(0, appended + 3, size=B).astype(np.int32)
+    bt_ref, n_ref, f_ref, o_ref = oracle.kv_rollback(bt, kv, tau, page, appended)
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    btd = g(bt)
+    n, f, o = sd.kv_rollback(btd, g(kv), g(tau), page, appended)
+    np.testing.assert_array_equal(btd.cpu().numpy(), bt_ref)
+    np.testing.assert_array_equal(n.cpu().numpy(), n_ref)
+    np.testing.assert_array_equal(o.cpu().numpy(), o_ref)
+    np.testing.assert_array_equal(f.cpu().numpy()[: o_ref[-1]], f_ref)
