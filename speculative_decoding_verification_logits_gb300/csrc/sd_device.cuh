@@ -1093,6 +1093,11 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
   __shared__ Static S;
   extern __shared__ __align__(128) uint8_t dyn[];
 
+  // launched as a programmatic dependent of the stream's previous kernel:
+  // nothing is read before that kernel has finished and its writes are
+  // visible (the launch itself overlaps its tail); the split finish waits
+  // further down, for its streaming grid
+  if (!SPLIT) asm volatile("griddepcontrol.wait;" ::: "memory");
   // every CTA of the cluster has started before any pushes into its memory
   cluster_arrive_relaxed();
   if (SPLIT && warp == 0) {

@@ -64,9 +64,12 @@ __global__ void __launch_bounds__(NT, 2) sd_flat_stream_kernel(const __grid_cons
   __shared__ int goff[SD_MAX_K + 2];
   __shared__ int wcnt[kMaxWarps];
   extern __shared__ __align__(128) uint8_t dyn[];
-  // The finish grid may be scheduled at once: its CTAs take the place of
-  // streaming CTAs as those exit and run their prologue meanwhile (their
-  // griddepcontrol.wait still waits for this whole grid).
+  // Launched as a programmatic dependent of the stream's previous kernel:
+  // nothing is read before that kernel has finished.  Then the finish grid
+  // may be scheduled at once: its CTAs take the place of streaming CTAs as
+  // those exit and run their prologue meanwhile (reading only inputs, now
+  // complete; their griddepcontrol.wait still waits for this whole grid).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const FlatLayout FL = flat_layout(NT, KF, P.B);
   uint8_t *ring = dyn + FL.ring;
@@ -319,12 +322,18 @@ sd_status_t launch_split(Params &P, size_t ws_bytes, cudaStream_t stream) {
   const Layout L = make_layout(NT, rows_per_seq(P), P.K + 1, KF, cs, P.slice, sz);
   if (L.total > kDynSmemCap) return SD_ERR_UNSUPPORTED;
 
-  // the streaming grid: an ordinary launch behind the stream's earlier work
+  // the streaming grid: a programmatic dependent of the stream's previous
+  // kernel (it waits for it before reading anything)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)G, 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = (size_t)FL.total;
   cfg.stream = stream;
+  cudaLaunchAttribute attr0[1];
+  attr0[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr0[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr0;
+  cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, (void (*)(const Params))flat_fn<E, KF, NT>(), P);
   if (e != cudaSuccess) {
     fprintf(stderr, "sd_verify stream launch failed: %s\n", cudaGetErrorString(e));

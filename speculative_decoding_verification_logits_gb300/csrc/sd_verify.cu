@@ -75,13 +75,17 @@ static sd_status_t launch_nt(Params &P, cudaStream_t stream) {
   cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = (size_t)L.total;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // a programmatic dependent of the stream's previous kernel: the kernel
+  // waits for it before reading anything, the launch overlaps its tail
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (env_int("SDV_VERBOSE", 0))
     fprintf(stderr,
             "sd_verify: mode=%d B=%d K=%d V=%d cs=%d NT=%d slice=%d rowsplit=%d KF=%d smem=%d\n",
