@@ -2,8 +2,9 @@
 
     python -m speculative_decoding_verification_logits_gb300.profile_case WORKLOAD [ROUNDS]
 
-Two input sets of the workload alternate; every round is one fused verify
-launch (plus the packing launch).  Prints the mean tau of the last round.
+Two input sets of the workload alternate; every round is the verify step
+(plus the packing launch, and for the D3D workload the drafter pack and the
+KV rollback).  Prints the mean tau of the last round.
 """
 import os
 import sys
@@ -28,6 +29,10 @@ def main():
         p = pool[i % 2]
         r = sd.verify(p.target, p.draft, p.tokens, p.temperature, p.seed + i, fanout=fan,
                       draft_bonus=p.draft_bonus, compact=True)
+        if "anchor" in p.meta:   # the D3D round: the drafter pack and the KV rollback
+            m = p.meta
+            sd.d3d_pack(r.keys, p.tokens, m["anchor"], m["anchor_pos"], m["mask_token"])
+            sd.kv_rollback(m["block_table"], m["kv_len"], r.tau, m["page_size"], p.K + 1)
     torch.cuda.synchronize()
     print("ok", r.tau.float().mean().item())
 
