@@ -134,10 +134,15 @@ VERIFY_SOURCES = ("sd_device.cuh", "sd_split.cu", "sd_verify.cu")
 
 
 def kernel_src_hash():
-    """Hash of the CUDA sources of the verify launches (the profiled kernels)."""
+    """Hash of the code of the verify launches' CUDA sources (the profiled
+    kernels), comments and blank space left out: a profile stays current
+    while the code it measured does."""
     h = hashlib.sha256()
     for name in VERIFY_SOURCES:
-        h.update(open(os.path.join(KERNEL_DIR, name), "rb").read())
+        text = open(os.path.join(KERNEL_DIR, name), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,26 +1,27 @@
-// GB300 (sm_103a) kernels of the speculative-decoding verify step.
+// GB300 (sm_103a) library of the speculative-decoding verify step: the C ABI
+// entry points, their argument checks and the choice of launch plan, the
+// packing kernels and the uniforms audit kernel.
 //
-// Layout of the work: one thread-block cluster per sequence (row b of the
-// batch).  The cluster's CTAs split the vocabulary into contiguous slices;
-// each CTA streams its slice of every logit row of the sequence -- target
-// rows K..0 and draft rows K-1..0, plus the optional draft row of the bonus
-// position.  Each thread copies its own 16-byte vectors a few steps ahead
-// into its own shared-memory slots (cp.async, so no block-wide barrier is
-// needed while streaming) and keeps only per-row statistics in registers:
-// max, lowest-index argmax, the sum of 2^(l s + c) (s = log2(e) / T, c a
-// per-thread offset carried exactly into the combine) and, for draft rows,
-// the few vectors that can hold the top-F keys.  One exchange over
-// distributed shared memory gives every CTA the statistics of all K+1
-// positions, so each CTA evaluates the left-to-right accept scan itself and
-// all of them agree on the first rejection m.  Only then is a single
-// inverse-CDF draw needed per sequence: over the residual max(0, p - q) at m,
-// or over p at the bonus position K.  The CTAs re-read their slices of those
-// one or two rows (rows are streamed in the order K..0, so the likely m ~ 0
-// rows were read last and are still in L2), exchange slice masses, and the
-// CTA holding the crossing point scans it.  The owning CTA writes the
-// sequence's tokens and tau, and the last sequence to finish (one atomic
-// counter) packs all sequences' tokens.  Nothing waits on another cluster
-// and there are no spin-waits.
+// Two launch plans compute the verify step (the kernels are in
+// sd_device.cuh and sd_split.cu):
+//  * the cluster kernel: one thread-block cluster per sequence.  Its CTAs
+//    split the vocabulary (or the sequence's rows laid end to end) and
+//    stream every logit row of the sequence once -- target rows K..0, draft
+//    rows K-1..0, the optional draft row of the bonus position -- keeping
+//    per-row statistics in registers (max, lowest-index argmax, the sum of
+//    2^(l s + c), the vectors that can hold the top-F keys).  One exchange
+//    over distributed shared memory gives every CTA the statistics of all
+//    positions, so every CTA runs the left-to-right accept scan itself and
+//    they agree on the first rejection m.  One inverse-CDF draw follows:
+//    over the residual max(0, p - q) at m, or over p at the bonus position;
+//    the CTAs re-read their slices of those rows (streamed last, so mostly
+//    from L2), exchange slice masses, and the CTA holding the crossing point
+//    scans it.  The owning CTA writes the sequence's tokens and tau.
+//  * the split launch (with caller scratch): a flat streaming grid over the
+//    rows of all sequences writes per-piece statistics, and a per-sequence
+//    finish -- the cluster kernel's code after its exchange -- combines them.
+// A one-CTA packing launch follows either as its programmatic dependent.
+// Nothing waits on another cluster and there are no spin-waits.
 //
 // Method sources (web pages, stated in prose there):
 //  "What is speculative decoding" explainer (lotook.com): the four-stage loop
