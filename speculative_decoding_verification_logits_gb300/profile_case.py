@@ -21,6 +21,15 @@ def main():
     name = sys.argv[1] if len(sys.argv) > 1 else "saguaro"
     n = int(sys.argv[2]) if len(sys.argv) > 2 else 4
     dev = torch.device("cuda:0")
+    if name == "ngram":   # prompt-lookup drafting rounds over two history sets
+        sets = [W.ngram_inputs(r, device=dev) for r in range(2)]
+        out = None
+        for i in range(n):
+            h, lens, s = sets[i % 2]
+            out = sd.ngram_draft(h, lens, s["K"], s["n_max"], s["n_min"])
+        torch.cuda.synchronize()
+        print("ok", float((out[3] >= 0).float().mean().item()))
+        return
     spec = W.WORKLOADS[name]
     fan = spec.get("fanout")
     pool = [W.workload(name, round_idx=i, device=dev) for i in range(2)]
