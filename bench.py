@@ -160,21 +160,31 @@ def profiled_traffic(workload):
     return float(m.group(1))
 
 
-def launches_per_step(B, K):
-    """Kernel launches of one verify round: the split launch (streaming grid,
-    finish, packing) where the library takes it -- with scratch, when the
-    cluster kernel would leave SMs idle or run one CTA per sequence -- else
-    the cluster kernel and the packing launch.  Mirrors the library's rule
-    with the cluster size it would pick (SDV_VERBOSE=1 prints the launch)."""
-    import torch
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    mode = int(os.environ.get("SDV_SPLIT", "-1") or -1)
-    if mode == 0:
-        return 2
-    if mode == 1:
-        return 3
-    cs = max(1, min(16, (2 * sms) // max(B, 1)))
-    return 3 if (cs <= 1 or B * cs < sms) else 2
+def launch_plan(call):
+    """The launch plan the library took for `call` (run once, synchronised):
+    with SDV_VERBOSE=1 it names it on stderr, read here at the descriptor
+    level.  Returns the kernel launches of one verify round: 3 for the split
+    launch (streaming grid, finish, packing), 2 for the cluster kernel and
+    the packing launch."""
+    import tempfile
+    old_env = os.environ.get("SDV_VERBOSE")
+    os.environ["SDV_VERBOSE"] = "1"
+    saved = os.dup(2)
+    with tempfile.TemporaryFile(mode="w+b") as f:
+        os.dup2(f.fileno(), 2)
+        try:
+            call()
+            torch.cuda.synchronize()
+        finally:
+            os.dup2(saved, 2)
+            os.close(saved)
+            if old_env is None:
+                del os.environ["SDV_VERBOSE"]
+            else:
+                os.environ["SDV_VERBOSE"] = old_env
+        f.seek(0)
+        text = f.read().decode(errors="replace")
+    return 3 if "sd_verify split:" in text else 2
 
 
 def algorithmic_bytes(inp: W.Inputs) -> int:
@@ -235,6 +245,7 @@ def run_gpu(args):
                            K + 1, out=rolls[i % n_sets], stream=stream)
 
     with torch.cuda.stream(stream):
+        n_launch = launch_plan(lambda: step(0)) + (2 if pack else 0)
         for i in range(max(args.warmup, 3)):
             step(i)
     torch.cuda.synchronize(dev)
@@ -363,7 +374,7 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": alg, "formula_bytes_per_launch": formula},
         # per step: the cluster kernel and the packing launch, or the streaming
         # grid, the finish and the packing launch (split launch)
-        "gpu_launches": (launches_per_step(B, K) + (2 if pack else 0)) * steps,
+        "gpu_launches": n_launch * steps,
         "clocks": clocks,
         "e2e": e2e,
         "hit_rate": hit_rate, "mean_tau": mean_tau, "status_bits": st,

@@ -68,6 +68,44 @@ def test_host_argument_checks_reject_bad_requests():
                                 None) == sd.SD_ERR_INVALID_ARG
 
 
+def test_next_row_entry_points_refuse_bad_requests():
+    # host-side checks only: every call below is refused before any launch
+    L = sd.lib()
+    P = ctypes.c_void_p
+    fake = P(1 << 20)   # a non-null address never dereferenced: the checks fail first
+    # D3D pack: K, n_keys out of range, null outputs, keys not 8-byte aligned
+    assert L.sd_d3d_pack(2, sd.SD_MAX_K + 1, 3, fake, fake, fake, fake, 0, fake, fake, fake,
+                         None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_d3d_pack(2, 4, -1, fake, fake, fake, fake, 0, fake, fake, fake,
+                         None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_d3d_pack(2, 4, 3, fake, fake, fake, fake, 0, None, fake, fake,
+                         None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_d3d_pack(2, 4, 3, P((1 << 20) + 4), fake, fake, fake, 0, fake, fake, fake,
+                         None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_d3d_pack(0, 4, 3, None, None, None, None, 0, None, None, None, None) == sd.SD_OK
+    # KV rollback: page size, negative sizes, null inputs
+    assert L.sd_kv_rollback(2, 0, 4, 5, fake, fake, fake, fake, fake, fake,
+                            None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_kv_rollback(2, 16, -1, 5, fake, fake, fake, fake, fake, fake,
+                            None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_kv_rollback(2, 16, 4, 5, None, fake, fake, fake, fake, fake,
+                            None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_kv_rollback(2, 16, 4, 5, fake, fake, fake, fake, fake, None,
+                            None) == sd.SD_ERR_INVALID_ARG
+    # n-gram drafter: n range, K range, history length beyond the packed key
+    for n_max, n_min in [(4, 0), (2, 3), (17, 1)]:
+        assert L.sd_ngram_draft(2, 64, 4, n_max, n_min, fake, fake, fake, fake, fake, fake,
+                                None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_ngram_draft(2, 64, sd.SD_MAX_K + 1, 4, 1, fake, fake, fake, fake, fake, fake,
+                            None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_ngram_draft(2, 1 << 26, 4, 4, 1, fake, fake, fake, fake, fake, fake,
+                            None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_ngram_draft(2, 64, 4, 4, 1, None, fake, fake, fake, fake, fake,
+                            None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_ngram_draft(0, 64, 4, 4, 1, None, None, None, None, None, None,
+                            None) == sd.SD_OK
+
+
 def test_python_binding_refuses_cpu_tensors():
     import torch
     t = torch.zeros(2, 3, 10)
