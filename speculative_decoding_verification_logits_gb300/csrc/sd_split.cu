@@ -14,14 +14,16 @@
 // range usually cuts one or two rows.
 // It writes, per row piece, the statistics the combine needs (max,
 // lowest-index argmax, offset exp-sum) and its best key candidates, to a
-// record in caller-provided scratch.  The rows most often needed again (the
-// draft and target rows of position 0) come last in every CTA's range, so
-// the draw finds them in L2.
+// record in caller-provided scratch.  The rows of the first positions, where
+// a rejection is likeliest, come last in the flat order (streamed by the
+// last CTAs of the grid); the draw re-reads its two rows from L2 when a
+// round's logits fit there, from HBM otherwise.
 //
 // The finish is sd_seq_kernel<..., SPLIT = true>: one cluster per sequence,
-// launched as a programmatic dependent of the streaming grid so that its
-// prologue (row table, drafted tokens, their logits, the sequence's place in
-// the flat order) overlaps the end of the stream.  After griddepcontrol.wait
+// launched as a programmatic dependent of the streaming grid; its CTAs take
+// the place of streaming CTAs as those exit (the register file holds no
+// more) and run their prologue (row table, drafted tokens, their logits, the
+// uniforms, the sequence's place in the flat order).  After griddepcontrol.wait
 // it combines the records of each of its rows in the same order in every CTA,
 // merges the key candidates, and continues exactly as the cluster kernel does
 // after its first exchange: accept scan, one inverse-CDF draw over the
