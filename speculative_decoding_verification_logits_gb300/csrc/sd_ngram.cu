@@ -37,6 +37,10 @@ __global__ void __launch_bounds__(NT) sd_ngram_kernel(int L, int K, int n_max, i
   cg::cluster_group cluster = cg::this_cluster();
   const int cs = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
   const int b = blockIdx.x / cs, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // a programmatic dependent of the stream's previous kernel: nothing is read
+  // before it has finished; the next launch may be scheduled at once
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int32_t *h = history + (int64_t)b * L;
   const int n_tok = min(max(__ldg(lengths + b), 0), L);
   __shared__ int32_t pat[kNgramMax];   // pat[s] = h[len-1-s]
@@ -116,13 +120,15 @@ extern "C" sd_status_t sd_ngram_draft(int32_t B, int32_t L, int32_t K, int32_t n
   cfg.gridDim = dim3((unsigned)(B * cs), 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.stream = (cudaStream_t)stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, sd_ngram_kernel<256>, L, K, n_max, n_min,
                                            history, lengths, drafts, count, match_pos, match_n);
   return e == cudaSuccess ? SD_OK : SD_ERR_CUDA;

@@ -23,6 +23,10 @@ __global__ void __launch_bounds__(256) sd_d3d_pack_kernel(
     int B, int K, int n_keys, const int2 *keys, const int32_t *draft_tokens,
     const int32_t *anchor, const int32_t *anchor_pos, int32_t mask, int32_t *tokens,
     int32_t *positions, int32_t *ctx, int64_t total) {
+  // a programmatic dependent of the stream's previous kernel: nothing is read
+  // before it has finished; the next launch may be scheduled at once
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int L = K + 1, nb = 1 + n_keys;
   for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
        x += (int64_t)gridDim.x * blockDim.x) {
@@ -68,8 +72,18 @@ extern "C" sd_status_t sd_d3d_pack(int32_t B, int32_t K, int32_t n_keys, const i
   if (keys && ((uintptr_t)keys % 8) != 0) return SD_ERR_INVALID_ARG;  // read as int2 pairs
   const int64_t total = (int64_t)B * (1 + n_keys) * (K + 1);
   const int64_t blocks = std::min<int64_t>((total + 255) / 256, 8LL * sm_count());
-  sd_d3d_pack_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
-      B, K, n_keys, reinterpret_cast<const int2 *>(keys), draft_tokens, anchor, anchor_pos,
-      mask_token, tokens, positions, ctx, total);
-  return cudaGetLastError() == cudaSuccess ? SD_OK : SD_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, sd_d3d_pack_kernel, (int)B, (int)K, (int)n_keys,
+                                           reinterpret_cast<const int2 *>(keys), draft_tokens,
+                                           anchor, anchor_pos, mask_token, tokens, positions, ctx,
+                                           total);
+  return e == cudaSuccess ? SD_OK : SD_ERR_CUDA;
 }

@@ -19,6 +19,10 @@ __global__ void __launch_bounds__(1024) sd_kv_rollback_kernel(
     int B, int page_size, int max_pages, int appended, const int32_t *kv_len,
     const int32_t *tau, int32_t *block_table, int32_t *new_len, int32_t *freed,
     int32_t *free_offsets) {
+  // a programmatic dependent of the stream's previous kernel: nothing is read
+  // before it has finished; the next launch may be scheduled at once
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ int red[32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int carry = 0;
@@ -86,7 +90,17 @@ extern "C" sd_status_t sd_kv_rollback(int32_t B, int32_t page_size, int32_t max_
                                                                              : SD_ERR_CUDA;
   if (!kv_len || !tau || !new_len || (max_pages > 0 && (!block_table || !freed)))
     return SD_ERR_INVALID_ARG;
-  sd_kv_rollback_kernel<<<1, 1024, 0, s>>>(B, page_size, max_pages, appended, kv_len, tau,
-                                            block_table, new_len, freed, free_offsets);
-  return cudaGetLastError() == cudaSuccess ? SD_OK : SD_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(1024, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, sd_kv_rollback_kernel, (int)B, (int)page_size,
+                                           (int)max_pages, (int)appended, kv_len, tau,
+                                           block_table, new_len, freed, free_offsets);
+  return e == cudaSuccess ? SD_OK : SD_ERR_CUDA;
 }
