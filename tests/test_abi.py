@@ -111,3 +111,18 @@ def test_python_binding_refuses_cpu_tensors():
     t = torch.zeros(2, 3, 10)
     with pytest.raises(ValueError):
         sd.verify(t, t[:, :2], torch.zeros(2, 2, dtype=torch.int32), torch.zeros(2), 1)
+
+
+def test_python_wrappers_of_next_rows_refuse_bad_tensors():
+    # the bindings refuse host tensors before calling the library
+    import torch
+    i32 = torch.zeros(4, 3, 2, dtype=torch.int32)
+    with pytest.raises(ValueError):   # CPU tensors
+        sd.d3d_pack(i32, torch.zeros(4, 5, dtype=torch.int32), torch.zeros(4, dtype=torch.int32),
+                    torch.zeros(4, dtype=torch.int32), 0)
+    with pytest.raises(ValueError):
+        sd.kv_rollback(torch.zeros(4, 8, dtype=torch.int32), torch.zeros(4, dtype=torch.int32),
+                       torch.zeros(4, dtype=torch.int32), 16, 6)
+    with pytest.raises(ValueError):
+        sd.ngram_draft(torch.zeros(4, 64, dtype=torch.int32), torch.zeros(4, dtype=torch.int32),
+                       4, 4, 1)
