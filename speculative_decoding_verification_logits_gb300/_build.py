@@ -17,7 +17,7 @@ HEADERS = sorted(glob.glob(os.path.join(PKG, "csrc", "*.cuh")) +
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
 ]
 
 
@@ -41,11 +41,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not stale():
         return LIB
     tag = f".tmp{os.getpid()}"
-    base = [nvc := nvcc(), *NVCC_FLAGS[:-1], "-I", os.path.join(ROOT, "include")]
+    nvc = nvcc()
+    base = [nvc, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include")]
     objs, procs = [], []
     for src in SOURCES:
         obj = os.path.join(PKG, os.path.basename(src) + tag + ".o")
-        cmd = [*[a for a in base if a != "-shared"], "-c", src, "-o", obj]
+        cmd = [*base, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         objs.append(obj)
