@@ -150,9 +150,9 @@ def workspace_bytes(B: int, K: int) -> int:
 
 
 def workspace(B: int, K: int, device=None, stream=None):
-    """Scratch for sd_verify: None while the library needs none
-    (sd_verify_workspace_size == 0), else a zero-filled buffer cached per
-    (device, stream)."""
+    """Scratch for sd_verify's split launch (sd_verify_workspace_size bytes:
+    one 96-byte record per row piece), cached per (device, stream) so that
+    calls ordered on one stream share it; None for sizes out of range."""
     need = workspace_bytes(B, K)
     if need == 0:
         return None
