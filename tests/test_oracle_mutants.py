@@ -46,9 +46,30 @@ MUTANTS = {
                                     "std::min(std::max(tau[b] + 1, 0), appended)"),
     "rollback_floor_pages": ("const int still = (n_new + page_size - 1) / page_size;",
                              "const int still = n_new / page_size;"),
+    # the guard that decides which sampled decisions are compared exactly
+    "guard_upper_edge_only": ("*near = std::min(C - target, target - prev) < kGuard * S;",
+                              "*near = (C - target) < kGuard * S;"),
+    "guard_lower_edge_only": ("*near = std::min(C - target, target - prev) < kGuard * S;",
+                              "*near = (target - prev) < kGuard * S;"),
+    "guard_absolute_window": ("*near = std::min(C - target, target - prev) < kGuard * S;",
+                              "*near = std::min(C - target, target - prev) < kGuard;"),
+    "guard_total_for_target": ("*near = std::min(C - target, target - prev) < kGuard * S;",
+                               "*near = std::min(C - S, S - prev) < kGuard * S;"),
+    "guard_never_flags_draw": ("*near = std::min(C - target, target - prev) < kGuard * S;",
+                               "*near = false;"),
+    "guard_flags_every_draw": ("*near = std::min(C - target, target - prev) < kGuard * S;",
+                               "*near = true;"),
+    "guard_fallthrough_unflagged": ("*near = true;  // the draw fell",
+                                    "*near = false;  // the draw fell"),
+    "guard_accept_window_wide": ("std::fabs(u - r[(size_t)j]) < kGuard",
+                                 "std::fabs(u - r[(size_t)j]) < 10 * kGuard"),
+    "guard_accept_never": ("if (res.guard_pos < 0 && std::fabs(u - r[(size_t)j]) < kGuard)",
+                           "if (false)"),
 }
 
 FAST_PINS = [
+    pins.test_guard_flags_decisions_near_a_boundary,
+    pins.test_guard_flags_draws_near_a_cdf_edge,
     pins.test_worked_example_greedy,
     pins.test_bonus_when_all_greedy_drafts_match,
     pins.test_greedy_argmax_ties_match_torch_first_occurrence,

@@ -450,11 +450,66 @@ def test_guard_flags_decisions_near_a_boundary(oracle_lib):
     tokens = np.array([0, 1], np.int32)
     base = oracle_lib.verify_row_u(target, draft, tokens, 1.0, [1e-9, 1e-9], [0.5] * 3)
     r0 = base["ratio"][0]
-    if r0 < 1:
-        near = oracle_lib.verify_row_u(target, draft, tokens, 1.0, [r0 + 5e-7, 1e-9], [0.5] * 3)
-        assert near["guard_pos"] == 0
-        far = oracle_lib.verify_row_u(target, draft, tokens, 1.0, [r0 + 5e-5, 1e-9], [0.5] * 3)
-        assert far["guard_pos"] == -1 or far["guard_pos"] > 0
+    assert r0 < 1     # the seed gives a rejectable first draft
+    for du, flagged in ((5e-7, True), (-5e-7, True), (2e-6, False), (-2e-6, False),
+                        (5e-5, False), (-5e-5, False)):
+        r = oracle_lib.verify_row_u(target, draft, tokens, 1.0, [r0 + du, 1e-9], [0.5] * 3)
+        # u - r within 1e-6 flags position 0; further away nothing is flagged
+        # (the draw at u = 0.5 is far from every CDF edge of these rows)
+        assert r["guard_pos"] == (0 if flagged else -1), (du, r["guard_pos"])
+
+
+def _cdf_case():
+    """Sequence of one draft whose first position is rejected and whose
+    residual max(0, p - q) has three equal bins: target row 0 uniform over
+    four tokens, draft row 0 twice as likely on token 0.  Returns the inputs
+    and the residual's unnormalised weights computed here in float64 from
+    the float32 logits (softmax written out with numpy)."""
+    target = np.zeros((2, 4), np.float32)
+    draft = np.zeros((1, 4), np.float32)
+    draft[0, 0] = np.float32(np.log(2.0))
+    tokens = np.array([0], np.int32)
+    p = np.exp(target[0].astype(np.float64))
+    p /= p.sum()
+    q = np.exp(draft[0].astype(np.float64))
+    q /= q.sum()
+    w = np.maximum(0.0, p - q)
+    return target, draft, tokens, w
+
+
+def test_guard_flags_draws_near_a_cdf_edge(oracle_lib):
+    # The inverse-CDF draw picks the smallest i with C_i > u S; the guard
+    # flags it when u S lies within 1e-6 S of either edge of bin i, and when
+    # rounding leaves u S at or past the total.  Residual weights here:
+    # (0, w, w, w) with S = 3w ~ 0.15, edges at S/3 and 2S/3.
+    target, draft, tokens, w = _cdf_case()
+    S = w.sum()
+    C = np.cumsum(w)
+    assert w[0] == 0 and np.allclose(w[1:], w[1]) and 0.14 < S < 0.16
+    # accept uniform 1 > p/q(d_0) = 0.25 / 0.4: position 0 is rejected
+    for edge in (1, 2):               # bins 1 | 2 and 2 | 3
+        for d, flagged in ((5e-7, True), (-5e-7, True), (3e-6, False), (-3e-6, False),
+                           (5e-5, False), (-5e-5, False)):
+            # u S placed d S away from the edge C[edge] (d in units of S)
+            u = C[edge] / S + d
+            r = oracle_lib.verify_row_u(target, draft, tokens, 1.0, [1.0], [u, 0.5])
+            assert r["n_acc"] == 0 and r["tau"] == 1
+            assert r["out_tokens"][0] == (edge + 1 if d > 0 else edge), (edge, d)
+            assert r["guard_pos"] == (0 if flagged else -1), (edge, d, r["guard_pos"])
+    # u S exactly on the total: no bin passes it, the last weighted token is
+    # taken and the draw is flagged
+    r = oracle_lib.verify_row_u(target, draft, tokens, 1.0, [1.0], [1.0, 0.5])
+    assert r["out_tokens"][0] == 3 and r["guard_pos"] == 0
+    # the window is relative to S: 5e-7 of an absolute unit is 3.3e-6 S, far
+    r = oracle_lib.verify_row_u(target, draft, tokens, 1.0, [1.0], [C[1] / S + 5e-7 / S, 0.5])
+    assert r["out_tokens"][0] == 2 and r["guard_pos"] == -1
+    # bonus draw (all accepted): over p of the last row, four equal bins of
+    # 1/4; u = 1/2 + 5e-7 is flagged, u = 1/2 + 5e-5 is not
+    same = target[:1].copy()
+    for du, flagged in ((5e-7, True), (5e-5, False)):
+        r = oracle_lib.verify_row_u(target, same, tokens, 1.0, [1e-9], [0.5, 0.5 + du])
+        assert r["n_acc"] == 1 and r["out_tokens"][1] == 2
+        assert r["guard_pos"] == (1 if flagged else -1)
 
 
 # ------------------------------------------------------------------- Philox ----
