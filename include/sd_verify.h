@@ -60,11 +60,13 @@ typedef enum {
 } sd_status_t;
 
 /* Device-side status bits, OR-ed into the optional *status word.  Kernels
- * never trap: a data error marks the affected row invalid (tau = 0, all
- * out_tokens = -1, num_accepted = 0, hit = 0) and sets a bit here. */
+ * never trap and never wait on one another: a data error marks the affected
+ * row invalid (tau = 0, all out_tokens = -1, num_accepted = 0, hit = 0) and
+ * sets a bit here. */
 #define SD_STATUS_BAD_TOKEN 0x1u /* a draft token outside [0, V)              */
 #define SD_STATUS_BAD_TEMP 0x2u  /* a temperature < 0, NaN or infinite        */
-#define SD_STATUS_TIMEOUT 0x8u   /* a bounded wait for a bulk copy gave up    */
+#define SD_STATUS_NONFINITE 0x4u /* with SD_FLAG_CHECK_FINITE: a row the call
+                                    read holds NaN or +inf, or only -inf      */
 
 typedef enum { SD_F32 = 0, SD_BF16 = 1 } sd_dtype_t;
 
@@ -78,6 +80,16 @@ typedef enum { SD_F32 = 0, SD_BF16 = 1 } sd_dtype_t;
                                 the draft rows read by this pass (keys_out)  */
 #define SD_FLAG_COMPACT 0x2u /* also pack the emitted tokens of all rows
                                 (offsets, packed), as sd_compact does         */
+#define SD_FLAG_CHECK_FINITE 0x4u /* check every logit row the call reads for
+                                a sequence (its K+1 target rows; draft row j
+                                when the sequence is sampled or keys are built
+                                at j; the bonus draft row when keys are built
+                                at K): a NaN or +inf, or a row of only -inf,
+                                makes the sequence invalid and sets
+                                SD_STATUS_NONFINITE (single -inf values are
+                                valid logits of weight 0).  Without the flag
+                                such rows give unspecified tokens (no fault).
+                                The keys of a flagged sequence are unspecified. */
 
 /*
  * Arguments of sd_verify.  Logits are contiguous, row-major, last dimension V,
@@ -144,11 +156,19 @@ typedef struct sd_verify_args {
 size_t sd_verify_workspace_size(int32_t B, int32_t K);
 
 /*
- * The verify step: per-row temperature softmax of the K+1 target and K draft
- * rows, the left-to-right accept/reject scan (argmax match for T == 0), the
- * correction token from the residual at the first rejection or the bonus
- * token from target row K, tau, the optional hit test, and optionally the
- * outcome-prediction keys and the compaction of all rows' tokens.
+ * The verify step ("What is speculative decoding" explainer (lotook.com),
+ * the four-stage loop: stages 2-4, score the K drafted positions in one
+ * target pass, accept left to right, resample the first rejection from a
+ * residual of both distributions or take the bonus token; "LLMの生成を5倍速く
+ * する「D3D」を図で読む" (animemo.app), 検証のしくみ③ and 検証のまとめ: the
+ * greedy match, tau = accepted drafts + 1; "Speculative Speculative
+ * Decoding" blog (jiwasawa.github.io), Saguaro 1. Outcome Prediction: the
+ * keys and the hit test): per-row temperature softmax of the K+1 target and
+ * K draft rows, the left-to-right accept/reject scan (argmax match for
+ * T == 0), the correction token from the residual at the first rejection or
+ * the bonus token from target row K, tau, the optional hit test, and
+ * optionally the outcome-prediction keys and the compaction of all rows'
+ * tokens.
  * Each logit row is streamed from memory once; the target and draft rows at
  * the first rejection (or target row K) are read a second time for the
  * draw, mostly from L2.  Two ways to run: a split launch (a streaming
@@ -192,7 +212,13 @@ sd_status_t sd_verify(const sd_verify_args *args, void *stream);
 sd_status_t sd_verify_noalloc(const sd_verify_args *args, void *stream);
 
 /*
- * Outcome prediction: for each row b and position k < K, the fanout[k]
+ * Outcome prediction ("Speculative Speculative Decoding" blog
+ * (jiwasawa.github.io), Saguaro 1. Outcome Prediction: the likely verify
+ * outcomes are the accept lengths paired with the draft's top tokens, with a
+ * fan-out per position; "LLMの生成を5倍速くする「D3D」を図で読む"
+ * (animemo.app), 答え:ありうる結果すべてに、先回りして下書きする: the
+ * drafter's own next candidates at each rejection position plus one
+ * all-accepted key): for each row b and position k < K, the fanout[k]
  * tokens with the highest draft logit at k other than the drafted token
  * d_k (ties to the lowest index, -inf logits never chosen), keyed (k, token):
  * the corrections a rejection at k could produce.  For k == K the fanout[K]
@@ -269,7 +295,11 @@ sd_status_t sd_kv_rollback(int32_t B, int32_t page_size, int32_t max_pages, int3
                            void *stream);
 
 /*
- * Compaction: offsets[b] = sum of tau over rows before b (B+1 entries) and
+ * Compaction ("What is speculative decoding" explainer (lotook.com), the
+ * four-stage loop: the accepted drafts and the resampled or bonus token are
+ * appended to the text; "LLMの生成を5倍速くする「D3D」を図で読む"
+ * (animemo.app), 検証のまとめ: tau tokens settle per round): offsets[b] =
+ * sum of tau over rows before b (B+1 entries) and
  * packed[offsets[b] + i] = out_tokens[b][i] for i < tau[b].  packed needs
  * room for B*(K+1) tokens.  Entries of tau outside [0, K+1] set
  * SD_STATUS_BAD_TOKEN in *status (optional) and count as 0.

@@ -76,6 +76,9 @@ def _bind(L):
     L.oracle_verify.argtypes = [i32, i32, i32, i32, P, P, P, P, u64, i64, P, i32,
                                 P, P, P, P, P, P, P, P, P, P, P]
     L.oracle_verify.restype = i32
+    L.oracle_verify_checked.argtypes = [i32, i32, i32, i32, P, P, P, P, u64, i64, P, i32,
+                                        P, P, P, P, P, P, P, P, P, P, P, i32, P, P, P]
+    L.oracle_verify_checked.restype = i32
     L.oracle_outcome_predict.argtypes = [i32, i32, i32, i32, P, P, P, P, P]
     L.oracle_outcome_predict.restype = i32
     L.oracle_compact.argtypes = [i32, i32, P, P, P, P]
@@ -146,10 +149,13 @@ def verify_row_u(target, draft, tokens, T, u_accept, u_sample):
 
 
 def verify(target, draft, tokens, temperature, seed: int, row_base: int = 0, keys=None,
-           stats: bool = False):
+           stats: bool = False, check_finite: bool = False, fanout=None, draft_bonus=None):
     """Batch verify with Philox uniforms.  target [B][K+1][V], draft
     [B][K][V], tokens [B][K], temperature [B].  keys: optional
-    [B][n_keys][2] int32.  Returns a dict of numpy arrays."""
+    [B][n_keys][2] int32.  check_finite: also check the rows the step reads
+    (draft rows of positions with fanout > 0 and, with fanout[K] > 0, the
+    draft_bonus rows count as read); 'nonfinite' [B] marks the sequences it
+    made invalid.  Returns a dict of numpy arrays."""
     target, dt = _logits(target)
     B, K1, V = target.shape
     K = K1 - 1
@@ -176,11 +182,20 @@ def verify(target, draft, tokens, temperature, seed: int, row_base: int = 0, key
                  q_tok=np.full((B, K), np.nan), argmax=np.zeros((B, K + 1), np.int32),
                  Zt=np.full((B, K + 1), np.nan), Zd=np.full((B, K), np.nan))
     g = r.get
-    invalid = lib().oracle_verify(
+    fan = None
+    if fanout is not None:
+        fan = np.ascontiguousarray(fanout, dtype=np.int32).reshape(K + 1)
+    bonus = None
+    if draft_bonus is not None:
+        bonus, dt3 = _logits(draft_bonus)
+        assert dt3 == dt and bonus.shape == (B, V)
+    r["nonfinite"] = np.zeros(B, np.uint8)
+    invalid = lib().oracle_verify_checked(
         B, K, V, dt, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(temps), seed, row_base,
         _ptr(keys), n_keys, _ptr(r["num_accepted"]), _ptr(r["out_tokens"]), _ptr(r["tau"]),
         _ptr(r["hit"]), _ptr(r["guard_pos"]), _ptr(g("ratio")), _ptr(g("p_tok")),
-        _ptr(g("q_tok")), _ptr(g("argmax")), _ptr(g("Zt")), _ptr(g("Zd")))
+        _ptr(g("q_tok")), _ptr(g("argmax")), _ptr(g("Zt")), _ptr(g("Zd")),
+        1 if check_finite else 0, _ptr(fan), _ptr(bonus), _ptr(r["nonfinite"]))
     r["invalid_rows"] = int(invalid)
     return r
 

@@ -164,7 +164,32 @@ struct RowResult {
   int n_acc = 0, tau = 0, token = -1;
   int guard_pos = -1;       // first position with a near-boundary decision
   bool valid = true;
+  bool nonfinite = false;   // invalid because a row it reads is not finite
   bool hit = false;
+};
+
+// A logit row fails the finiteness check when it holds a NaN or +inf, or
+// when every value is -inf (no distribution can be formed from it); single
+// -inf values are allowed and carry zero weight.
+bool row_not_finite(const void *base, int dtype, int64_t row, int V) {
+  bool any_finite = false;
+  for (int i = 0; i < V; ++i) {
+    const double v = widen(base, dtype, row * (int64_t)V + i);
+    if (std::isnan(v) || v == std::numeric_limits<double>::infinity()) return true;
+    if (v != -std::numeric_limits<double>::infinity()) any_finite = true;
+  }
+  return !any_finite;
+}
+
+// Optional finiteness check of the rows a verify call reads for one
+// sequence: the K+1 target rows; draft row j when the sequence is sampled or
+// keys are built at position j (keys_at[j] != 0); the bonus draft row when
+// keys are built at position K.
+struct FiniteCheck {
+  bool on = false;
+  const int32_t *keys_at = nullptr;  // [K+1] or null: no keys
+  const void *bonus = nullptr;       // bonus draft rows [B][V] or null
+  int64_t bonus_row = 0;
 };
 
 // One sequence of the verify step with the uniforms given explicitly.
@@ -177,7 +202,8 @@ RowResult verify_one(int K, int V, int dtype, const void *target, int64_t trow0,
                      const void *draft, int64_t drow0, const int32_t *tokens, double T,
                      const double *u_accept, const double *u_sample,
                      double *ratio, double *p_tok, double *q_tok, int32_t *argmax_out,
-                     double *Zt_out, double *Zd_out, int32_t *out_tokens) {
+                     double *Zt_out, double *Zd_out, int32_t *out_tokens,
+                     const FiniteCheck &fc = FiniteCheck()) {
   RowResult res;
   for (int j = 0; j <= K; ++j) out_tokens[j] = -1;
   bool tokens_ok = true;
@@ -189,6 +215,20 @@ RowResult verify_one(int K, int V, int dtype, const void *target, int64_t trow0,
     res.tau = 0;
     res.n_acc = 0;
     return res;
+  }
+  if (fc.on) {
+    bool bad = false;
+    for (int j = 0; j <= K && !bad; ++j) bad = row_not_finite(target, dtype, trow0 + j, V);
+    for (int j = 0; j < K && !bad; ++j)
+      if (T > 0.0 || (fc.keys_at && fc.keys_at[j] > 0))
+        bad = row_not_finite(draft, dtype, drow0 + j, V);
+    if (!bad && fc.bonus && fc.keys_at && fc.keys_at[K] > 0)
+      bad = row_not_finite(fc.bonus, dtype, fc.bonus_row, V);
+    if (bad) {
+      res.valid = false;
+      res.nonfinite = true;
+      return res;
+    }
   }
 
   // target rows j = 0..K: argmax, and softmax for T > 0.
@@ -302,12 +342,18 @@ int oracle_verify_row_u(int K, int V, int dtype, const void *target, const void 
 // hit (optional): [B].  Per-position optional outputs as in verify_one,
 // laid out [B][K] (ratio, p_tok, q_tok, Zd) and [B][K+1] (argmax, Zt).
 // Returns the number of invalid rows.
-int oracle_verify(int B, int K, int V, int dtype, const void *target, const void *draft,
-                  const int32_t *tokens, const float *temperature, uint64_t seed,
-                  int64_t row_base, const int32_t *keys, int n_keys, int32_t *num_accepted,
-                  int32_t *out_tokens, int32_t *tau, uint8_t *hit, int32_t *guard_pos,
-                  double *ratio, double *p_tok, double *q_tok, int32_t *argmax_out,
-                  double *Zt, double *Zd) {
+// check_finite (optional): with it, rows the call reads are checked as
+// FiniteCheck describes; fanout [K+1] (or null) marks the positions whose
+// draft rows are read for keys, draft_bonus [B][V] (or null) the bonus draft
+// rows; nonfinite [B] (optional) receives 1 for each sequence the check
+// made invalid.
+int oracle_verify_checked(int B, int K, int V, int dtype, const void *target, const void *draft,
+                          const int32_t *tokens, const float *temperature, uint64_t seed,
+                          int64_t row_base, const int32_t *keys, int n_keys,
+                          int32_t *num_accepted, int32_t *out_tokens, int32_t *tau, uint8_t *hit,
+                          int32_t *guard_pos, double *ratio, double *p_tok, double *q_tok,
+                          int32_t *argmax_out, double *Zt, double *Zd, int check_finite,
+                          const int32_t *fanout, const void *draft_bonus, uint8_t *nonfinite) {
   int invalid = 0;
   std::vector<double> ua((size_t)std::max(K, 1)), us((size_t)K + 1);
   for (int b = 0; b < B; ++b) {
@@ -315,13 +361,19 @@ int oracle_verify(int B, int K, int V, int dtype, const void *target, const void
     for (int j = 0; j < K; ++j) ua[(size_t)j] = uniform_from_philox(seed, row, (uint32_t)j, 0u);
     for (int j = 0; j <= K; ++j) us[(size_t)j] = uniform_from_philox(seed, row, (uint32_t)j, 1u);
     const size_t pk = (size_t)b * (size_t)K, pk1 = (size_t)b * (size_t)(K + 1);
+    FiniteCheck fc;
+    fc.on = check_finite != 0;
+    fc.keys_at = fanout;
+    fc.bonus = draft_bonus;
+    fc.bonus_row = b;
     RowResult r = verify_one(
         K, V, dtype, target, (int64_t)b * (K + 1), draft, (int64_t)b * K, tokens + pk,
         (double)temperature[b], ua.data(), us.data(), ratio ? ratio + pk : nullptr,
         p_tok ? p_tok + pk : nullptr, q_tok ? q_tok + pk : nullptr,
         argmax_out ? argmax_out + pk1 : nullptr, Zt ? Zt + pk1 : nullptr, Zd ? Zd + pk : nullptr,
-        out_tokens + pk1);
+        out_tokens + pk1, fc);
     if (!r.valid) ++invalid;
+    if (nonfinite) nonfinite[b] = r.nonfinite ? 1 : 0;
     num_accepted[b] = r.n_acc;
     tau[b] = r.tau;
     if (guard_pos) guard_pos[b] = r.guard_pos;
@@ -336,6 +388,17 @@ int oracle_verify(int B, int K, int V, int dtype, const void *target, const void
     }
   }
   return invalid;
+}
+
+int oracle_verify(int B, int K, int V, int dtype, const void *target, const void *draft,
+                  const int32_t *tokens, const float *temperature, uint64_t seed,
+                  int64_t row_base, const int32_t *keys, int n_keys, int32_t *num_accepted,
+                  int32_t *out_tokens, int32_t *tau, uint8_t *hit, int32_t *guard_pos,
+                  double *ratio, double *p_tok, double *q_tok, int32_t *argmax_out,
+                  double *Zt, double *Zd) {
+  return oracle_verify_checked(B, K, V, dtype, target, draft, tokens, temperature, seed, row_base,
+                               keys, n_keys, num_accepted, out_tokens, tau, hit, guard_pos, ratio,
+                               p_tok, q_tok, argmax_out, Zt, Zd, 0, nullptr, nullptr, nullptr);
 }
 
 // Outcome prediction ([SSD] Saguaro outcome prediction; [D3D] 先回りして

@@ -25,9 +25,9 @@ import torch
 from . import _build
 
 SD_OK, SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED, SD_ERR_CUDA = 0, 1, 2, 3
-SD_STATUS_BAD_TOKEN, SD_STATUS_BAD_TEMP, SD_STATUS_TIMEOUT = 0x1, 0x2, 0x8
+SD_STATUS_BAD_TOKEN, SD_STATUS_BAD_TEMP, SD_STATUS_NONFINITE = 0x1, 0x2, 0x4
 SD_F32, SD_BF16 = 0, 1
-SD_FLAG_PREDICT, SD_FLAG_COMPACT = 0x1, 0x2
+SD_FLAG_PREDICT, SD_FLAG_COMPACT, SD_FLAG_CHECK_FINITE = 0x1, 0x2, 0x4
 SD_MAX_K, SD_MAX_V, SD_MAX_FANOUT = 32, 262144, 8
 
 _P = ctypes.c_void_p
@@ -205,15 +205,17 @@ def alloc_outputs(B, K, device, *, hit=False, compact=False, stats=False, n_keys
 
 def verify(target, draft, tokens, temperature, seed: int, *, row_base: int = 0,
            cache_keys=None, fanout=None, draft_bonus=None, compact: bool = False,
-           stats: bool = False, out: VerifyResult | None = None, ws=None,
-           stream=None) -> VerifyResult:
+           stats: bool = False, check_finite: bool = False, out: VerifyResult | None = None,
+           ws=None, stream=None) -> VerifyResult:
     """Run sd_verify on the current (or given) stream.
 
     target [B][K+1][V], draft [B][K][V] (float32 or bfloat16, CUDA,
     contiguous), tokens [B][K] int32, temperature [B] float32.  cache_keys:
     [B][n_keys][2] int32 keys to test the outcome against.  fanout ([K+1]
     ints) asks for the outcome-prediction keys to be built in the same pass
-    (draft_bonus [B][V] optional).  compact=True also packs the tokens."""
+    (draft_bonus [B][V] optional).  compact=True also packs the tokens.
+    check_finite=True sets SD_FLAG_CHECK_FINITE: a sequence whose rows hold
+    NaN or +inf (or only -inf) comes back invalid with SD_STATUS_NONFINITE."""
     _need(target, "target")
     dev = target.device
     B, K1, V = target.shape
@@ -241,6 +243,8 @@ def verify(target, draft, tokens, temperature, seed: int, *, row_base: int = 0,
             raise ValueError("cache_keys must be [B][n_keys][2]")
     if compact:
         flags |= SD_FLAG_COMPACT
+    if check_finite:
+        flags |= SD_FLAG_CHECK_FINITE
     r = out or alloc_outputs(B, K, dev, hit=cache_keys is not None or n_keys > 0,
                              compact=compact, stats=stats, n_keys=n_keys)
     w = ws if ws is not None else workspace(B, K, dev, stream)

@@ -79,6 +79,9 @@ struct Params {
   int32_t gstream;         // CTAs of the streaming grid
   int8_t grp_x[SD_MAX_K + 1];
   size_t ws_bytes;         // bytes at ws
+  int32_t chk;             // SD_FLAG_CHECK_FINITE: rows read are checked
+  int32_t kf;              // key candidates per piece record (split launch)
+  int32_t pw;              // split finish: draw iterations per warp (mass rows)
 };
 
 // ------------------------------------------------------------------ Philox --
@@ -329,6 +332,14 @@ struct Elt<float> {
   static __device__ __forceinline__ float load_global(const uint8_t *p) {
     return __ldg(reinterpret_cast<const float *>(p));
   }
+  // max of the 4 values where a NaN wins: NaN or +inf anywhere shows here
+  static __device__ __forceinline__ float vmax_nan(const uint4 &v) {
+    float a, b, c;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(a) : "f"(__uint_as_float(v.x)), "f"(__uint_as_float(v.y)));
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(b) : "f"(__uint_as_float(v.z)), "f"(__uint_as_float(v.w)));
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(c) : "f"(a), "f"(b));
+    return c;
+  }
 };
 template <>
 struct Elt<__nv_bfloat16> {
@@ -357,6 +368,17 @@ struct Elt<__nv_bfloat16> {
   }
   static __device__ __forceinline__ float load_global(const uint8_t *p) {
     return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(p)) << 16);
+  }
+  // max of the 8 values where a NaN wins (packed bf16x2 maxima), widened
+  static __device__ __forceinline__ float vmax_nan(const uint4 &v) {
+    uint32_t a, c, m;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x), "r"(v.y));
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(v.z), "r"(v.w));
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(c));
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(__uint_as_float(m << 16)),
+        "f"(__uint_as_float(m & 0xffff0000u)));
+    return r;
   }
 };
 
@@ -449,25 +471,6 @@ __device__ __forceinline__ uint4 load_vec_direct(const RowInfo &R, int q, int v0
   return load_vec_slow<E>(R, q, v0, v1);
 }
 
-// One 16-byte vector q (< qend) of row R into this thread's k-th slot of a
-// ring slot (`slot`: shared address of this thread's vector 0 there); the
-// ragged ends are read when consumed.
-template <int NT>
-__device__ __forceinline__ void issue_vec(const RowInfo &R, int q, int qend, uint32_t slot, int k) {
-  if (q < qend && q >= R.qlo && q < R.qhi) cp_async16(slot + k * NT * 16, R.gbase + 16 * q);
-}
-template <typename E, int NT>
-__device__ __forceinline__ uint4 fetch_vec(const RowInfo &R, int q, int qend, const uint8_t *slot,
-                                           int k, int v0, int v1) {
-  if (q < qend && q >= R.qlo && q < R.qhi)
-    return *reinterpret_cast<const uint4 *>(slot + k * NT * 16);
-  if (q >= qend || q >= R.nvec) {
-    const uint32_t w = Elt<E>::kNegInfWord;
-    return make_uint4(w, w, w, w);
-  }
-  return load_vec_slow<E>(R, q, v0, v1);
-}
-
 // -------------------------------------------------------- shared memory --
 // Per-warp statistics of one row: max, sum z of 2^(l s + c), offset c,
 // lowest index of the max.
@@ -544,8 +547,7 @@ struct Static {
   int red_i[kMaxWarps];
   float u_acc[SD_MAX_K];      // accept uniforms u(b, j, 0)
   float u_draw[SD_MAX_K + 1]; // draw uniforms u(b, m, 1) for every m
-  int rflat[kMaxRows];        // split finish: the row's index in the flat stream
-  int pc0[kMaxRows], pc1[kMaxRows];  //   and the streaming CTAs that covered it
+  int fvalid;                 // 0: a row read failed the finiteness check
   int tok;
 };
 
@@ -571,32 +573,6 @@ __device__ __forceinline__ void issuer_row(Issuer &I, const Static &S, int nrows
   }
 }
 
-// Copy one step (kU vectors per thread) into the next ring slot.
-template <int NT>
-__device__ __forceinline__ void issue_step(Issuer &I, const Static &S, int nrows, uint32_t ring_t) {
-  constexpr int kStepVec = NT * kU;
-  constexpr uint32_t kSlot = kU * NT * 16;
-  if (I.row < nrows) {
-    if (I.step >= I.sf0 && I.step < I.sf1) {
-#pragma unroll
-      for (int k = 0; k < kU; ++k) cp_async16(I.slot + k * NT * 16, I.ptr + k * NT * 16);
-    } else {
-#pragma unroll
-      for (int k = 0; k < kU; ++k) {
-        const int q = I.step * kStepVec + k * NT + (int)threadIdx.x;
-        if (q >= I.qlo && q < I.qhi) cp_async16(I.slot + k * NT * 16, I.ptr + k * NT * 16);
-      }
-    }
-    I.ptr += kStepVec * 16;
-    if (++I.step == I.nsteps) {
-      ++I.row;
-      issuer_row<NT>(I, S, nrows);
-    }
-  }
-  cp_commit();
-  I.slot += kSlot;
-  if (I.slot == ring_t + kDepth * kSlot) I.slot = ring_t;
-}
 // --------------------------------------------------------- finalization --
 // Exclusive scan of tau and packing of out_tokens, one CTA.  `cg_loads`
 // reads values written by other CTAs of the same grid through L2.
@@ -763,133 +739,174 @@ __device__ __forceinline__ float step_max(const uint4 (&v)[kU], int kv, float *v
   return g;
 }
 
-// One step of one row: kU vectors per thread (the first kv of them unless
-// FULL).  EXP: offset exp-sum; ARG: running max and the first vector that
-// reached it; KEYS: the thread's best KF vectors by masked max.
-template <typename E, int KF, int NT, bool EXP, bool ARG, bool KEYS, bool FULL>
-__device__ __forceinline__ void step_body(RowAcc<KF> &A, const uint4 (&v)[kU], int kv, int step,
-                                          int qd_step, int qd, int excl, int v0, int hp, float s,
-                                          uint64_t s2) {
-  constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec;
-  const int qbase = step * (NT * kU) + threadIdx.x;
-  if (ARG || KEYS) {
-    float vm[kU];
-    const float gmax = step_max<E, FULL>(v, kv, vm);
-    if (gmax > A.m) {
-      A.m = gmax;
-      if (ARG) {
-        int kb = kU - 1;
+// What a row's stream computes (flags, uniform per row).
+enum : int { kFExp = 1, kFArg = 2, kFKeys = 4, kFChk = 8 };
+
+__device__ __forceinline__ int row_flags(int type, bool chk) {
+  int f = chk ? kFChk : 0;
+  if (type == kRowE || type == kRowEA || type == kRowEK) f |= kFExp;
+  if (type == kRowEA || type == kRowA) f |= kFArg;
+  if (type == kRowK || type == kRowEK) f |= kFKeys;
+  return f;
+}
+
+__device__ __forceinline__ void st_shared16(uint32_t a, const uint4 &w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w.x), "r"(w.y), "r"(w.z),
+               "r"(w.w)
+               : "memory");
+}
+
+// Copy one step (kU vectors per thread) into the next ring slot.  Vectors
+// wholly inside the piece are copied with cp.async; the ragged ends are
+// assembled from element loads and past the piece the slot gets -inf, both
+// stored by this thread, which alone reads its slots.
+template <typename E, int NT>
+__device__ __forceinline__ void issue_fill(Issuer &I, const Static &S, int nrows, uint32_t ring_t) {
+  constexpr int kStepVec = NT * kU;
+  constexpr uint32_t kSlot = kU * NT * 16;
+  if (I.row < nrows) {
+    if (I.step >= I.sf0 && I.step < I.sf1) {
 #pragma unroll
-        for (int k = kU - 1; k >= 0; --k)
-          if (vm[k] == gmax) kb = k;
-#pragma unroll
-        for (int k = 0; k < kU; ++k)
-          if (k == kb) {
-            A.bv = v[k];
-            A.bq = qbase + k * NT;
-          }
-      }
-      if (EXP) {
-        const float cn = -(gmax * s);
-        if (A.c == INFINITY) {
-          A.c = cn;
-        } else if (A.c - cn > kRebase) {  // the max rose by more than kRebase (log2)
-          const float f = ex2(cn - A.c);
-          A.z *= f;
-          A.zc *= f;
-          A.c = cn;
+      for (int k = 0; k < kU; ++k) cp_async16(I.slot + k * NT * 16, I.ptr + k * NT * 16);
+    } else {
+      const RowInfo &R = S.rows[I.row];
+#pragma unroll 1
+      for (int k = 0; k < kU; ++k) {
+        const int q = I.step * kStepVec + k * NT + (int)threadIdx.x;
+        if (q >= I.qlo && q < I.qhi) {
+          cp_async16(I.slot + k * NT * 16, I.ptr + k * NT * 16);
+        } else {
+          const uint32_t ni = Elt<E>::kNegInfWord;
+          const uint4 w = q < R.nvec ? load_vec_slow<E>(R, q, R.v0, R.v1) : make_uint4(ni, ni, ni, ni);
+          st_shared16(I.slot + k * NT * 16, w);
         }
       }
     }
-    if (EXP && A.c != INFINITY) kahan_add(A.z, A.zc, exp_sum<E, FULL>(v, kv, s2, pk2(A.c, A.c)));
-    if (KEYS) {
-      // The top-KF elements of a set lie in its top-KF vectors ranked by
-      // (max, index): every vector holding one of them has a max at least the
-      // KF-th value, and at most KF vectors reach it.  Track those vectors.
-      if (step == qd_step) {
+    I.ptr += kStepVec * 16;
+    if (++I.step == I.nsteps) {
+      ++I.row;
+      issuer_row<NT>(I, S, nrows);
+    }
+  }
+  cp_commit();
+  I.slot += kSlot;
+  if (I.slot == ring_t + kDepth * kSlot) I.slot = ring_t;
+}
+
+// One step of one row: kU whole vectors per thread (-inf padded).  kFExp:
+// offset exp-sum; kFArg: running max and the first vector that reached it;
+// kFKeys: the thread's best KF vectors by masked max; kFChk: NaN or +inf
+// seen.  The running max is kept for every row (the finiteness check and
+// the offset use it).
+template <typename E, int KF, int NT>
+__device__ __forceinline__ void step_gen(RowAcc<KF> &A, const uint4 (&v)[kU], int step, int fl,
+                                         int qd_step, int qd, int excl, int v0, int hp, float s,
+                                         uint64_t s2, bool &bad) {
+  constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec;
+  const int qbase = step * (NT * kU) + threadIdx.x;
+  float vm[kU];
+  const float gmax = step_max<E, true>(v, kU, vm);
+  if (fl & kFChk) {
 #pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int q = qbase + k * NT;
-          if (q == qd) {  // the vector holding the excluded token: its max without it
-            float f[N];
-            Elt<E>::unpack(v[k], f);
-            float mm = -INFINITY;
+    for (int k = 0; k < kU; ++k) bad |= !(Elt<E>::vmax_nan(v[k]) < INFINITY);
+  }
+  if (gmax > A.m) {
+    A.m = gmax;
+    if (fl & kFArg) {
+      int kb = kU - 1;
 #pragma unroll
-            for (int i = 0; i < N; ++i)
-              if (elem_index(v0, hp, q, i, sz) != excl) mm = fmaxf(mm, f[i]);
-            vm[k] = mm;
-          }
+      for (int k = kU - 1; k >= 0; --k)
+        if (vm[k] == gmax) kb = k;
+#pragma unroll
+      for (int k = 0; k < kU; ++k)
+        if (k == kb) {
+          A.bv = v[k];
+          A.bq = qbase + k * NT;
+        }
+    }
+    if (fl & kFExp) {
+      const float cn = -(gmax * s);
+      if (A.c == INFINITY) {
+        A.c = cn;
+      } else if (A.c - cn > kRebase) {  // the max rose by more than kRebase (log2)
+        const float f = ex2(cn - A.c);
+        A.z *= f;
+        A.zc *= f;
+        A.c = cn;
+      }
+    }
+  }
+  if ((fl & kFExp) && A.c != INFINITY)
+    kahan_add(A.z, A.zc, exp_sum<E, true>(v, kU, s2, pk2(A.c, A.c)));
+  if constexpr (KF > 0) {
+  if (fl & kFKeys) {
+    // The top-KF elements of a set lie in its top-KF vectors ranked by
+    // (max, index): every vector holding one of them has a max at least the
+    // KF-th value, and at most KF vectors reach it.  Track those vectors.
+    if (step == qd_step) {
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
+        const int q = qbase + k * NT;
+        if (q == qd) {  // the vector holding the excluded token: its max without it
+          float f[N];
+          Elt<E>::unpack(v[k], f);
+          float mm = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < N; ++i)
+            if (elem_index(v0, hp, q, i, sz) != excl) mm = fmaxf(mm, f[i]);
+          vm[k] = mm;
         }
       }
-      if (step == 0) {  // the warp's KF-th best first vector bounds the rest from below
-        const int lane = threadIdx.x & 31;
-        float x = vm[0], th = -INFINITY;
+    }
+    if (step == 0) {  // the warp's KF-th best first vector bounds the rest from below
+      const int lane = threadIdx.x & 31;
+      float x = vm[0], th = -INFINITY;
 #pragma unroll
-        for (int r = 0; r < KF; ++r) {
-          th = rmax_f(x);
-          const unsigned w = ballot(x == th);
-          if (lane == __ffs(w) - 1) x = -INFINITY;
-        }
-        A.theta = th;
+      for (int r = 0; r < KF; ++r) {
+        th = rmax_f(x);
+        const unsigned w = ballot(x == th);
+        if (lane == __ffs(w) - 1) x = -INFINITY;
       }
-      const float vbest = fmaxf(fmaxf(vm[0], vm[1]), fmaxf(vm[2], vm[3]));
-      if (vbest > A.kv[KF - 1] && vbest >= A.theta) {  // rare once the row is under way
+      A.theta = th;
+    }
+    const float vbest = fmaxf(fmaxf(vm[0], vm[1]), fmaxf(vm[2], vm[3]));
+    if (vbest > A.kv[KF - 1] && vbest >= A.theta) {  // rare once the row is under way
 #pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          if (vm[k] > A.kv[KF - 1] && vm[k] >= A.theta) {
-            A.kv[KF - 1] = vm[k];
-            A.kq[KF - 1] = qbase + k * NT;
+      for (int k = 0; k < kU; ++k) {
+        if (vm[k] > A.kv[KF - 1] && vm[k] >= A.theta) {
+          A.kv[KF - 1] = vm[k];
+          A.kq[KF - 1] = qbase + k * NT;
 #pragma unroll
-            for (int x = KF - 1; x > 0; --x) {
-              if (A.kv[x] > A.kv[x - 1]) {  // later vectors lose ties
-                const float t1 = A.kv[x];
-                A.kv[x] = A.kv[x - 1];
-                A.kv[x - 1] = t1;
-                const int t2 = A.kq[x];
-                A.kq[x] = A.kq[x - 1];
-                A.kq[x - 1] = t2;
-              }
+          for (int x = KF - 1; x > 0; --x) {
+            if (A.kv[x] > A.kv[x - 1]) {  // later vectors lose ties
+              const float t1 = A.kv[x];
+              A.kv[x] = A.kv[x - 1];
+              A.kv[x - 1] = t1;
+              const int t2 = A.kq[x];
+              A.kq[x] = A.kq[x - 1];
+              A.kq[x - 1] = t2;
             }
           }
         }
       }
     }
-  } else if (EXP) {
-    // Exp-only rows: the offset comes from the first step that has a finite
-    // value and moves only when a step's sum shows a far larger value.
-    if (A.c == INFINITY) {
-      float vm[kU];
-      const float g = step_max<E, FULL>(v, kv, vm);
-      if (g > -INFINITY) A.c = -(g * s);
-    }
-    if (A.c != INFINITY) {
-      float ss = exp_sum<E, FULL>(v, kv, s2, pk2(A.c, A.c));
-      if (!(ss <= kBig)) {
-        float vm[kU];
-        const float cn = -(step_max<E, FULL>(v, kv, vm) * s);
-        if (cn < A.c) {
-          const float f = ex2(cn - A.c);
-          A.z *= f;
-          A.zc *= f;
-          A.c = cn;
-        }
-        ss = exp_sum<E, FULL>(v, kv, s2, pk2(A.c, A.c));
-      }
-      kahan_add(A.z, A.zc, ss);
-    }
+  }
   }
 }
 
-// End of a row: warp statistics into `ws`, the warp's best KF key vectors
-// into wsel[0..KF).
-template <typename E, int KF, bool EXP, bool ARG, bool KEYS>
-__device__ __forceinline__ void row_end(RowAcc<KF> &A, int v0, int hp, WStat *ws, int *wsel) {
+// End of a row piece: warp statistics into `ws` (a piece that failed the
+// finiteness check gets a NaN sum), the warp's best KF key vectors into
+// wsel[0..KF).
+template <typename E, int KF>
+__device__ __forceinline__ void row_end_gen(RowAcc<KF> &A, int fl, bool bad, int v0, int hp,
+                                            WStat *ws, int *wsel) {
   constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec;
   constexpr int KFm = RowAcc<KF>::KFm;
   const int lane = threadIdx.x & 31;
   WStat st{-INFINITY, 0.f, INFINITY, INT32_MAX};
-  if (ARG) {
-    const float mw = rmax_f(A.m);
+  const float mw = rmax_f(A.m);
+  st.m = mw;
+  if (fl & kFArg) {
     int idx = INT32_MAX;
     if (A.m == mw && mw > -INFINITY && A.bq >= 0) {
       float f[N];
@@ -898,18 +915,18 @@ __device__ __forceinline__ void row_end(RowAcc<KF> &A, int v0, int hp, WStat *ws
       for (int i = N - 1; i >= 0; --i)
         if (f[i] == mw) idx = elem_index(v0, hp, A.bq, i, sz);
     }
-    st.m = mw;
     st.idx = rmin_i(idx);
   }
-  if (EXP) {
+  if (fl & kFExp) {
     const bool has = A.z > 0.f;
     const float cw = rmin_f(has ? A.c : INFINITY);  // smallest offset: the largest max
     const float zt = has ? (A.z - A.zc) * ex2(cw - A.c) : 0.f;
     st.z = warp_sum(zt);
     st.c = cw;
   }
+  if ((fl & kFChk) && ballot(bad) != 0u) st.z = __int_as_float(0x7fffffff);
   if (lane == 0) *ws = st;
-  if (KEYS) {
+  if (KF > 0 && (fl & kFKeys)) {
 #pragma unroll
     for (int r = 0; r < KFm; ++r) {
       float bv = A.kv[0];
@@ -928,49 +945,6 @@ __device__ __forceinline__ void row_end(RowAcc<KF> &A, int v0, int hp, WStat *ws
     }
   }
   A.reset();
-}
-
-// Stream this CTA's slice of one row: each step first copies the step
-// kDepth-1 ahead (possibly of a later row), then waits for its own copies.
-template <typename E, int KF, int NT, bool EXP, bool ARG, bool KEYS>
-__device__ __forceinline__ void stream_row(RowAcc<KF> &A, const RowInfo &R, Issuer &I,
-                                           const Static &S, int nrows, const uint8_t *ring,
-                                           uint32_t ring_t, uint32_t &c_off, int v0, int v1,
-                                           float s, uint64_t s2, WStat *ws, int *wsel) {
-  constexpr int kStepVec = NT * kU;
-  constexpr uint32_t kSlot = kU * NT * 16;
-  const int nsteps = R.nsteps, sf0 = R.sf0, sf1 = R.sf1, qlo = R.qlo, qhi = R.qhi;
-  const int nvec = R.nvec, qd_step = R.qd_step, qd = R.qd, excl = R.excl, hp = R.hp;
-  for (int step = 0; step < nsteps; ++step) {
-    issue_step<NT>(I, S, nrows, ring_t);
-    cp_wait<kDepth - 1>();  // this step's copies have landed
-    const uint8_t *src = ring + c_off;
-    uint4 v[kU];
-    if (step >= sf0 && step < sf1) {
-#pragma unroll
-      for (int k = 0; k < kU; ++k) v[k] = *reinterpret_cast<const uint4 *>(src + k * NT * 16);
-      step_body<E, KF, NT, EXP, ARG, KEYS, true>(A, v, kU, step, qd_step, qd, excl, v0, hp, s, s2);
-    } else {
-      const int kv = min(kU, (nvec - step * kStepVec + NT - 1) / NT);
-#pragma unroll
-      for (int k = 0; k < kU; ++k) {
-        const int q = step * kStepVec + k * NT + (int)threadIdx.x;
-        if (q >= qlo && q < qhi) {
-          v[k] = *reinterpret_cast<const uint4 *>(src + k * NT * 16);
-        } else if (q < nvec) {
-          v[k] = load_vec_slow<E>(R, q, v0, v1);
-        } else {
-          const uint32_t w = Elt<E>::kNegInfWord;
-          v[k] = make_uint4(w, w, w, w);
-        }
-      }
-      step_body<E, KF, NT, EXP, ARG, KEYS, false>(A, v, kv, step, qd_step, qd, excl, v0, hp, s,
-                                                  s2);
-    }
-    c_off += kSlot;
-    if (c_off >= kDepth * kSlot) c_off -= kDepth * kSlot;
-  }
-  row_end<E, KF, EXP, ARG, KEYS>(A, v0, hp, ws, wsel);
 }
 
 // The CTA's best KF elements (value desc, index asc) of key row R from the
@@ -1071,14 +1045,12 @@ static __device__ __forceinline__ void seq_outputs(const Params &P, const Static
     if (P.hit) P.hit[b] = (uint8_t)(hit ? 1 : 0);
     if (!valid && P.status)
       atomicOr(P.status, (tvalid ? 0 : (int)SD_STATUS_BAD_TEMP) |
-                             (S.dvalid ? 0 : (int)SD_STATUS_BAD_TOKEN));
+                             (S.dvalid ? 0 : (int)SD_STATUS_BAD_TOKEN) |
+                             ((tvalid && S.dvalid && !S.fvalid) ? (int)SD_STATUS_NONFINITE : 0));
   }
 }
 
-// SPLIT: the finish of the split launch -- the rows were streamed by
-// sd_flat_stream_kernel, whose piece records replace this kernel's stream and
-// its first cluster exchange; everything from the combine on is shared.
-template <typename E, int KF, int NT, bool SPLIT = false>
+template <typename E, int KF, int NT>
 __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ Params P) {
   constexpr int sz = Elt<E>::kSize, NV = Elt<E>::kPerVec;
   constexpr int KFm = KF > 0 ? KF : 1;
@@ -1095,20 +1067,10 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
 
   // launched as a programmatic dependent of the stream's previous kernel:
   // nothing is read before that kernel has finished and its writes are
-  // visible (the launch itself overlaps its tail); the split finish waits
-  // further down, for its streaming grid
-  if (!SPLIT) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // visible (the launch itself overlaps its tail)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // every CTA of the cluster has started before any pushes into its memory
   cluster_arrive_relaxed();
-  if (SPLIT && warp == 0) {
-    // Run the out-of-line helpers of the accept scan and the draw once, on
-    // values the compiler cannot fold, before anything else: the first jump
-    // into a helper late in the chain otherwise costs microseconds.
-    const ff w0 = ff_warp_scan(ff{(float)(lane * P.V), (float)P.K});
-    const ff w1 = ff_warp_sum(w0);
-    const float w2 = exp2_ff(ff{w1.lo, 0.f});
-    if (w2 == -1.f) S.tok = -2;  // never true: keeps the calls
-  }
 
   const int v0 = min(rank * P.slice, P.V);
   const int v1 = min(v0 + P.slice, P.V);
@@ -1208,37 +1170,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
   // [v0, v1) of every row, or an equal share of the sequence's rows laid end
   // to end in stream order, cut at whole streaming steps of a row (a few row
   // pieces per CTA instead of a piece of every row)
-  if constexpr (SPLIT) {
-    // This sequence's rank among the sampled sequences and their count place
-    // its rows in the flat stream (see Params); streaming CTA c covered steps
-    // [U c / G, U (c+1) / G).
-    int ns = 0, rk = 0;
-    for (int x0 = 0; x0 < P.B; x0 += NT) {
-      const int x = x0 + tid;
-      const float tx = x < P.B ? P.temps[x] : 0.f;
-      const bool sx = tx > 0.f && tx <= 3.4e38f;
-      ns += __syncthreads_count(sx);
-      rk += __syncthreads_count(sx && x < b);
-    }
-    if (tid < nrows) {
-      const RowInfo &R = S.rows[tid];
-      const int g = K - R.j;
-      int64_t off = 0, rtot = 0;
-      for (int x = 0; x <= K; ++x) {
-        const int n = P.B + (P.grp_x[x] == 2 ? P.B : (P.grp_x[x] == 1 ? ns : 0));
-        if (x < g) off += n;
-        rtot += n;
-      }
-      const int gx = P.grp_x[g];
-      const bool xpres = gx == 2 || (gx == 1 && sampled);
-      const int64_t r = off + b + (gx == 2 ? b : (gx == 1 ? rk : 0)) +
-                        ((R.kind == kTarget && xpres) ? 1 : 0);
-      const int64_t U = rtot * P.spr, G = P.gstream;
-      S.rflat[tid] = (int)r;
-      S.pc0[tid] = (int)(((r * P.spr + 1) * G - 1) / U);
-      S.pc1[tid] = (int)(((r + 1) * P.spr * G - 1) / U);
-    }
-  } else if (tid < nrows) {
+  if (tid < nrows) {
     RowInfo &R = S.rows[tid];
     if (P.rowsplit) {
       constexpr int ue = NT * kU * 16 / sz;  // elements per streaming step
@@ -1268,51 +1200,47 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
   ff *cmass = reinterpret_cast<ff *>(dyn + L.cmass);
   float *pmass = reinterpret_cast<float *>(dyn + L.pmass);
 
-  // ---- stream every row once
-  if constexpr (!SPLIT) {
-    const uint64_t s2 = pk2(s, s);
+  // ---- stream every row once: one row loop for every kind of row
+  {
     Issuer I;
     I.row = 0;
     I.slot = ring_t;
     issuer_row<NT>(I, S, nrows);
 #pragma unroll
-    for (int d = 0; d < kDepth - 1; ++d) issue_step<NT>(I, S, nrows, ring_t);
+    for (int d = 0; d < kDepth - 1; ++d) issue_fill<E, NT>(I, S, nrows, ring_t);
     uint32_t c_off = tid * 16;
     RowAcc<KF> A;
     A.reset();
+    const bool chk = P.chk != 0;
+    const uint64_t s2 = pk2(s, s);
+    constexpr uint32_t kSlot = kU * NT * 16;
+#pragma unroll 1
     for (int r = 0; r < nrows; ++r) {
       const RowInfo &R = S.rows[r];
       WStat *ws = &wstat[r * NW + warp];
       int *wk = &wsel[(R.j * NW + warp) * KFm];
+      const int fl = row_flags(R.type, chk);
       if (R.nsteps == 0) {  // this CTA holds none of the row
         if (lane == 0) *ws = WStat{-INFINITY, 0.f, INFINITY, INT32_MAX};
-        if (KF > 0 && (R.type == kRowK || R.type == kRowEK) && lane < KFm) wk[lane] = INT32_MAX;
+        if (KF > 0 && (fl & kFKeys) && lane < KFm) wk[lane] = INT32_MAX;
         continue;
       }
-      switch (R.type) {
-        case kRowE:
-          stream_row<E, KF, NT, true, false, false>(A, R, I, S, nrows, ring, ring_t, c_off, R.v0, R.v1,
-                                                   s, s2, ws, wk);
-          break;
-        case kRowEA:
-          stream_row<E, KF, NT, true, true, false>(A, R, I, S, nrows, ring, ring_t, c_off, R.v0, R.v1,
-                                                  s, s2, ws, wk);
-          break;
-        case kRowA:
-          stream_row<E, KF, NT, false, true, false>(A, R, I, S, nrows, ring, ring_t, c_off, R.v0,
-                                                   R.v1, s, s2, ws, wk);
-          break;
-        default:
-          if (KF > 0) {
-            if (R.type == kRowK)
-              stream_row<E, KF, NT, false, false, (KF > 0)>(A, R, I, S, nrows, ring, ring_t, c_off,
-                                                            R.v0, R.v1, s, s2, ws, wk);
-            else
-              stream_row<E, KF, NT, true, false, (KF > 0)>(A, R, I, S, nrows, ring, ring_t, c_off,
-                                                           R.v0, R.v1, s, s2, ws, wk);
-          }
-          break;
+      const int nsteps = R.nsteps, qd_step = R.qd_step, qd = R.qd, excl = R.excl;
+      const int rv0 = R.v0, hp = R.hp;
+      bool bad = false;
+#pragma unroll 1
+      for (int step = 0; step < nsteps; ++step) {
+        issue_fill<E, NT>(I, S, nrows, ring_t);
+        cp_wait<kDepth - 1>();  // this step's copies have landed
+        const uint8_t *src = ring + c_off;
+        uint4 v[kU];
+#pragma unroll
+        for (int k = 0; k < kU; ++k) v[k] = *reinterpret_cast<const uint4 *>(src + k * NT * 16);
+        step_gen<E, KF, NT>(A, v, step, fl, qd_step, qd, excl, rv0, hp, s, s2, bad);
+        c_off += kSlot;
+        if (c_off >= kDepth * kSlot) c_off -= kDepth * kSlot;
       }
+      row_end_gen<E, KF>(A, fl, bad, rv0, hp, ws, wk);
     }
     cp_wait<0>();
   }
@@ -1324,16 +1252,13 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
   }
   __syncthreads();
 
-  if constexpr (SPLIT) {
-    // the streaming grid has finished and its records are visible
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    cluster_wait();  // pairs with the arrive at the top
-  } else {
-  // ---- CTA statistics per row (thread per row), pushed into every CTA
+  // ---- CTA statistics per row (thread per row), pushed into every CTA (a
+  // warp with a NaN sum, from the finiteness check, makes the sum NaN)
   cluster_wait();  // pairs with the arrive at the top
   if (tid < nrows) {
     const int r = tid;
     float M = -INFINITY;
+    bool poison = false;
 #pragma unroll 1
     for (int w = 0; w < NW; ++w) M = fmaxf(M, wstat[r * NW + w].m);
     int I = INT32_MAX;
@@ -1343,6 +1268,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       const WStat x = wstat[r * NW + w];
       if (x.m == M) I = min(I, x.idx);
       if (x.z > 0.f) C = fminf(C, x.c);
+      poison |= x.z != x.z;
     }
     ff Z{0.f, 0.f};
 #pragma unroll 1
@@ -1350,6 +1276,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       const WStat x = wstat[r * NW + w];
       if (x.z > 0.f) Z = ff_add(Z, two_prod(x.z, ex2(C - x.c)));
     }
+    if (poison) Z.hi = __int_as_float(0x7fffffff);
     CStat cst;
     cst.m = M;
     cst.idx = I;
@@ -1378,34 +1305,11 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
     }
   }
   cluster.sync();  // (1) every CTA's statistics are in every CTA
-  }
 
   // ---- combine the cluster's statistics (same arithmetic in every CTA)
-  if constexpr (SPLIT) {
-    // the same combine over the row's piece records (at most kMaxParts):
-    // one warp per row, lane p holding piece p, all records loaded at once
-    for (int r = warp; r < nrows; r += NW) {
-      const int np = S.pc1[r] - S.pc0[r] + 1;
-      CStat x{-INFINITY, INT32_MAX, INFINITY, 0.f, 0.f};
-      if (lane < np) {
-        const float *rp = reinterpret_cast<const float *>(
-            P.ws + (int64_t)(S.pc0[r] + lane + S.rflat[r]) * kRecBytes);
-        const float4 a4 = __ldcg(reinterpret_cast<const float4 *>(rp));
-        x = CStat{a4.x, __float_as_int(a4.y), a4.z, a4.w, __ldcg(rp + 4)};
-      }
-      const float M = rmax_f(x.m);
-      const int I = rmin_i(x.m == M ? x.idx : INT32_MAX);
-      const float C = rmin_f(x.zhi > 0.f ? x.c : INFINITY);
-      const ff zt = x.zhi > 0.f ? ff_mul_f(ff{x.zhi, x.zlo}, ex2(C - x.c)) : ff{0.f, 0.f};
-      const ff Z = ff_warp_sum(zt);
-      if (lane == 0) {
-        S.M[r] = M;
-        S.C[r] = C;
-        S.Z[r] = Z;
-        S.amax[r] = I == INT32_MAX ? 0 : I;
-      }
-    }
-  } else if (!SPLIT && tid < nrows) {
+  if (tid == 0) S.fvalid = 1;
+  __syncthreads();
+  if (tid < nrows) {
     const int r = tid;
     float M = -INFINITY;
 #pragma unroll 1
@@ -1419,15 +1323,18 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       if (x.zhi > 0.f) C = fminf(C, x.c);
     }
     ff Z{0.f, 0.f};
+    bool poison = false;
 #pragma unroll 1
     for (int p = 0; p < cs; ++p) {
       const CStat &x = cstat[p * nrows + r];
       if (x.zhi > 0.f) Z = ff_add(Z, ff_mul_f(ff{x.zhi, x.zlo}, ex2(C - x.c)));
+      poison |= x.zhi != x.zhi;
     }
     S.M[r] = M;
     S.C[r] = C;
     S.Z[r] = Z;
     S.amax[r] = I == INT32_MAX ? 0 : I;
+    if (P.chk && (poison || !(M > -INFINITY))) S.fvalid = 0;
   }
   if (KF > 0 && P.keys) {
     // keys of each position: the best fan of the cs x KF CTA candidates
@@ -1446,17 +1353,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
         const int c = lane + 32 * h;  // candidate c: CTA c / KF, rank c % KF
         cv[h] = -INFINITY;
         ci[h] = INT32_MAX;
-        if constexpr (SPLIT) {
-          // candidate c: piece c / KF of the key row, rank c % KF
-          const int kr = present ? S.drow[j] : 0;
-          if (present && c < (S.pc1[kr] - S.pc0[kr] + 1) * KFm) {
-            const float2 e = __ldcg(reinterpret_cast<const float2 *>(
-                P.ws + (int64_t)(S.pc0[kr] + c / KFm + S.rflat[kr]) * kRecBytes + 32 +
-                (c % KFm) * 8));
-            cv[h] = e.x;
-            ci[h] = __float_as_int(e.y);
-          }
-        } else if (present && c < cs * KFm) {
+        if (present && c < cs * KFm) {
           const float2 e = ckeys[((c / KFm) * npos + j) * KFm + c % KFm];
           cv[h] = e.x;
           ci[h] = __float_as_int(e.y);
@@ -1525,7 +1422,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
         rej = !a;
       }
       const unsigned rejects = ballot(rej);
-      if (sampled && tvalid && dvalid && lane < 2) {  // the rows the draw reads
+      if (sampled && tvalid && dvalid && S.fvalid && lane < 2) {  // the rows the draw reads
         const int mm = rejects ? __ffs(rejects) - 1 : K;
         if (lane == 0) {
           S.dt = S.rows[S.trow[mm]];
@@ -1538,7 +1435,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       if (lane == 0) {
         const int mm = rejects ? __ffs(rejects) - 1 : K;
         S.m = mm;
-        S.valid = (tvalid && dvalid) ? 1 : 0;
+        S.valid = (tvalid && dvalid && S.fvalid) ? 1 : 0;
         S.kind = 0;
         S.owner = 0;
         S.tok = -1;
@@ -1808,28 +1705,57 @@ static int env_int(const char *name, int dflt) {
   return s && *s ? atoi(s) : dflt;
 }
 
-static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
+// Host-side state is kept per device: a process may drive several GPUs, and
+// SM counts, kernel attributes and occupancy answers belong to one of them.
+constexpr int kMaxDevices = 64;
+
+static int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    dev = 0;
   }
-  return n;
+  return dev;
 }
+
+static int sm_count() {
+  static int n[kMaxDevices];
+  const int dev = current_device();
+  if (n[dev] <= 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 1;
+  }
+  return n[dev];
+}
+
+// Sets a kernel's dynamic shared-memory limit (and, for cluster kernels, the
+// non-portable cluster sizes) once on each device it is launched on.
+struct FuncAttrs {
+  std::mutex mu;
+  bool done[kMaxDevices] = {};
+  void apply(const void *fn, int smem_cap, bool clusters, const char *what) {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> g(mu);
+    if (done[dev]) return;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cap) !=
+        cudaSuccess)
+      fprintf(stderr, "sd_verify: shared-memory limit of %s not set: %s\n", what,
+              cudaGetErrorString(cudaGetLastError()));
+    if (clusters &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      cudaGetLastError();
+    done[dev] = true;
+  }
+};
 
 static const int kDynSmemCap = 227 * 1024 - (int)sizeof(Static) - 256;
 
-template <typename E, int KF, int NT, bool SPLIT = false>
+template <typename E, int KF, int NT>
 static void *kernel_fn() {
-  static std::once_flag once;
-  void *fn = (void *)sd_seq_kernel<E, KF, NT, SPLIT>;
-  std::call_once(once, [fn] {
-    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmemCap);
-    cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    cudaGetLastError();
-  });
+  static FuncAttrs attrs;
+  void *fn = (void *)sd_seq_kernel<E, KF, NT>;
+  attrs.apply(fn, kDynSmemCap, true, "the cluster kernel");
   return fn;
 }
 
@@ -1882,14 +1808,16 @@ static int smem_bytes(const Params &P, int cs) {
 }
 
 // Clusters of cs CTAs with `smem` bytes each that the device holds at once.
-template <typename E, int KF, int NT, bool SPLIT = false>
+template <typename E, int KF, int NT>
 static int max_active_clusters(int cs, int smem) {
   static std::mutex mu;
-  static int cache[kMaxCS + 1][8];
-  static int cache_smem[kMaxCS + 1][8];
+  static int cache[kMaxDevices][kMaxCS + 1][8];
+  static int cache_smem[kMaxDevices][kMaxCS + 1][8];
+  const int dev = current_device();
+  void *fn = kernel_fn<E, KF, NT>();
   std::lock_guard<std::mutex> g(mu);
   const int slot = (smem / 1024) % 8;
-  if (cache_smem[cs][slot] == smem + 1) return cache[cs][slot];
+  if (cache_smem[dev][cs][slot] == smem + 1) return cache[dev][cs][slot];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)cs, 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
@@ -1902,19 +1830,19 @@ static int max_active_clusters(int cs, int smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kernel_fn<E, KF, NT, SPLIT>(), &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
-  cache[cs][slot] = n;
-  cache_smem[cs][slot] = smem + 1;
+  cache[dev][cs][slot] = n;
+  cache_smem[dev][cs][slot] = smem + 1;
   return n;
 }
 
 // Cluster size: the largest cs up to about SDV_CPS (default 2) CTAs per SM
 // for which all B clusters are resident at once (one wave); if none is,
 // the size that leaves the fewest waves.
-template <typename E, int KF, int NT, bool SPLIT = false>
+template <typename E, int KF, int NT>
 static int choose_cs(const Params &P) {
   const int forced = env_int("SDV_CS", 0);
   if (forced) return forced;
@@ -1927,7 +1855,7 @@ static int choose_cs(const Params &P) {
   for (int cs = target; cs >= 1; --cs) {
     const int smem = smem_bytes<E, KF, NT>(P, cs);
     if (smem > kDynSmemCap) break;
-    const int n = max_active_clusters<E, KF, NT, SPLIT>(cs, smem);
+    const int n = max_active_clusters<E, KF, NT>(cs, smem);
     if (n <= 0) continue;
     if (n >= B) return cs;
     const int64_t waves = (B + n - 1) / n;

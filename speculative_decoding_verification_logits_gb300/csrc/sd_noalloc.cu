@@ -26,7 +26,6 @@ namespace sdv {
 constexpr size_t kStaticScratchBytes = (size_t)2 << 20;
 static __device__ __align__(256) uint8_t g_sd_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
 static std::mutex g_scratch_mu;
 static void *g_scratch_addr[kMaxDevices];
 

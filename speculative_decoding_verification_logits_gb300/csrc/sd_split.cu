@@ -1,37 +1,50 @@
-// Split launch of the verify step: a flat streaming grid, then the
-// per-sequence finish.
+// Split launch of the verify step: a flat streaming grid over the logit rows
+// of all sequences, then a compact per-sequence finish.
 //
-// The cluster kernel gives each sequence its own cluster, which leaves SMs
-// unevenly loaded whenever the clusters do not tile the device exactly, and
-// makes every CTA of a cluster wait for the slowest one before the accept
-// scan.  Here the streaming is one grid of about two CTAs per SM over all
-// logit rows of all sequences laid end to end.  Every CTA gets the same
-// number of streaming steps (16 KB each), so every SM moves the same number
-// of bytes.  Rows are grouped by position, j = K first: in group j, sequence
-// after sequence, draft row j (the bonus draft row for j = K), when the
-// sequence needs it, then target row j.  Draft rows with keys and target
-// rows alternate, so every CTA sees the same mix of row kinds.  A CTA's
-// range usually cuts one or two rows.
-// It writes, per row piece, the statistics the combine needs (max,
-// lowest-index argmax, offset exp-sum) and its best key candidates, to a
-// record in caller-provided scratch.  The rows of the first positions, where
-// a rejection is likeliest, come last in the flat order (streamed by the
-// last CTAs of the grid); the draw re-reads its two rows from L2 when a
-// round's logits fit there, from HBM otherwise.
+// Streaming grid.  About two CTAs per SM stream the rows of all sequences
+// laid end to end; every CTA gets the same number of 16 KB streaming steps,
+// so every SM moves the same bytes.  Rows are grouped by position, j = K
+// first: in group j, sequence after sequence, draft row j (the bonus draft
+// row for j = K) when the sequence needs it, then target row j; draft rows
+// with keys and target rows alternate, so every CTA sees the same mix of
+// row kinds.  The rows of the first positions, where a rejection is
+// likeliest, come last and are still in L2 when the finish re-reads them.
+// One row loop serves every kind of row (the statistics a row needs --
+// offset exp-sum, argmax, key vectors, the finiteness check -- are switched
+// per row), and ragged vectors are assembled into the copy ring where they
+// are issued, so the loop always consumes whole steps.  Per row piece the
+// CTA writes a record: max, lowest-index argmax, the offset exp-sum as a
+// float-float pair and its best key candidates.
 //
-// The finish is sd_seq_kernel<..., SPLIT = true>: one cluster per sequence,
-// launched as a programmatic dependent of the streaming grid; its CTAs take
-// the place of streaming CTAs as those exit (the register file holds no
-// more) and run their prologue (row table, drafted tokens, their logits, the
-// uniforms, the sequence's place in the flat order).  After griddepcontrol.wait
-// it combines the records of each of its rows in the same order in every CTA,
-// merges the key candidates, and continues exactly as the cluster kernel does
-// after its first exchange: accept scan, one inverse-CDF draw over the
-// cluster's vocabulary slices, outputs.  The packing launch follows as before.
+// Finish.  One thread-block cluster per sequence, launched as a
+// programmatic dependent of the streaming grid: its prologue (drafted
+// tokens, their logits, the uniforms, the sequence's place in the flat
+// order) reads only inputs and overlaps the stream's tail.  Then every CTA
+// combines the records of each row in the same order, so all CTAs take the
+// same accept decisions; warp 0 runs the accept scan while the other warps
+// merge the key candidates.  The draw (residual max(0, p - q) at the first
+// rejection m, or p at the bonus position) splits the vocabulary over the
+// cluster's CTAs: each warp reads its contiguous share of the two rows with
+// all of its loads in flight at once, keeps one mass per (iteration, lane),
+// and the CTA masses are exchanged over distributed shared memory.  The CTA
+// holding u * S then narrows the crossing down warp -> iteration -> lane ->
+// element with one float-float search routine.  The kernel is kept small
+// (loops, one shared search routine, no per-kind copies of the row code):
+// the chain after the stream runs once per sequence, and straight-line code
+// that misses the instruction caches costs several cycles per instruction.
+//
+// Method sources (web pages): "What is speculative decoding" explainer
+// (lotook.com), the four-stage loop and the FAQ on losslessness;
+// "Speculative Speculative Decoding" blog (jiwasawa.github.io), Saguaro
+// 1. Outcome Prediction; "LLMの生成を5倍速くする「D3D」を図で読む"
+// (animemo.app), 検証のまとめ.  Readings where they are silent are listed in
+// include/sd_verify.h.
 
 #include "sd_device.cuh"
 
 namespace sdv {
+
+// =========================================================== streaming grid
 
 // Dynamic shared memory of the streaming kernel (byte offsets).
 struct FlatLayout {
@@ -59,6 +72,7 @@ __global__ void __launch_bounds__(NT, 2) sd_flat_stream_kernel(const __grid_cons
   constexpr int KFm = KF > 0 ? KF : 1;
   constexpr int NW = NT / 32;
   constexpr int ue = NT * kU * 16 / sz;  // elements per streaming step
+  constexpr uint32_t kSlot = kU * NT * 16;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = P.K;
 
@@ -69,8 +83,8 @@ __global__ void __launch_bounds__(NT, 2) sd_flat_stream_kernel(const __grid_cons
   // Launched as a programmatic dependent of the stream's previous kernel:
   // nothing is read before that kernel has finished.  Then the finish grid
   // may be scheduled at once: its CTAs take the place of streaming CTAs as
-  // those exit and run their prologue meanwhile (reading only inputs, now
-  // complete; their griddepcontrol.wait still waits for this whole grid).
+  // those exit and run their prologue meanwhile (reading only inputs; their
+  // griddepcontrol.wait still waits for this whole grid).
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const FlatLayout FL = flat_layout(NT, KF, P.B);
@@ -86,6 +100,7 @@ __global__ void __launch_bounds__(NT, 2) sd_flat_stream_kernel(const __grid_cons
   for (int g = 0; g <= K; ++g) sonly |= P.grp_x[g] == 1;
   int ns = 0;
   if (sonly) {
+#pragma unroll 1
     for (int x0 = 0; x0 < P.B; x0 += NT) {
       const int x = x0 + tid;
       const float tx = x < P.B ? P.temps[x] : 0.f;
@@ -172,57 +187,51 @@ __global__ void __launch_bounds__(NT, 2) sd_flat_stream_kernel(const __grid_cons
   }
   __syncthreads();
 
-  // ---- stream the pieces (the same row loops as the cluster kernel, with
-  // each row's own scale)
+  // ---- stream the pieces: one row loop for every kind of row
   {
     Issuer I;
     I.row = 0;
     I.slot = ring_t;
     issuer_row<NT>(I, S, nrows);
 #pragma unroll
-    for (int d = 0; d < kDepth - 1; ++d) issue_step<NT>(I, S, nrows, ring_t);
+    for (int d = 0; d < kDepth - 1; ++d) issue_fill<E, NT>(I, S, nrows, ring_t);
     uint32_t c_off = tid * 16;
     RowAcc<KF> A;
     A.reset();
+    const bool chk = P.chk != 0;
+#pragma unroll 1
     for (int r = 0; r < nrows; ++r) {
       const RowInfo &R = S.rows[r];
-      WStat *ws = &wstat[r * NW + warp];
-      int *wk = &wsel[(r * NW + warp) * KFm];
+      const int fl = row_flags(R.type, chk);
       const float s = R.s;
       const uint64_t s2 = pk2(s, s);
-      switch (R.type) {
-        case kRowE:
-          stream_row<E, KF, NT, true, false, false>(A, R, I, S, nrows, ring, ring_t, c_off, R.v0, R.v1,
-                                                   s, s2, ws, wk);
-          break;
-        case kRowEA:
-          stream_row<E, KF, NT, true, true, false>(A, R, I, S, nrows, ring, ring_t, c_off, R.v0, R.v1,
-                                                  s, s2, ws, wk);
-          break;
-        case kRowA:
-          stream_row<E, KF, NT, false, true, false>(A, R, I, S, nrows, ring, ring_t, c_off, R.v0,
-                                                   R.v1, s, s2, ws, wk);
-          break;
-        default:
-          if (KF > 0) {
-            if (R.type == kRowK)
-              stream_row<E, KF, NT, false, false, (KF > 0)>(A, R, I, S, nrows, ring, ring_t, c_off,
-                                                            R.v0, R.v1, s, s2, ws, wk);
-            else
-              stream_row<E, KF, NT, true, false, (KF > 0)>(A, R, I, S, nrows, ring, ring_t, c_off,
-                                                           R.v0, R.v1, s, s2, ws, wk);
-          }
-          break;
+      const int nsteps = R.nsteps, qd_step = R.qd_step, qd = R.qd, excl = R.excl;
+      const int v0 = R.v0, hp = R.hp;
+      bool bad = false;
+#pragma unroll 1
+      for (int step = 0; step < nsteps; ++step) {
+        issue_fill<E, NT>(I, S, nrows, ring_t);
+        cp_wait<kDepth - 1>();  // this step's copies have landed
+        const uint8_t *src = ring + c_off;
+        uint4 v[kU];
+#pragma unroll
+        for (int k = 0; k < kU; ++k) v[k] = *reinterpret_cast<const uint4 *>(src + k * NT * 16);
+        step_gen<E, KF, NT>(A, v, step, fl, qd_step, qd, excl, v0, hp, s, s2, bad);
+        c_off += kSlot;
+        if (c_off >= kDepth * kSlot) c_off -= kDepth * kSlot;
       }
+      row_end_gen<E, KF>(A, fl, bad, v0, hp, &wstat[r * NW + warp], &wsel[(r * NW + warp) * KFm]);
     }
     cp_wait<0>();
   }
   __syncthreads();
 
-  // ---- one record per piece: the warps combined as in the cluster kernel
+  // ---- one record per piece: the warps combined in a fixed order (a warp
+  // with a NaN sum, from the finiteness check, makes the piece's sum NaN)
   if (tid < nrows) {
     const int r = tid;
     float M = -INFINITY;
+    bool poison = false;
 #pragma unroll 1
     for (int w = 0; w < NW; ++w) M = fmaxf(M, wstat[r * NW + w].m);
     int Ix = INT32_MAX;
@@ -232,6 +241,7 @@ __global__ void __launch_bounds__(NT, 2) sd_flat_stream_kernel(const __grid_cons
       const WStat x = wstat[r * NW + w];
       if (x.m == M) Ix = min(Ix, x.idx);
       if (x.z > 0.f) C = fminf(C, x.c);
+      poison |= x.z != x.z;
     }
     ff Z{0.f, 0.f};
 #pragma unroll 1
@@ -239,11 +249,13 @@ __global__ void __launch_bounds__(NT, 2) sd_flat_stream_kernel(const __grid_cons
       const WStat x = wstat[r * NW + w];
       if (x.z > 0.f) Z = ff_add(Z, two_prod(x.z, ex2(C - x.c)));
     }
+    if (poison) Z.hi = __int_as_float(0x7fffffff);
     float *rec = reinterpret_cast<float *>(P.ws + (int64_t)S.rows[r].rec * kRecBytes);
     *reinterpret_cast<float4 *>(rec) = make_float4(M, __int_as_float(Ix), C, Z.hi);
     rec[4] = Z.lo;
   }
   if (KF > 0) {
+#pragma unroll 1
     for (int r = warp; r < nrows; r += NW) {
       const RowInfo &R = S.rows[r];
       if (!(R.type == kRowK || R.type == kRowEK)) continue;
@@ -253,22 +265,616 @@ __global__ void __launch_bounds__(NT, 2) sd_flat_stream_kernel(const __grid_cons
   }
 }
 
-// ------------------------------------------------------------------- host --
+// =================================================================== finish
+
+constexpr int kFinNT = 256;
+constexpr int kFinNW = kFinNT / 32;
+constexpr int kFinCH = 8;  // draw iterations whose loads a warp keeps in flight together
+
+// Row slots of one sequence in the finish: slot j (0..K) is target row j,
+// slot K + 1 + j the draft row j (j < K) or the bonus draft row (j = K).
+struct FinS {
+  int rflat[kMaxRows];  // the slot's row in the flat stream, -1 if absent
+  int pc0[kMaxRows];    // first streaming CTA over the row
+  int npc[kMaxRows];    // streaming CTAs over the row (piece records)
+  float M[kMaxRows];
+  float C[kMaxRows];
+  ff Z[kMaxRows];
+  int amax[kMaxRows];
+  int d[SD_MAX_K];
+  float ld_t[SD_MAX_K], ld_d[SD_MAX_K];
+  float u_acc[SD_MAX_K];
+  float u_draw[SD_MAX_K + 1];
+  int2 keys[(SD_MAX_K + 1) * SD_MAX_FANOUT];
+  RowInfo dt, dd;  // draw: target and draft row at m on this CTA's slice
+  RowInfo ddt;     // the draft row read element-wise on the target's vector grid
+  ff wmass[kFinNW];
+  ff cmass[2][kMaxCS];  // per-CTA masses of the draw, entry c pushed by CTA c
+  ff t_loc, t_w;
+  int m, kind, valid, dvalid, fvalid, tok, owner, cstar, wsel;
+};
+
+// The crossing point of a warp's values x (one per lane, in index order)
+// for target t: the first lane with positive mass whose inclusive prefix
+// exceeds t; if none (rounding put t at or past the total), the last lane
+// with positive mass (crossed = 0); l = -1 when no lane has mass.  `before`
+// is the prefix before lane l, `total` the warp's sum.  Whole warp.
+struct Cross {
+  int l, crossed;
+  ff before, total;
+};
+static __device__ __noinline__ Cross ff_cross(ff x, ff t) {
+  const ff incl = ff_warp_scan(x);
+  const unsigned cross = ballot(ff_pos(x) && ff_gt(incl, t));
+  const unsigned pos = ballot(ff_pos(x));
+  Cross c;
+  c.crossed = cross != 0u;
+  c.l = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : -1);
+  c.before = ff_shfl(ff_sub(incl, x), c.l < 0 ? 0 : c.l);
+  if (c.l < 0) c.before = ff{0.f, 0.f};
+  c.total = ff_shfl(incl, 31);
+  return c;
+}
+
+// The sequence's outputs, by one warp: lane j writes token j, the lanes test
+// the keys together.
+static __device__ void fin_outputs(const Params &P, const FinS &S, int b, bool tvalid) {
+  const int lane = threadIdx.x & 31, K = P.K;
+  int32_t *out = P.out_tokens + (int64_t)b * (K + 1);
+  const bool valid = S.valid != 0;
+  const int mm = valid ? S.m : -1, tok = S.tok;
+  for (int j = lane; j <= K; j += 32) out[j] = !valid ? -1 : (j < mm ? S.d[j] : (j == mm ? tok : -1));
+  bool h = false;
+  if (valid && P.hit) {
+    if (P.keys) {
+      for (int k2 = lane; k2 < P.n_keys_out; k2 += 32)
+        h |= S.keys[k2].x == mm && S.keys[k2].y == tok;
+    } else if (P.keys_in) {
+      const int32_t *kb = P.keys_in + (int64_t)b * P.n_keys_in * 2;
+      for (int k2 = lane; k2 < P.n_keys_in; k2 += 32)
+        h |= kb[2 * k2] == mm && kb[2 * k2 + 1] == tok;
+    }
+  }
+  const bool hit = ballot(h) != 0u;
+  if (lane == 0) {
+    P.num_accepted[b] = valid ? mm : 0;
+    P.tau[b] = valid ? mm + 1 : 0;
+    if (P.hit) P.hit[b] = (uint8_t)(hit ? 1 : 0);
+    if (!valid && P.status) {
+      int bits = 0;
+      if (!tvalid) bits |= (int)SD_STATUS_BAD_TEMP;
+      if (!S.dvalid) bits |= (int)SD_STATUS_BAD_TOKEN;
+      if (tvalid && S.dvalid && !S.fvalid) bits |= (int)SD_STATUS_NONFINITE;
+      atomicOr(P.status, bits);
+    }
+  }
+}
+
+// Weights pass of the draw over one warp's contiguous share [wq0, wq1) of
+// this CTA's slice vectors: iteration it covers vectors wq0 + 32 it + lane.
+// Writes the mass of each (iteration, lane) to pmw[it][lane] and returns the
+// lane's total (Kahan-summed) as a float-float pair.  Whole vectors are read
+// with all loads of a chunk in flight at once; the at most two ragged
+// vectors of the slice are assembled afterwards, and a draft row off the
+// target's vector grid takes the element-wise loop.
+template <typename E>
+__device__ __noinline__ ff draw_pass(const RowInfo &Rt, const RowInfo &Rd, const RowInfo &Rdt,
+                                     bool residual, bool d_vec, int wq0, int wq1, int v0, int v1,
+                                     uint64_t s2, uint64_t ct2, uint64_t cd2, float *pmw) {
+  const int lane = threadIdx.x & 31;
+  const int nit = (wq1 - wq0 + 31) / 32;
+  const uint32_t ni = Elt<E>::kNegInfWord;
+  float tsum = 0.f, tcomp = 0.f;
+  if (residual && !d_vec) {
+#pragma unroll 1
+    for (int it = 0; it < nit; ++it) {
+      const int q = wq0 + it * 32 + lane;
+      float ms = 0.f;
+      if (q < wq1)
+        ms = vec_mass<E>(load_vec_direct<E>(Rt, q, v0, v1), load_vec_slow<E>(Rdt, q, v0, v1), true,
+                         s2, ct2, cd2);
+      pmw[it * 32 + lane] = ms;
+      kahan_add(tsum, tcomp, ms);
+    }
+    return two_sum(tsum, -tcomp);
+  }
+  const uint8_t *const tg = Rt.gbase;
+  const uint8_t *const dg = residual ? Rd.gbase : Rt.gbase;
+  const int tlo = Rt.qlo, thi = Rt.qhi;
+#pragma unroll 1
+  for (int it0 = 0; it0 < nit; it0 += kFinCH) {
+    uint4 tv[kFinCH], dv[kFinCH];
+#pragma unroll
+    for (int c = 0; c < kFinCH; ++c) {
+      const int q = wq0 + (it0 + c) * 32 + lane;
+      tv[c] = dv[c] = make_uint4(ni, ni, ni, ni);
+      if (q < wq1 && q >= tlo && q < thi) {
+        tv[c] = __ldcg(reinterpret_cast<const uint4 *>(tg + 16 * q));
+        if (residual) dv[c] = __ldcg(reinterpret_cast<const uint4 *>(dg + 16 * q));
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kFinCH; ++c) {
+      if (it0 + c < nit) {
+        const float ms = vec_mass<E>(tv[c], dv[c], residual, s2, ct2, cd2);
+        pmw[(it0 + c) * 32 + lane] = ms;
+        kahan_add(tsum, tcomp, ms);
+      }
+    }
+  }
+  // the ragged vectors, by the lanes that own them: vector 0 when the slice
+  // starts off the 16-byte grid (tlo = 1), the last when it ends off it
+#pragma unroll 1
+  for (int x = 0; x < 2; ++x) {
+    const int q = x == 0 ? (tlo > 0 ? 0 : -1) : (thi < Rt.nvec ? Rt.nvec - 1 : -1);
+    if (q < wq0 || q >= wq1 || (x == 1 && q == 0 && tlo > 0)) continue;
+    if (((q - wq0) & 31) == lane) {
+      const uint4 tvv = load_vec_slow<E>(Rt, q, v0, v1);
+      const uint4 dvv = residual ? load_vec_slow<E>(Rd, q, v0, v1) : tvv;
+      const float ms = vec_mass<E>(tvv, dvv, residual, s2, ct2, cd2);
+      pmw[((q - wq0) >> 5) * 32 + lane] = ms;
+      kahan_add(tsum, tcomp, ms);
+    }
+  }
+  return two_sum(tsum, -tcomp);
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kFinNT, 2) sd_finish_kernel(const __grid_constant__ Params P) {
+  constexpr int NT = kFinNT, NW = kFinNW;
+  constexpr int sz = Elt<E>::kSize, NV = Elt<E>::kPerVec;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int cs = P.cs;
+  const int b = blockIdx.x / cs;
+  const int K = P.K;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nslot = 2 * K + 2;
+
+  __shared__ FinS S;
+  extern __shared__ __align__(128) float pm[];  // [NW][pw][32] masses of the draw
+
+  // every CTA of the cluster has started before any pushes into its memory
+  cluster_arrive_relaxed();
+
+  // ---- prologue: inputs only (the streaming grid may still be running)
+  const float T = P.temps[b];
+  const bool tvalid = (T >= 0.f) && (T <= 3.4e38f);  // rejects NaN / inf / < 0
+  const bool sampled = tvalid && T > 0.f;
+  const float s = sampled ? log2e_over(T) : 0.f;
+  if (warp == 0) {
+    const int d = lane < K ? P.tokens[(int64_t)b * K + lane] : 0;
+    const bool dok = lane >= K || (d >= 0 && d < P.V);
+    const bool dvalid = __all_sync(0xffffffffu, dok);
+    if (lane < K) {
+      S.d[lane] = d;
+      float lt = -INFINITY, ld = -INFINITY;
+      if (sampled && dvalid) {
+        lt = Elt<E>::load_global(P.target + (((int64_t)b * (K + 1) + lane) * P.V + d) * sz);
+        ld = Elt<E>::load_global(P.draft + (((int64_t)b * K + lane) * P.V + d) * sz);
+      }
+      S.ld_t[lane] = lt;
+      S.ld_d[lane] = ld;
+    }
+    if (lane == 0) {
+      S.dvalid = dvalid ? 1 : 0;
+      S.fvalid = 1;
+    }
+    if (sampled)
+      for (int q = lane; q <= K; q += 32) {
+        if (q < K) S.u_acc[q] = uniform_u(P.seed, P.row_base + b, q, 0);
+        S.u_draw[q] = uniform_u(P.seed, P.row_base + b, q, 1);
+      }
+  }
+  // this sequence's place among the sampled sequences places its rows in
+  // the flat stream; streaming CTA c covered steps [U c / G, U (c+1) / G)
+  int ns = 0, rk = 0;
+#pragma unroll 1
+  for (int x0 = 0; x0 < P.B; x0 += NT) {
+    const int x = x0 + tid;
+    const float tx = x < P.B ? P.temps[x] : 0.f;
+    const bool sx = tx > 0.f && tx <= 3.4e38f;
+    ns += __syncthreads_count(sx);
+    rk += __syncthreads_count(sx && x < b);
+  }
+  if (tid < nslot) {
+    const int is_x = tid > K, j = is_x ? tid - (K + 1) : tid;
+    const int g = K - j;
+    int64_t off = 0, rtot = 0;
+    for (int x = 0; x <= K; ++x) {
+      const int n = P.B + (P.grp_x[x] == 2 ? P.B : (P.grp_x[x] == 1 ? ns : 0));
+      if (x < g) off += n;
+      rtot += n;
+    }
+    const int gx = P.grp_x[g];
+    const bool xpres = gx == 2 || (gx == 1 && sampled);
+    const int64_t r = off + b + (gx == 2 ? b : (gx == 1 ? rk : 0)) + ((!is_x && xpres) ? 1 : 0);
+    const int64_t U = rtot * P.spr, G = P.gstream;
+    const int c0 = (int)(((r * P.spr + 1) * G - 1) / U);
+    const int c1 = (int)(((r + 1) * P.spr * G - 1) / U);
+    S.rflat[tid] = (is_x && !xpres) ? -1 : (int)r;
+    S.pc0[tid] = c0;
+    S.npc[tid] = c1 - c0 + 1;
+  }
+  __syncthreads();
+
+  // ---- the streaming grid has finished and its records are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // ---- row statistics: one warp per row, lane p holding piece p (the same
+  // arithmetic in every CTA of the cluster)
+  const bool chk = P.chk != 0;
+#pragma unroll 1
+  for (int r = warp; r < nslot; r += NW) {
+    if (S.rflat[r] < 0) continue;
+    const int np = S.npc[r];
+    CStat x{-INFINITY, INT32_MAX, INFINITY, 0.f, 0.f};
+    if (lane < np) {
+      const float *rp = reinterpret_cast<const float *>(
+          P.ws + (int64_t)(S.pc0[r] + lane + S.rflat[r]) * kRecBytes);
+      const float4 a4 = __ldcg(reinterpret_cast<const float4 *>(rp));
+      x = CStat{a4.x, __float_as_int(a4.y), a4.z, a4.w, __ldcg(rp + 4)};
+    }
+    const bool poison = ballot(x.zhi != x.zhi) != 0u;
+    const float M = rmax_f(x.m);
+    const int I = rmin_i(x.m == M ? x.idx : INT32_MAX);
+    const float C = rmin_f(x.zhi > 0.f ? x.c : INFINITY);
+    const ff zt = x.zhi > 0.f ? ff_mul_f(ff{x.zhi, x.zlo}, ex2(C - x.c)) : ff{0.f, 0.f};
+    const ff Z = ff_warp_sum(zt);
+    if (lane == 0) {
+      S.M[r] = M;
+      S.C[r] = C;
+      S.Z[r] = Z;
+      S.amax[r] = I == INT32_MAX ? 0 : I;
+      if (chk && (poison || !(M > -INFINITY))) S.fvalid = 0;
+    }
+  }
+  __syncthreads();
+
+  const int v0 = min(rank * P.slice, P.V);
+  const int v1 = min(v0 + P.slice, P.V);
+  if (warp == 0) {
+    // ---- accept tests, one lane per position (K <= 32)
+    const int j = lane;
+    const bool dvalid = S.dvalid != 0;
+    int rej = 0;
+    if (j < K) {
+      const int d = S.d[j];
+      int a = 0;
+      if (!sampled) {
+        a = (dvalid && d == S.amax[j]) ? 1 : 0;
+      } else if (dvalid) {
+        const int rd = K + 1 + j;
+        const float lt = S.ld_t[j], ldr = S.ld_d[j];
+        // log2 of 2^(l_d s + C), carried as float-float (the products exact)
+        const ff xt = ff_add_f(two_prod(lt, s), S.C[j]);
+        const ff xd = ff_add_f(two_prod(ldr, s), S.C[rd]);
+        const float zt = ff_f(S.Z[j]), zd = ff_f(S.Z[rd]);
+        const float r = (ldr == -INFINITY) ? INFINITY  // q(d) = 0
+                                           : exp2_ff(ff_sub(xt, xd)) * __fdiv_rn(zd, zt);
+        a = (S.u_acc[j] <= r) ? 1 : 0;
+        if (rank == 0) {
+          const int64_t pj = (int64_t)b * K + j;
+          if (P.ratio_out) P.ratio_out[pj] = r;
+          if (P.p_out) P.p_out[pj] = __fdiv_rn(exp2_ff(xt), zt);
+          if (P.q_out) P.q_out[pj] = __fdiv_rn(exp2_ff(xd), zd);
+        }
+      }
+      rej = !a;
+    }
+    const unsigned rejects = ballot(rej);
+    const int mm = rejects ? __ffs(rejects) - 1 : K;
+    const bool valid = tvalid && dvalid && S.fvalid != 0;
+    if (sampled && valid && lane < 2 && (lane == 0 || mm < K)) {  // the rows the draw reads
+      RowInfo &R = lane == 0 ? S.dt : S.dd;
+      R.g = lane == 0 ? P.target + ((int64_t)b * (K + 1) + mm) * P.V * sz
+                      : P.draft + ((int64_t)b * K + mm) * P.V * sz;
+      R.excl = -1;
+      row_geometry<NT>(R, v0, v1, sz);
+    }
+    __syncwarp();
+    if (sampled && valid && lane == 0 && mm < K && S.dd.hp != S.dt.hp) {
+      S.ddt = S.dt;
+      S.ddt.g = S.dd.g;
+      S.ddt.qlo = 1;  // every vector assembled from element loads
+      S.ddt.qhi = 0;
+    }
+    if (lane == 0) {
+      S.m = mm;
+      S.valid = valid ? 1 : 0;
+      S.kind = 0;
+      S.owner = 0;
+      S.tok = -1;
+      S.cstar = 0;
+      if (valid) {
+        if (!sampled) S.tok = S.amax[mm];
+        else S.kind = mm < K ? 1 : 2;
+      }
+    }
+    if (rank == 0 && P.argmax_out)
+      for (int jj = lane; jj <= K; jj += 32) P.argmax_out[(int64_t)b * (K + 1) + jj] = S.amax[jj];
+  } else if (P.keys) {
+    // ---- keys of each position: the best fan of the pieces' candidates
+    const int kf = P.kf;
+#pragma unroll 1
+    for (int j = warp - 1; j <= K; j += NW - 1) {
+      const int fan = P.fanout[j];
+      if (fan <= 0) continue;
+      const int xs = K + 1 + j;
+      const bool present = S.rflat[xs] >= 0;
+      const int ncand = present ? S.npc[xs] * kf : 0;
+      constexpr int PER = (kMaxParts * 8 + 31) / 32;
+      float cv[PER];
+      int ci[PER];
+#pragma unroll
+      for (int h = 0; h < PER; ++h) {
+        const int c = lane + 32 * h;  // candidate c: piece c / kf, rank c % kf
+        cv[h] = -INFINITY;
+        ci[h] = INT32_MAX;
+        if (c < ncand) {
+          const float2 e = __ldcg(reinterpret_cast<const float2 *>(
+              P.ws + (int64_t)(S.pc0[xs] + c / kf + S.rflat[xs]) * kRecBytes + 32 + (c % kf) * 8));
+          cv[h] = e.x;
+          ci[h] = __float_as_int(e.y);
+        }
+      }
+      int2 *kdst = &S.keys[P.fan_off[j]];
+      int32_t *kout =
+          P.keys_out ? P.keys_out + ((int64_t)b * P.n_keys_out + P.fan_off[j]) * 2 : nullptr;
+#pragma unroll 1
+      for (int r2 = 0; r2 < fan; ++r2) {
+        float bv = -INFINITY;
+        int bi = INT32_MAX;
+#pragma unroll
+        for (int h = 0; h < PER; ++h)
+          if (cv[h] > bv || (cv[h] == bv && ci[h] < bi)) {
+            bv = cv[h];
+            bi = ci[h];
+          }
+        warp_best(bv, bi);
+#pragma unroll
+        for (int h = 0; h < PER; ++h)
+          if (bi != INT32_MAX && ci[h] == bi) {
+            cv[h] = -INFINITY;
+            ci[h] = INT32_MAX;
+          }
+        if (lane == 0) {
+          const int2 key = bi == INT32_MAX ? make_int2(-1, -1) : make_int2(j, bi);
+          kdst[r2] = key;
+          if (rank == 0 && kout) {
+            kout[2 * r2] = key.x;
+            kout[2 * r2 + 1] = key.y;
+          }
+        }
+      }
+    }
+  }
+  cluster_wait();  // pairs with the arrive at the top: every CTA has started
+  __syncthreads();
+
+  // ---- one inverse-CDF draw per sequence (residual at m, or p at K)
+#pragma unroll 1
+  for (int attempt = 0; attempt < 2 && S.kind != 0; ++attempt) {
+    const int mm = S.m;
+    const bool residual = S.kind == 1;
+    const RowInfo &Rt = S.dt;
+    const bool d_vec = residual && S.dd.hp == Rt.hp;  // the same vector grid
+    const RowInfo &Rdt = S.ddt;  // otherwise: element-wise on the target's grid
+    const float Ct = S.C[mm];
+    const float Cd = residual ? S.C[K + 1 + mm] : 0.f;
+    const float Rz = residual ? __fdiv_rn(ff_f(S.Z[mm]), ff_f(S.Z[K + 1 + mm])) : 0.f;
+    const uint64_t s2 = pk2(s, s), ct2 = pk2(Ct, Ct);
+    const float cdr = residual ? Cd + __log2f(Rz) : 0.f;  // the draft weight scaled by R
+    const uint64_t cd2 = pk2(cdr, cdr);
+    const int nvec = Rt.nvec;
+    const int wr = (nvec + NW - 1) / NW;  // vectors per warp
+    const int wq0 = min(warp * wr, nvec), wq1 = min(wq0 + wr, nvec);
+    float *pmw = pm + warp * P.pw * 32;  // [iteration][lane] masses of this warp
+    const ff lm = draw_pass<E>(Rt, S.dd, Rdt, residual, d_vec, wq0, wq1, v0, v1, s2, ct2, cd2, pmw);
+    const ff wm = ff_warp_sum(lm);
+    if (lane == 0) S.wmass[warp] = wm;
+    __syncthreads();
+    if (warp == 0) {
+      // the CTA's mass into every CTA of the cluster
+      const ff m_l = lane < NW ? S.wmass[lane] : ff{0.f, 0.f};
+      const ff tot_cta = ff_warp_sum(m_l);
+      if (lane < cs) *cluster.map_shared_rank(&S.cmass[attempt][rank], lane) = tot_cta;
+    }
+    cluster.sync();  // slice masses are in every CTA
+    if (warp == 0) {
+      const ff sc = lane < cs ? S.cmass[attempt][lane] : ff{0.f, 0.f};  // lane c: CTA c
+      const ff tot = ff_warp_sum(sc);
+      if (ff_pos(tot) || !residual) {
+        const ff t = ff_mul_f(tot, S.u_draw[mm]);
+        const Cross c = ff_cross(sc, t);
+        if (lane == 0) {
+          S.cstar = c.l < 0 ? 0 : c.l;
+          S.t_loc = ff_sub(t, c.before);
+          S.owner = S.cstar;
+        }
+      } else if (lane == 0) {
+        S.kind = 2;  // identically zero residual: draw from p at m
+      }
+    }
+    __syncthreads();
+    if (S.kind == 2 && residual) continue;  // every CTA takes this branch
+    if (rank == S.cstar) {
+      if (warp == 0) {
+        const ff m_l = lane < NW ? S.wmass[lane] : ff{0.f, 0.f};
+        const Cross c = ff_cross(m_l, S.t_loc);
+        if (lane == 0) {
+          S.wsel = c.l < 0 ? 0 : c.l;
+          S.t_w = ff_sub(S.t_loc, c.before);
+        }
+      }
+      __syncthreads();
+      if (warp == S.wsel) {
+        // the crossing iteration: lane t sums the 32 lane masses of
+        // iteration tb + t (reading its row rotated across the banks)
+        const int nit = (wq1 - wq0 + 31) / 32;
+        ff tw = S.t_w, cum{0.f, 0.f};
+        int isel = -1;
+        ff t_it{0.f, 0.f};
+#pragma unroll 1
+        for (int tb = 0; tb < nit; tb += 32) {
+          const int t = tb + lane;
+          ff mt{0.f, 0.f};
+          if (t < nit) {
+            ff a0{0.f, 0.f}, a1{0.f, 0.f};
+#pragma unroll 4
+            for (int i = 0; i < 32; i += 2) {
+              a0 = ff_add_f(a0, pmw[t * 32 + ((i + lane) & 31)]);
+              a1 = ff_add_f(a1, pmw[t * 32 + ((i + 1 + lane) & 31)]);
+            }
+            mt = ff_add(a0, a1);
+          }
+          const ff rem = ff_sub(tw, cum);
+          const Cross c = ff_cross(mt, rem);
+          if (c.l >= 0) {  // a crossing here, or the last iteration with mass so far
+            isel = tb + c.l;
+            t_it = ff_sub(rem, c.before);
+            if (c.crossed) break;
+          }
+          cum = ff_add(cum, c.total);
+        }
+        int tok = -1;
+        if (isel >= 0) {
+          // the crossing lane within that iteration
+          const Cross cl = ff_cross(ff{pmw[isel * 32 + lane], 0.f}, t_it);
+          if (cl.l >= 0) {
+            const ff t_l = ff_sub(t_it, cl.before);
+            // that lane's vector, one element per lane (index order), the
+            // first element past t_l; if rounding leaves none, the last one
+            // with weight
+            const int q = wq0 + isel * 32 + cl.l;
+            const int i = lane % NV;
+            uint4 tvv = load_vec_direct<E>(Rt, q, v0, v1);
+            uint4 dvv = tvv;
+            if (residual)
+              dvv = d_vec ? load_vec_direct<E>(S.dd, q, v0, v1) : load_vec_slow<E>(Rdt, q, v0, v1);
+            float ww[NV];
+            pass_weights<E>(tvv, dvv, residual, s2, ct2, cd2, ww);
+            float wi = 0.f;
+#pragma unroll
+            for (int ii = 0; ii < NV; ++ii)
+              if (ii == i) wi = ww[ii];
+            const int ei = elem_index(v0, Rt.hp, q, i, sz);
+            const bool ok = lane < NV && ei >= v0 && ei < v1 && wi > 0.f;
+            const Cross ce = ff_cross(ff{ok ? wi : 0.f, 0.f}, t_l);
+            tok = __shfl_sync(0xffffffffu, ei, ce.l < 0 ? 0 : ce.l);
+            if (ce.l < 0) tok = -1;
+          }
+        }
+        if (lane == 0) S.tok = tok >= 0 ? tok : S.amax[mm];
+      }
+      __syncthreads();
+    }
+    break;
+  }
+
+  // ---- the sequence's outputs (owning CTA, one warp)
+  if (rank == S.owner && warp == 0) fin_outputs(P, S, b, tvalid);
+  // No CTA touches another's shared memory after the last cluster barrier,
+  // which every CTA passes, so the CTAs may leave independently.
+}
+
+// ===================================================================== host
+
 // Dynamic shared memory the streaming kernel may use: the 227 KB a CTA can
 // hold less its static part (Static, the class offsets, the warp counts).
 static const int kFlatSmemCap = 227 * 1024 - (int)sizeof(Static) - 1024;
+static const int kFinSmemCap = 227 * 1024 - (int)sizeof(FinS) - 256;
 
 template <typename E, int KF, int NT>
 static void *flat_fn() {
-  static std::once_flag once;
+  static FuncAttrs attrs;
   void *fn = (void *)sd_flat_stream_kernel<E, KF, NT>;
-  std::call_once(once, [fn] {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kFlatSmemCap) !=
-        cudaSuccess)
-      fprintf(stderr, "sd_verify: shared-memory limit of the streaming kernel not set: %s\n",
-              cudaGetErrorString(cudaGetLastError()));
-  });
+  attrs.apply(fn, kFlatSmemCap, false, "the streaming kernel");
   return fn;
+}
+
+template <typename E>
+static void *fin_fn() {
+  static FuncAttrs attrs;
+  void *fn = (void *)sd_finish_kernel<E>;
+  attrs.apply(fn, kFinSmemCap, true, "the finish kernel");
+  return fn;
+}
+
+// Vocabulary slice of one finish CTA: an even share, a multiple of 16
+// elements (so a 16-byte aligned row keeps its slices aligned).
+static int fin_slice(int V, int cs) { return (int)((((int64_t)V + cs - 1) / cs + 15) / 16 * 16); }
+
+// Iterations of 32 vectors one warp of the finish takes in the draw over a
+// slice of `slice` elements (the slice may start off the 16-byte grid).
+static int fin_pw(int slice, int sz) {
+  const int nvec = (int)(((int64_t)slice * sz + 31) / 16) + 1;
+  return ((nvec + kFinNW - 1) / kFinNW + 31) / 32;
+}
+static int fin_smem(int pw) { return align128(4 * kFinNW * pw * 32); }
+
+// Clusters of cs finish CTAs with `smem` bytes each that the device holds at once.
+template <typename E>
+static int fin_active_clusters(int cs, int smem) {
+  static std::mutex mu;
+  static int cache[kMaxDevices][kMaxCS + 1];
+  static int cache_smem[kMaxDevices][kMaxCS + 1];
+  const int dev = current_device();
+  void *fn = fin_fn<E>();
+  std::lock_guard<std::mutex> g(mu);
+  if (cache_smem[dev][cs] == smem + 1) return cache[dev][cs];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cs, 1, 1);
+  cfg.blockDim = dim3(kFinNT, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[dev][cs] = n;
+  cache_smem[dev][cs] = smem + 1;
+  return n;
+}
+
+// Cluster size of the finish: the largest cs up to about two CTAs per SM for
+// which all B clusters are resident at once; if none is, the size that
+// leaves the fewest waves.
+template <typename E>
+static int choose_fin_cs(const Params &P) {
+  constexpr int sz = Elt<E>::kSize;
+  const int forced = env_int("SDV_CS", 0);
+  if (forced >= 1 && forced <= kMaxCS) return forced;
+  const int per_sm = std::max(1, env_int("SDV_CPS", 2));
+  const int B = std::max(P.B, 1);
+  const int target = (int)std::min<int64_t>(
+      kMaxCS, std::max<int64_t>(1, (int64_t)per_sm * sm_count() / B));
+  int best = -1;
+  int64_t best_waves = INT64_MAX;
+  for (int cs = target; cs >= 1; --cs) {
+    const int smem = fin_smem(fin_pw(fin_slice(P.V, cs), sz));
+    if (smem > kFinSmemCap) break;
+    const int n = fin_active_clusters<E>(cs, smem);
+    if (n <= 0) continue;
+    if (n >= B) return cs;
+    const int64_t waves = (B + n - 1) / n;
+    if (waves < best_waves) {
+      best_waves = waves;
+      best = cs;
+    }
+  }
+  if (best > 0) return best;
+  for (int cs = target; cs <= kMaxCS; ++cs)
+    if (fin_smem(fin_pw(fin_slice(P.V, cs), sz)) <= kFinSmemCap) return cs;
+  return kMaxCS;
 }
 
 // Groups of the flat stream (see Params): g = 0..K for position K - g.
@@ -302,6 +908,7 @@ sd_status_t launch_split(Params &P, size_t ws_bytes, cudaStream_t stream) {
   int64_t rmin = 0, rmax = 0;
   flat_groups(P, rmin, rmax);
   P.spr = (P.V + ue - 1) / ue;
+  P.kf = KF > 0 ? KF : 1;
   // About two CTAs per SM.  Never more CTAs than steps (no CTA is empty),
   // nor so many that one row spans more than kMaxParts CTAs.
   int64_t G = std::min<int64_t>(2LL * sm_count(), kMaxStreamGrid);
@@ -316,13 +923,14 @@ sd_status_t launch_split(Params &P, size_t ws_bytes, cudaStream_t stream) {
   const FlatLayout FL = flat_layout(NT, KF, P.B);
   if (FL.total > kFlatSmemCap) return SD_ERR_UNSUPPORTED;
   P.gstream = (int)G;
-  const int cs = choose_cs<E, KF, NT, true>(P);
+  const int cs = choose_fin_cs<E>(P);
   if (cs < 1 || cs > kMaxCS) return SD_ERR_UNSUPPORTED;
   P.cs = cs;
-  P.slice = slice_for(P.V, cs, sz, NT);
+  P.slice = fin_slice(P.V, cs);
   P.rowsplit = 0;
-  const Layout L = make_layout(NT, rows_per_seq(P), P.K + 1, KF, cs, P.slice, sz);
-  if (L.total > kDynSmemCap) return SD_ERR_UNSUPPORTED;
+  P.pw = fin_pw(P.slice, sz);
+  const int fsmem = fin_smem(P.pw);
+  if (fsmem > kFinSmemCap) return SD_ERR_UNSUPPORTED;
 
   // the streaming grid: a programmatic dependent of the stream's previous
   // kernel (it waits for it before reading anything)
@@ -344,8 +952,8 @@ sd_status_t launch_split(Params &P, size_t ws_bytes, cudaStream_t stream) {
   // the finish: one cluster per sequence, a programmatic dependent
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3((unsigned)(P.B * cs), 1, 1);
-  cfg2.blockDim = dim3(NT, 1, 1);
-  cfg2.dynamicSmemBytes = (size_t)L.total;
+  cfg2.blockDim = dim3(kFinNT, 1, 1);
+  cfg2.dynamicSmemBytes = (size_t)fsmem;
   cfg2.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -358,8 +966,8 @@ sd_status_t launch_split(Params &P, size_t ws_bytes, cudaStream_t stream) {
   cfg2.numAttrs = 2;
   if (env_int("SDV_VERBOSE", 0))
     fprintf(stderr, "sd_verify split: B=%d K=%d V=%d G=%d spr=%d cs=%d slice=%d KF=%d "
-            "smem=%d/%d\n", P.B, P.K, P.V, (int)G, P.spr, cs, P.slice, KF, FL.total, L.total);
-  e = cudaLaunchKernelEx(&cfg2, (void (*)(const Params))kernel_fn<E, KF, NT, true>(), P);
+            "smem=%d/%d\n", P.B, P.K, P.V, (int)G, P.spr, cs, P.slice, KF, FL.total, fsmem);
+  e = cudaLaunchKernelEx(&cfg2, (void (*)(const Params))fin_fn<E>(), P);
   if (e != cudaSuccess) {
     fprintf(stderr, "sd_verify finish launch failed: %s\n", cudaGetErrorString(e));
     return SD_ERR_CUDA;

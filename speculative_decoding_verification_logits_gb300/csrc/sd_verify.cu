@@ -100,20 +100,15 @@ static sd_status_t launch_nt(Params &P, cudaStream_t stream) {
   return SD_OK;
 }
 
-// With scratch from the caller, the split launch where it pays: where the
-// cluster kernel would leave SMs without a CTA (B cs < SMs) or would give
-// each sequence a single CTA (cs = 1), so that one SM streams a whole
-// sequence.  Otherwise -- or without scratch, or when the request is
-// outside the split launch's limits -- the cluster kernel.  SDV_SPLIT=1 / 0
-// forces either.
+// With scratch from the caller, the split launch (a flat streaming grid over
+// all sequences' rows, every SM moving the same bytes, then the compact
+// finish); without scratch, or when the request is outside the split
+// launch's limits, the cluster kernel.  SDV_SPLIT=0 forces the cluster
+// kernel.
 template <typename E, int KF>
 static sd_status_t launch_kf(Params &P, cudaStream_t s) {
   const int mode = env_int("SDV_SPLIT", -1);
-  bool split = P.ws != nullptr && mode != 0;
-  if (split && mode < 0 && P.mode == kVerify) {
-    const int cs = choose_cs<E, KF, 256>(P);
-    split = cs <= 1 || (int64_t)P.B * cs < sm_count();
-  }
+  const bool split = P.ws != nullptr && mode != 0 && P.mode == kVerify;
   if (split) {
     const sd_status_t st = launch_split<E, KF>(P, P.ws_bytes, s);
     if (st != SD_ERR_UNSUPPORTED) return st;
@@ -160,7 +155,8 @@ sd_status_t sd_verify(const sd_verify_args *a, void *stream) {
   if ((int64_t)a->B * kMaxCS > INT32_MAX) return SD_ERR_INVALID_ARG;
   const bool predict = (a->flags & SD_FLAG_PREDICT) != 0;
   const bool compact = (a->flags & SD_FLAG_COMPACT) != 0;
-  if (a->flags & ~(SD_FLAG_PREDICT | SD_FLAG_COMPACT)) return SD_ERR_INVALID_ARG;
+  if (a->flags & ~(SD_FLAG_PREDICT | SD_FLAG_COMPACT | SD_FLAG_CHECK_FINITE))
+    return SD_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   if (compact && !a->offsets) return SD_ERR_INVALID_ARG;
   if (a->B == 0) {
@@ -202,6 +198,7 @@ sd_status_t sd_verify(const sd_verify_args *a, void *stream) {
   P.K = a->K;
   P.V = a->V;
   P.compact = compact ? 1 : 0;
+  P.chk = (a->flags & SD_FLAG_CHECK_FINITE) ? 1 : 0;
   P.ws = (uint8_t *)a->workspace;
   P.ws_bytes = a->workspace ? a->workspace_bytes : 0;
   if (predict) {

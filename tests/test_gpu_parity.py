@@ -332,6 +332,63 @@ def test_repeated_calls_and_scratch(dev, monkeypatch, capfd):
     _check(*compare_verify(c, o, inp2.temperature.cpu().numpy(), check_stats=False))
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_check_finite_flags_rows_read(dev, path, dt):
+    # SD_FLAG_CHECK_FINITE: a NaN or +inf, or a row of only -inf, in any row
+    # the call reads makes that sequence invalid with SD_STATUS_NONFINITE; a
+    # single -inf is a valid logit; every other sequence is exact against the
+    # oracle (which applies the same rule to the same rows)
+    B, K, V = 24, 4, 9001
+    fan = [2, 0, 1, 0, 1]                      # keys at positions 0, 2 and K
+    temps = [0.0 if b % 3 == 0 else 0.8 for b in range(B)]
+    inp = W.synth(B, K, V, dt, kind="peaked", sigma=3.0, draft_sigma=1.0, peaks=10,
+                  temperature=temps, seed=606, device=dev, bonus_row=True)
+    t, d, bo = inp.target.float(), inp.draft.float(), inp.draft_bonus.float()
+    rng = np.random.default_rng(606)
+    planted = [float("nan"), float("inf"), "allneg", float("-inf"), None]
+    for b in range(B):
+        kind = planted[b % 5]
+        if kind is None:
+            continue
+        where = (b // 5) % 3
+        arr = t[b] if where == 0 else d[b] if where == 1 else bo[b:b + 1]
+        r = int(rng.integers(0, arr.shape[0]))
+        if kind == "allneg":
+            arr[r, :] = float("-inf")
+        else:
+            arr[r, int(rng.integers(0, V))] = kind
+    dtype = inp.target.dtype
+    inp.target, inp.draft = t.to(dtype).contiguous(), d.to(dtype).contiguous()
+    inp.draft_bonus = bo.to(dtype).contiguous()
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, fanout=fan,
+                  draft_bonus=inp.draft_bonus, check_finite=True, compact=True)
+    torch.cuda.synchronize()
+    o = oracle.verify(_np(inp.target), _np(inp.draft), inp.tokens.cpu().numpy(),
+                      inp.temperature.cpu().numpy(), inp.seed, check_finite=True, fanout=fan,
+                      draft_bonus=_np(inp.draft_bonus))
+    flagged = o["nonfinite"].astype(bool)
+    assert 5 < flagged.sum() < B
+    np.testing.assert_array_equal(r.tau.cpu().numpy() == 0, flagged)
+    assert int(r.status.item()) & sd.SD_STATUS_NONFINITE
+    assert (r.out_tokens.cpu().numpy()[flagged] == -1).all()
+    assert (r.hit.cpu().numpy()[flagged] == 0).all()
+    keys_ref = oracle.outcome_predict(_np(inp.draft), inp.tokens.cpu().numpy(), fan,
+                                      _np(inp.draft_bonus))
+    ok = ~flagged
+    np.testing.assert_array_equal(r.keys.cpu().numpy()[ok], keys_ref[ok])
+    o2 = _oracle_for(inp, keys=keys_ref)
+    rows = list(np.nonzero(ok)[0])
+    stats, bad = compare_verify(r, {k: (v[rows] if isinstance(v, np.ndarray) else v)
+                                    for k, v in o2.items()}, np.asarray(temps)[rows],
+                                check_stats=False, rows=rows)
+    _check(stats, bad)
+    # without the flag the same call faults nothing and flags nothing
+    r2 = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, fanout=fan,
+                   draft_bonus=inp.draft_bonus, compact=True)
+    torch.cuda.synchronize()
+    assert not int(r2.status.item()) & sd.SD_STATUS_NONFINITE
+
+
 def test_row_base_splits_batch_identically(dev, path):
     B, K, V = 10, 4, 9000
     inp = W.synth(B, K, V, "bf16", kind="normal", temperature=0.9, seed=31, device=dev)

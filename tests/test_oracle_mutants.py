@@ -63,6 +63,13 @@ MUTANTS = {
                                     "*near = false;  // the draw fell"),
     "guard_accept_window_wide": ("std::fabs(u - r[(size_t)j]) < kGuard",
                                  "std::fabs(u - r[(size_t)j]) < 10 * kGuard"),
+    "finite_allows_posinf": ("if (std::isnan(v) || v == std::numeric_limits<double>::infinity()) return true;",
+                             "if (std::isnan(v)) return true;"),
+    "finite_allows_all_neg_inf": ("  return !any_finite;\n}", "  return false;\n}"),
+    "finite_reads_every_draft_row": ("if (T > 0.0 || (fc.keys_at && fc.keys_at[j] > 0))",
+                                     "if (true)"),
+    "finite_skips_bonus_row": ("if (!bad && fc.bonus && fc.keys_at && fc.keys_at[K] > 0)",
+                               "if (false)"),
     "guard_accept_never": ("if (res.guard_pos < 0 && std::fabs(u - r[(size_t)j]) < kGuard)",
                            "if (false)"),
 }
@@ -70,6 +77,7 @@ MUTANTS = {
 FAST_PINS = [
     pins.test_guard_flags_decisions_near_a_boundary,
     pins.test_guard_flags_draws_near_a_cdf_edge,
+    pins.test_finite_check_flags_exactly_the_rows_read,
     pins.test_worked_example_greedy,
     pins.test_bonus_when_all_greedy_drafts_match,
     pins.test_greedy_argmax_ties_match_torch_first_occurrence,

@@ -512,6 +512,56 @@ def test_guard_flags_draws_near_a_cdf_edge(oracle_lib):
         assert r["guard_pos"] == (1 if flagged else -1)
 
 
+def _row_bad(row):
+    """NaN or +inf anywhere, or nothing but -inf: the check's definition."""
+    row = np.asarray(row, np.float64)
+    return bool(np.isnan(row).any() or np.isposinf(row).any() or np.isneginf(row).all())
+
+
+def test_finite_check_flags_exactly_the_rows_read(oracle_lib):
+    # The optional finiteness check makes a sequence invalid when a row the
+    # step reads for it holds NaN or +inf, or only -inf.  Rows read: the K+1
+    # target rows; draft row j when the sequence is sampled or keys are built
+    # at j; the bonus draft row when keys are built at K.  Brute force over
+    # planted values, against a numpy restatement of that rule.
+    rng = np.random.default_rng(123)
+    B, K, V = 40, 3, 12
+    target = rng.normal(size=(B, K + 1, V)).astype(np.float32)
+    draft = rng.normal(size=(B, K, V)).astype(np.float32)
+    bonus = rng.normal(size=(B, V)).astype(np.float32)
+    tokens = rng.integers(0, V, size=(B, K)).astype(np.int32)
+    temps = np.where(np.arange(B) % 2 == 0, 0.0, 0.8).astype(np.float32)
+    fan = np.array([2, 0, 1, 1], np.int32)       # keys at positions 0, 2 and K
+    planted = [np.nan, np.inf, "allneg", -np.inf]  # the last one alone is allowed
+    for b in range(B):
+        kind = planted[b % 4]
+        where = (b // 4) % 3                     # 0 target, 1 draft, 2 bonus
+        arr = target[b] if where == 0 else draft[b] if where == 1 else bonus[b:b + 1]
+        r = rng.integers(0, arr.shape[0])
+        if kind == "allneg":
+            arr[r, :] = -np.inf
+        else:
+            arr[r, rng.integers(0, V)] = kind
+    ref = oracle_lib.verify(target, draft, tokens, temps, seed=5, fanout=fan, draft_bonus=bonus,
+                            check_finite=True)
+    plain = oracle_lib.verify(target, draft, tokens, temps, seed=5)
+    for b in range(B):
+        rows = [target[b, j] for j in range(K + 1)]
+        rows += [draft[b, j] for j in range(K) if temps[b] > 0 or fan[j] > 0]
+        if fan[K] > 0:
+            rows.append(bonus[b])
+        expect = any(_row_bad(x) for x in rows)
+        assert bool(ref["nonfinite"][b]) == expect, b
+        if expect:
+            assert ref["tau"][b] == 0 and (ref["out_tokens"][b] == -1).all()
+        else:
+            assert ref["tau"][b] == plain["tau"][b]
+            np.testing.assert_array_equal(ref["out_tokens"][b], plain["out_tokens"][b])
+    assert ref["nonfinite"].sum() > 10 and ref["nonfinite"].sum() < B
+    assert plain["nonfinite"].sum() == 0         # without the check nothing is flagged
+    assert ref["invalid_rows"] == int(ref["nonfinite"].sum())
+
+
 # ------------------------------------------------------------------- Philox ----
 # Random123's published known-answer vectors for Philox4x32-10
 # (Salmon et al., SC'11 distribution): (counter, key) -> output.
