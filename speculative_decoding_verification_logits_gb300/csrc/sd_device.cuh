@@ -796,8 +796,8 @@ __device__ __forceinline__ void issue_fill(Issuer &I, const Static &S, int nrows
 // One step of one row: kU whole vectors per thread (-inf padded).  kFExp:
 // offset exp-sum; kFArg: running max and the first vector that reached it;
 // kFKeys: the thread's best KF vectors by masked max; kFChk: NaN or +inf
-// seen.  The running max is kept for every row (the finiteness check and
-// the offset use it).
+// seen.  The running max is kept for every row but the exp-only ones (the
+// finiteness check and the offset of the others use it).
 template <typename E, int KF, int NT>
 __device__ __forceinline__ void step_gen(RowAcc<KF> &A, const uint4 (&v)[kU], int step, int fl,
                                          int qd_step, int qd, int excl, int v0, int hp, float s,
@@ -805,6 +805,30 @@ __device__ __forceinline__ void step_gen(RowAcc<KF> &A, const uint4 (&v)[kU], in
   constexpr int sz = Elt<E>::kSize, N = Elt<E>::kPerVec;
   const int qbase = step * (NT * kU) + threadIdx.x;
   float vm[kU];
+  if (fl == kFExp) {
+    // Exp-only rows: the offset comes from the first step that has a finite
+    // value and moves only when a step's sum shows a far larger value (no
+    // running max: nothing reads it for these rows).
+    if (A.c == INFINITY) {
+      const float g = step_max<E, true>(v, kU, vm);
+      if (g > -INFINITY) A.c = -(g * s);
+    }
+    if (A.c != INFINITY) {
+      float ss = exp_sum<E, true>(v, kU, s2, pk2(A.c, A.c));
+      if (!(ss <= kBig)) {
+        const float cn = -(step_max<E, true>(v, kU, vm) * s);
+        if (cn < A.c) {
+          const float f = ex2(cn - A.c);
+          A.z *= f;
+          A.zc *= f;
+          A.c = cn;
+        }
+        ss = exp_sum<E, true>(v, kU, s2, pk2(A.c, A.c));
+      }
+      kahan_add(A.z, A.zc, ss);
+    }
+    return;
+  }
   const float gmax = step_max<E, true>(v, kU, vm);
   if (fl & kFChk) {
 #pragma unroll
@@ -1013,6 +1037,15 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+// A full cluster barrier (release / acquire) for code that every thread of
+// every warp reaches together.  The .aligned form keeps each warp converged
+// past the barrier; the unaligned form that cluster_group::sync() uses may
+// release the threads of a warp separately, and the float-float shuffle code
+// that follows it then ran several times slower.
+__device__ __forceinline__ void cluster_sync_aligned() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+               "memory");
 }
 
 // The sequence's outputs, by one warp: lane j writes token j, the lanes
@@ -1304,7 +1337,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
             stage[x % KFm];
     }
   }
-  cluster.sync();  // (1) every CTA's statistics are in every CTA
+  cluster_sync_aligned();  // (1) every CTA's statistics are in every CTA
 
   // ---- combine the cluster's statistics (same arithmetic in every CTA)
   if (tid == 0) S.fvalid = 1;
@@ -1546,7 +1579,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
         const ff tot_cta = ff_shfl(incl, 31);
         if (lane < cs) *cluster.map_shared_rank(&cmass[attempt * cs + rank], lane) = tot_cta;
       }
-      cluster.sync();  // (2) slice masses are in every CTA
+      cluster_sync_aligned();  // (2) slice masses are in every CTA
       if (warp == 0) {
         const ff sc = lane < cs ? cmass[attempt * cs + lane] : ff{0.f, 0.f};  // lane c: CTA c
         const ff incl = ff_warp_scan(sc);

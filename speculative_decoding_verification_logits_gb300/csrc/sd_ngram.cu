@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(NT) sd_ngram_kernel(int L, int K, int n_max, i
   __shared__ unsigned cbest;           // rank 0: the cluster's best key
   if (tid < n_max) pat[tid] = tid < n_tok ? __ldg(h + n_tok - 1 - tid) : -1;
   if (tid == 0) best = cbest = 0u;
-  cluster.sync();  // every CTA has started (and zeroed cbest) before any push
+  cluster_sync_aligned();  // every CTA has started (and zeroed cbest) before any push
   // CTA `rank` of the row's cluster takes rounds rank, rank + cs, ...: its
   // own rounds hold decreasing places, so a full-length match ends them
   for (int j0 = n_tok - 1 - rank * NT * kJP; j0 >= 1; j0 -= cs * NT * kJP) {
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(NT) sd_ngram_kernel(int L, int K, int n_max, i
     if ((best >> kJBits) == (unsigned)n_max) break;  // nothing later can beat it
   }
   if (tid == 0) atomicMax(cluster.map_shared_rank(&cbest, 0), best);
-  cluster.sync();  // every CTA's best is in rank 0
+  cluster_sync_aligned();  // every CTA's best is in rank 0
   if (rank != 0) return;
   const unsigned key = cbest;
   const int c = (int)(key >> kJBits), j = (int)(key & ((1u << kJBits) - 1u));

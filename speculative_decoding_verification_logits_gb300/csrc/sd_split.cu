@@ -66,8 +66,15 @@ __host__ __device__ inline FlatLayout flat_layout(int NT, int KF, int B) {
   return L;
 }
 
+// CTAs of the streaming kernel per SM (three, where the registers allow it
+// for rows without key tracking, measured slower: more CTAs contend for the
+// same HBM bandwidth and the last wave of steps ends later).
+template <int KF>
+constexpr int stream_ctas_per_sm() { return 2; }
+
 template <typename E, int KF, int NT>
-__global__ void __launch_bounds__(NT, 2) sd_flat_stream_kernel(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(NT, stream_ctas_per_sm<KF>())
+    sd_flat_stream_kernel(const __grid_constant__ Params P) {
   constexpr int sz = Elt<E>::kSize;
   constexpr int KFm = KF > 0 ? KF : 1;
   constexpr int NW = NT / 32;
@@ -505,17 +512,28 @@ __global__ void __launch_bounds__(kFinNT, 2) sd_finish_kernel(const __grid_const
   // ---- row statistics: one warp per row, lane p holding piece p (the same
   // arithmetic in every CTA of the cluster)
   const bool chk = P.chk != 0;
+  // the records of two of a warp's rows are loaded together, then reduced
 #pragma unroll 1
-  for (int r = warp; r < nslot; r += NW) {
-    if (S.rflat[r] < 0) continue;
-    const int np = S.npc[r];
-    CStat x{-INFINITY, INT32_MAX, INFINITY, 0.f, 0.f};
-    if (lane < np) {
+  for (int r0 = warp; r0 < nslot; r0 += 2 * NW) {
+  float4 ra[2];
+  float rb[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = r0 + i * NW;
+    ra[i] = make_float4(-INFINITY, __int_as_float(INT32_MAX), INFINITY, 0.f);
+    rb[i] = 0.f;
+    if (r < nslot && S.rflat[r] >= 0 && lane < S.npc[r]) {
       const float *rp = reinterpret_cast<const float *>(
           P.ws + (int64_t)(S.pc0[r] + lane + S.rflat[r]) * kRecBytes);
-      const float4 a4 = __ldcg(reinterpret_cast<const float4 *>(rp));
-      x = CStat{a4.x, __float_as_int(a4.y), a4.z, a4.w, __ldcg(rp + 4)};
+      ra[i] = __ldcg(reinterpret_cast<const float4 *>(rp));
+      rb[i] = __ldcg(rp + 4);
     }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = r0 + i * NW;
+    if (r >= nslot || S.rflat[r] < 0) continue;
+    const CStat x{ra[i].x, __float_as_int(ra[i].y), ra[i].z, ra[i].w, rb[i]};
     const bool poison = ballot(x.zhi != x.zhi) != 0u;
     const float M = rmax_f(x.m);
     const int I = rmin_i(x.m == M ? x.idx : INT32_MAX);
@@ -529,6 +547,7 @@ __global__ void __launch_bounds__(kFinNT, 2) sd_finish_kernel(const __grid_const
       S.amax[r] = I == INT32_MAX ? 0 : I;
       if (chk && (poison || !(M > -INFINITY))) S.fvalid = 0;
     }
+  }
   }
   __syncthreads();
 
@@ -681,7 +700,7 @@ __global__ void __launch_bounds__(kFinNT, 2) sd_finish_kernel(const __grid_const
       const ff tot_cta = ff_warp_sum(m_l);
       if (lane < cs) *cluster.map_shared_rank(&S.cmass[attempt][rank], lane) = tot_cta;
     }
-    cluster.sync();  // slice masses are in every CTA
+    cluster_sync_aligned();  // slice masses are in every CTA
     if (warp == 0) {
       const ff sc = lane < cs ? S.cmass[attempt][lane] : ff{0.f, 0.f};  // lane c: CTA c
       const ff tot = ff_warp_sum(sc);
@@ -909,9 +928,9 @@ sd_status_t launch_split(Params &P, size_t ws_bytes, cudaStream_t stream) {
   flat_groups(P, rmin, rmax);
   P.spr = (P.V + ue - 1) / ue;
   P.kf = KF > 0 ? KF : 1;
-  // About two CTAs per SM.  Never more CTAs than steps (no CTA is empty),
+  // Two CTAs per SM.  Never more CTAs than steps (no CTA is empty),
   // nor so many that one row spans more than kMaxParts CTAs.
-  int64_t G = std::min<int64_t>(2LL * sm_count(), kMaxStreamGrid);
+  int64_t G = std::min<int64_t>((int64_t)stream_ctas_per_sm<KF>() * sm_count(), kMaxStreamGrid);
   const int forced = env_int("SDV_GRID", 0);
   if (forced > 0) G = std::min<int64_t>(forced, kMaxStreamGrid);
   G = std::min<int64_t>({G, (int64_t)(kMaxParts - 1) * rmin, rmin * P.spr});
