@@ -14,7 +14,10 @@ fused sd_verify launch per step.
 
 Prints one JSON line (rank 0).  Timing: W untimed warm-up steps, then
 exactly K steps between barrier + synchronize on both sides, CUDA events on
-the launching stream, max over ranks.  Inputs rotate over a pool of input
+the launching stream, max over ranks.  The default run also measures every
+config of the benchmark table (1 small, 2 peaked, 3 zipf, 4 saguaro, 5 mix)
+into `per_config` (each with its own steps, clocks, roofline fraction, CPU
+baseline sample and that sample's parity counts).  Inputs rotate over a pool of input
 sets whose total exceeds 4x the L2 size, so no step reads logits a recent
 step left in L2.  ``--impl reference`` times the CPU oracle on the host
 cores instead (the reference arm).
@@ -163,9 +166,9 @@ def profiled_traffic(workload):
 def launch_plan(call):
     """The launch plan the library took for `call` (run once, synchronised):
     with SDV_VERBOSE=1 it names it on stderr, read here at the descriptor
-    level.  Returns the kernel launches of one verify round: 3 for the split
-    launch (streaming grid, finish, packing), 2 for the cluster kernel and
-    the packing launch."""
+    level.  Returns the kernel launches of one verify round and the
+    plan's name: 3 for the split launch (streaming grid, finish, packing), 2
+    for the cluster kernel and the packing launch."""
     import tempfile
     old_env = os.environ.get("SDV_VERBOSE")
     os.environ["SDV_VERBOSE"] = "1"
@@ -184,7 +187,7 @@ def launch_plan(call):
                 os.environ["SDV_VERBOSE"] = old_env
         f.seek(0)
         text = f.read().decode(errors="replace")
-    return 3 if "sd_verify split:" in text else 2
+    return (3, "split") if "sd_verify split:" in text else (2, "cluster")
 
 
 def algorithmic_bytes(inp: W.Inputs) -> int:
@@ -192,25 +195,44 @@ def algorithmic_bytes(inp: W.Inputs) -> int:
 
 
 # ---------------------------------------------------------------- GPU arm ---
-def run_gpu(args):
-    import speculative_decoding_verification_logits_gb300 as sd
+# BASELINE configs 1..5, in order: the per-config object of the default run
+CONFIGS = ["small", "peaked", "zipf", "saguaro", "mix"]
 
-    ws_n, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if ws_n > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    sd.lib()
-    name = args.workload
+
+def l2_note(n_sets, set_bytes, l2):
+    return (f"rotating {n_sets} input sets ({n_sets * set_bytes / 1e6:.0f} MB, "
+            f"> 4x L2 {l2 / 1e6:.0f} MB)")
+
+
+def pool_size(set_bytes, l2):
+    """Input sets in the rotating pool: together more than 4x L2."""
+    return max(2, int(np.ceil(4 * l2 / set_bytes)) + 1)
+
+
+def config_of(name, ws_n, l2):
+    """The `config` object of a workload's line (the same on both arms)."""
+    s = W.WORKLOADS[name]
+    B, K, V = s["B"], s["K"], s["V"]
+    es = 2 if s["dtype"] == "bf16" else 4
+    set_bytes = ((2 * K + 1) * V * B + (B * V if s.get("fanout") else 0)) * es
+    n_sets = pool_size(set_bytes, l2)
+    return {"workload": describe(name), "global_batch": B * ws_n, "seq_len": K + 1,
+            "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU",
+            "l2": l2_note(n_sets, set_bytes, l2)}
+
+
+def measure(name, steps, warmup, dev, rank, ws_n, e2e_steps=0):
+    """Timed verify rounds of one workload on this GPU (graph-replayed, inputs
+    rotating over a pool larger than 4x L2), and optionally the end-to-end
+    rounds through host buffers.  Returns a dict; collective timing (max over
+    ranks) when ws_n > 1."""
+    import speculative_decoding_verification_logits_gb300 as sd
     spec = W.WORKLOADS[name]
     fan = spec.get("fanout")
-
-    # pool of input sets totalling more than 4x L2
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     one = W.workload(name, round_idx=0, device=dev)
     set_bytes = W.logit_bytes(one, algorithmic=False, with_bonus=True)
-    n_sets = max(2, int(np.ceil(4 * l2 / set_bytes)) + 1)
+    n_sets = pool_size(set_bytes, l2)
     pool = [one] + [W.workload(name, round_idx=i, device=dev) for i in range(1, n_sets)]
     B, K, V = one.B, one.K, one.V
     for p in pool:   # distinct uniforms per rank
@@ -245,13 +267,14 @@ def run_gpu(args):
                            K + 1, out=rolls[i % n_sets], stream=stream)
 
     with torch.cuda.stream(stream):
-        n_launch = launch_plan(lambda: step(0)) + (2 if pack else 0)
-        for i in range(max(args.warmup, 3)):
+        n_launch, plan_name = launch_plan(lambda: step(0))
+        n_launch += 2 if pack else 0
+        for i in range(max(warmup, 3)):
             step(i)
     torch.cuda.synchronize(dev)
 
     # capture G steps per graph (launch-bound inner loop), replay to cover K
-    G = min(args.steps, max(n_sets, (256 // n_sets) * n_sets))
+    G = min(steps, max(n_sets, (256 // n_sets) * n_sets))
     graphs = {}
 
     def graph_for(n):
@@ -263,7 +286,7 @@ def run_gpu(args):
             graphs[n] = g
         return graphs[n]
 
-    full, rem = divmod(args.steps, G)
+    full, rem = divmod(steps, G)
     plan = [G] * full + ([rem] if rem else [])
     with torch.cuda.stream(stream):
         for n in set(plan):
@@ -291,7 +314,7 @@ def run_gpu(args):
             for n in plan:
                 graphs[n].replay()
 
-    with ClockSampler(local) as clk:
+    with ClockSampler(dev.index) as clk:
         ms = timed(replay_all)
     clocks = clk.summary()
 
@@ -302,7 +325,7 @@ def run_gpu(args):
 
     # ---- end to end: inputs from pinned host memory, results back to host
     e2e = None
-    if not args.no_e2e:
+    if e2e_steps > 0:
         host = []
         for p in pool[:2]:
             hp = {}
@@ -323,9 +346,9 @@ def run_gpu(args):
         h2d = sum(t.numel() * t.element_size() for t in host[0].values())
         d2h = sum(t.numel() * t.element_size() for t in r_host.values())
         out0 = outs[0]
-        n_e2e = max(1, min(args.steps, args.e2e_steps))
+        n_e2e = max(1, e2e_steps)
 
-        def e2e_steps():
+        def e2e_run():
             for i in range(n_e2e):
                 hp = host[i % 2]
                 for k, t in hp.items():
@@ -341,46 +364,106 @@ def run_gpu(args):
                     t.copy_(getattr(out0, k), non_blocking=True)
 
         with torch.cuda.stream(stream):
-            e2e_steps()
-            ms_e2e = timed(e2e_steps)
+            e2e_run()
+            ms_e2e = timed(e2e_run)
         e2e = {"value": ws_n * n_e2e / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e}
 
+    # one round of set 0 with its first seed: the CPU baseline's oracle sample
+    # runs on the same inputs, and its outputs are compared with these
+    with torch.cuda.stream(stream):
+        so = sd.verify(one.target, one.draft, one.tokens, one.temperature, one.seed,
+                       row_base=one.meta["row_base"], fanout=fan, draft_bonus=one.draft_bonus,
+                       compact=True, ws=wss, stream=stream)
+    torch.cuda.synchronize(dev)
+    sample = {k: getattr(so, k).cpu().numpy() for k in ("num_accepted", "out_tokens", "tau",
+                                                        "hit") if getattr(so, k) is not None}
+    if fan is not None:
+        sample["keys"] = so.keys.cpu().numpy()
+    alg = algorithmic_bytes(one)
+    formula = W.logit_bytes(one, algorithmic=False, with_bonus=fan is not None)
+    return dict(name=name, ms=ms, steps=steps, clocks=clocks, e2e=e2e, hit_rate=hit_rate,
+                mean_tau=mean_tau, status=st, n_launch=n_launch, plan=plan_name, alg=alg,
+                formula=formula, l2=l2, B=B, K=K, dtype=one.meta["dtype"], sample=sample)
+
+
+def run_gpu(args):
+    import speculative_decoding_verification_logits_gb300 as sd
+
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sd.lib()
+    name = args.workload
+    m = measure(name, args.steps, args.warmup, dev, rank, ws_n,
+                e2e_steps=0 if args.no_e2e else min(args.steps, args.e2e_steps))
+    # every BASELINE config measured in the same run (the default run only)
+    per = {}
+    if name == HEADLINE and not args.no_per_config:
+        for c in CONFIGS:
+            per[c] = m if c == name else measure(c, max(args.steps, args.config_steps),
+                                                 args.warmup, dev, rank, ws_n)
     if ws_n > 1:
         torch.distributed.destroy_process_group()
     if rank != 0:
         return None
 
-    steps = args.steps
-    per_launch_ms = ms / steps
-    alg = algorithmic_bytes(one)
-    formula = W.logit_bytes(one, algorithmic=False, with_bonus=fan is not None)
     pk, pk_kind = peaks()
-    achieved = alg / (per_launch_ms / 1e3) / 1e9
-    traffic = profiled_traffic(name)
+
+    def roofline(mx):
+        per_launch_ms = mx["ms"] / mx["steps"]
+        achieved = mx["alg"] / (per_launch_ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_source": pk_kind,
+                "kernel": "verify step: all launches of one round (duration = step time)",
+                "algorithmic_bytes_per_launch": mx["alg"],
+                "formula_bytes_per_launch": mx["formula"]}
+
+    rl = roofline(m)
+    rl["traffic"] = profiled_traffic(name)
     line = {
-        "metric": METRIC, "value": ws_n * steps / (ms / 1e3), "unit": UNIT, "n_gpus": ws_n,
-        "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": one.meta["dtype"],
+        "metric": METRIC, "value": ws_n * m["steps"] / (m["ms"] / 1e3), "unit": UNIT,
+        "n_gpus": ws_n, "steps": m["steps"], "warmup": args.warmup,
+        "ms_per_step": m["ms"] / m["steps"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": m["dtype"],
         "data": "synthetic (seeded logits shaped like the workload; draft tokens drawn from q)",
-        "config": {"workload": describe(name), "global_batch": B * ws_n, "seq_len": K + 1,
-                   "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU",
-                   "l2": f"rotating {n_sets} input sets ({n_sets * set_bytes / 1e6:.0f} MB, "
-                         f"> 4x L2 {l2 / 1e6:.0f} MB)"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                     "peak_source": pk_kind,
-                     "kernel": "verify step: all launches of one round (duration = step time)",
-                     "algorithmic_bytes_per_launch": alg, "formula_bytes_per_launch": formula},
-        # per step: the cluster kernel and the packing launch, or the streaming
-        # grid, the finish and the packing launch (split launch)
-        "gpu_launches": n_launch * steps,
-        "clocks": clocks,
-        "e2e": e2e,
-        "hit_rate": hit_rate, "mean_tau": mean_tau, "status_bits": st,
+        "config": config_of(name, ws_n, m["l2"]),
+        "roofline": rl,
+        # per step: the streaming grid, the finish and the packing launch
+        # (split launch), or the cluster kernel and the packing launch
+        "gpu_launches": m["n_launch"] * m["steps"],
+        "clocks": m["clocks"],
+        "e2e": m["e2e"],
+        "hit_rate": m["hit_rate"], "mean_tau": m["mean_tau"], "status_bits": m["status"],
+        "launch_plan": m["plan"],
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(name, args.cpu_seconds)
+        line["cpu_baseline"], line["parity_sample"] = cpu_baseline(name, args.cpu_seconds,
+                                                                   m["sample"])
+    if per:
+        pc = {}
+        for i, c in enumerate(CONFIGS):
+            mc = per[c]
+            r = roofline(mc)
+            e = {"config": i + 1, "workload": describe(c),
+                 "rounds_per_s": ws_n * mc["steps"] / (mc["ms"] / 1e3),
+                 "ms_per_step": mc["ms"] / mc["steps"], "steps": mc["steps"],
+                 "algorithmic_gbs": r["achieved"], "frac": r["frac"],
+                 "algorithmic_bytes_per_step": mc["alg"], "launch_plan": mc["plan"],
+                 "gpu_launches_per_step": mc["n_launch"], "clocks": mc["clocks"],
+                 "mean_tau": mc["mean_tau"], "hit_rate": mc["hit_rate"],
+                 "status_bits": mc["status"]}
+            if not args.no_cpu_baseline:
+                if c == name:
+                    cb, ps = line["cpu_baseline"], line["parity_sample"]
+                else:
+                    cb, ps = cpu_baseline(c, args.config_cpu_seconds, mc["sample"])
+                e["cpu_baseline"], e["parity_sample"] = cb, ps
+            pc[c] = e
+        line["per_config"] = pc
     return line
 
 
@@ -529,6 +612,7 @@ def _oracle_round(inp: W.Inputs, rows, threads):
     with ThreadPoolExecutor(threads) as ex:
         pairs = list(ex.map(one, rows))
     res = [r for r, _ in pairs]
+    keys = [k for _, k in pairs]
     out = np.concatenate([r["out_tokens"] for r in res])
     tau = np.concatenate([r["tau"] for r in res])
     oracle.compact(out, tau)
@@ -540,27 +624,93 @@ def _oracle_round(inp: W.Inputs, rows, threads):
         oracle.kv_rollback(inp.meta["block_table"].cpu().numpy()[idx],
                            inp.meta["kv_len"].cpu().numpy()[idx], tau,
                            inp.meta["page_size"], inp.K + 1)
-    return res
+    return res, keys
 
 
-def cpu_baseline(name, seconds):
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or ''."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "hardware")):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return ""
+
+
+def _parity(res, keys, inp, gpu):
+    """Row-by-row comparison of the oracle's results (rows 0..B-1 of the
+    round, in order) with the GPU's for the same inputs: exact outside the
+    guard band; guarded rows counted."""
+    B, K = inp.B, inp.K
+    temps = inp.temperature.cpu().numpy()
+    c = dict(rows=B, positions=B * max(K, 1), sampled=0, guarded=0, guarded_mismatch=0,
+             mismatch_outside_guard=0, keys_mismatch=0)
+    for b in range(B):
+        o = res[b]
+        same = (int(o["tau"][0]) == int(gpu["tau"][b])
+                and int(o["num_accepted"][0]) == int(gpu["num_accepted"][b])
+                and np.array_equal(o["out_tokens"][0], gpu["out_tokens"][b]))
+        if "hit" in gpu and inp.fanout is not None:
+            same = same and int(o["hit"][0]) == int(gpu["hit"][b])
+        sampled = temps[b] > 0
+        c["sampled"] += int(sampled)
+        guarded = sampled and int(o["guard_pos"][0]) >= 0
+        c["guarded"] += int(guarded)
+        if not same:
+            c["guarded_mismatch" if guarded else "mismatch_outside_guard"] += 1
+        if keys[b] is not None and "keys" in gpu:
+            c["keys_mismatch"] += int(not np.array_equal(keys[b][0], gpu["keys"][b]))
+    return c
+
+
+def cpu_baseline(name, seconds, gpu_sample=None):
+    """The oracle on a bounded sample of round 0 of the workload, on this
+    host's cores (the reported CPU baseline).  The first pass runs every row
+    of the round once, and its results are compared with the GPU's for the
+    same inputs (`gpu_sample`), giving the parity counts."""
     import oracle
     oracle.build()
     cores = os.cpu_count() or 1
-    inp = W.workload(name, round_idx=0, device="cpu")
+    # the GPU's inputs (drawn on the device: its generator differs from the
+    # host's), copied to the host by the oracle's marshalling
+    dev = torch.device("cuda", torch.cuda.current_device()) if gpu_sample is not None else "cpu"
+    inp = W.workload(name, round_idx=0, device=dev)
     B = inp.B
-    # calibrate on one row, then size the sample to ~`seconds` of wall time
+    # calibrate on one row (single thread), then size the sample to about
+    # `seconds` of wall time on all cores, at least one pass over the round
     t0 = time.perf_counter()
     _oracle_round(inp, [0], 1)
     per_row = time.perf_counter() - t0
-    n_rows = int(max(1, min(B * 50, seconds * cores / max(per_row, 1e-6))))
+    n_rows = int(max(B, min(B * 50, seconds * cores / max(per_row, 1e-6))))
     rows = [i % B for i in range(n_rows)]
     t0 = time.perf_counter()
-    _oracle_round(inp, rows, cores)
+    res, keys = _oracle_round(inp, rows, cores)
     dt = time.perf_counter() - t0
-    return {"value": (n_rows / B) / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n_rows} rows ({n_rows / B:.2f} rounds) of {name}, one row per oracle "
-                      f"call, {cores} threads; single-thread {per_row * 1e3:.1f} ms/row"}
+    cb = {"value": (n_rows / B) / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+          "cpu": cpu_model(), "single_thread_ms_per_round": per_row * B * 1e3,
+          "sample": f"{n_rows} rows ({n_rows / B:.2f} rounds) of {name}, one row per oracle "
+                    f"call, {cores} threads; single-thread {per_row * 1e3:.1f} ms/row"}
+    ps = _parity(res[:B], keys[:B], inp, gpu_sample) if gpu_sample is not None else None
+    return cb, ps
+
+
+def _l2_bytes():
+    """L2 size of GPU 0 when one is visible (it names the rotation in
+    `config`), else 0."""
+    try:
+        if torch.cuda.is_available():
+            return torch.cuda.get_device_properties(0).L2_cache_size
+    except Exception:
+        pass
+    return 0
 
 
 def run_reference(args):
@@ -611,9 +761,10 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws_n,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": describe(name), "global_batch": B},
+            "data": "synthetic", "config": config_of(name, ws_n, _l2_bytes()),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "cpu": cpu_model(), "sample": sample,
+                             "single_thread_ms_per_round": per_row * B * 1e3},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -628,6 +779,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure the headline workload only (no per_config object)")
+    ap.add_argument("--config-steps", type=int, default=500,
+                    help="timed steps of each config in per_config (at least --steps)")
+    ap.add_argument("--config-cpu-seconds", type=float, default=4.0,
+                    help="oracle sample time of each config in per_config")
     args = ap.parse_args()
     if args.impl == "reference":
         line = run_reference(args)

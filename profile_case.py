@@ -1,6 +1,6 @@
 """Run a few verify rounds of one synthetic workload (for profilers).
 
-    python -m speculative_decoding_verification_logits_gb300.profile_case WORKLOAD [ROUNDS]
+    python profile_case.py WORKLOAD [ROUNDS]
 
 Two input sets of the workload alternate; every round is the verify step
 (plus the packing launch, and for the D3D workload the drafter pack and the
@@ -9,7 +9,7 @@ KV rollback).  Prints the mean tau of the last round.
 import os
 import sys
 
-sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
 
 import torch  # noqa: E402
 

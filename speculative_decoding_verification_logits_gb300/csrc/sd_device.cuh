@@ -171,6 +171,14 @@ __device__ __forceinline__ bool ff_gt(ff x, ff y) {
 }
 __device__ __forceinline__ bool ff_pos(ff x) { return x.hi > 0.f; }
 __device__ __forceinline__ float ff_f(ff x) { return x.hi + x.lo; }
+// a / b for float-float a, b > 0, rounded to float: one correction step on
+// the float quotient with the remainder carried exactly (within an ulp).
+__device__ __forceinline__ float ff_ratio(ff a, ff b) {
+  const float q0 = __fdiv_rn(a.hi, b.hi);
+  const ff p = two_prod(q0, b.hi);
+  const float r = ((a.hi - p.hi) - p.lo) + fmaf(-q0, b.lo, a.lo);
+  return q0 + __fdiv_rn(r, b.hi);
+}
 __device__ __forceinline__ ff ff_shfl(ff x, int src) {
   __syncwarp();
   return ff{__shfl_sync(0xffffffffu, x.hi, src), __shfl_sync(0xffffffffu, x.lo, src)};
@@ -268,6 +276,11 @@ __device__ __forceinline__ void upk2(uint64_t r, float &lo, float &hi) {
 __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
@@ -633,11 +646,14 @@ __device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
 
 // Weights of the sampling pass for the elements of one target vector, two
 // lanes per instruction: the residual Zt (p - q)+ =
-// max(0, 2^(l s + Ct) - 2^(l' s + Cd + log2 R)) with R = Zt / Zd (cd2 holds
-// Cd + log2 R), or Zt p = 2^(l s + Ct) for a draw from p.
+// max(0, 2^(l s + Ct) - R 2^(l' s + Cd)) with R = Zt / Zd (r2 holds R, cd2
+// Cd), or Zt p = 2^(l s + Ct) for a draw from p.  R is applied as a product
+// rather than folded into the exponent, which would add the error of a
+// hardware log2 to every draft weight.
 template <typename E>
 __device__ __forceinline__ void pass_weights(const uint4 &tv, const uint4 &dv, bool residual,
-                                             uint64_t s2, uint64_t ct2, uint64_t cd2, float *w) {
+                                             uint64_t s2, uint64_t ct2, uint64_t cd2, uint64_t r2,
+                                             float *w) {
   constexpr int N = Elt<E>::kPerVec;
   float ft[N], fd[N];
   Elt<E>::unpack(tv, ft);
@@ -650,7 +666,7 @@ __device__ __forceinline__ void pass_weights(const uint4 &tv, const uint4 &dv, b
     if (residual) {
       float c, d;
       upk2(fma2(pk2(fd[i], fd[i + 1]), s2, cd2), c, d);
-      p = sub2(p, pk2(ex2(c), ex2(d)));
+      p = sub2(p, mul2(pk2(ex2(c), ex2(d)), r2));
     }
     upk2(p, w[i], w[i + 1]);
     if (residual) {
@@ -663,10 +679,10 @@ __device__ __forceinline__ void pass_weights(const uint4 &tv, const uint4 &dv, b
 // Mass of one target vector in the sampling pass (sum of its weights).
 template <typename E>
 __device__ __forceinline__ float vec_mass(const uint4 &tv, const uint4 &dv, bool residual,
-                                          uint64_t s2, uint64_t ct2, uint64_t cd2) {
+                                          uint64_t s2, uint64_t ct2, uint64_t cd2, uint64_t r2) {
   constexpr int N = Elt<E>::kPerVec;
   float w[N];
-  pass_weights<E>(tv, dv, residual, s2, ct2, cd2, w);
+  pass_weights<E>(tv, dv, residual, s2, ct2, cd2, r2, w);
   uint64_t acc = pk2(w[0], w[1]);
 #pragma unroll
   for (int i = 2; i < N; i += 2) acc = add2(acc, pk2(w[i], w[i + 1]));
@@ -1442,7 +1458,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
           const float zt = ff_f(S.Z[rt]), zd = ff_f(S.Z[rd]);
           const float r = (ldr == -INFINITY)
                               ? INFINITY  // q(d) = 0
-                              : exp2_ff(ff_sub(xt, xd)) * __fdiv_rn(zd, zt);
+                              : exp2_ff(ff_sub(xt, xd)) * ff_ratio(S.Z[rd], S.Z[rt]);
           const float u = S.u_acc[j];
           a = (u <= r) ? 1 : 0;
           if (rank == 0) {
@@ -1504,11 +1520,9 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
       }
       const float Ct = S.C[S.trow[mm]];
       const float Cd = residual ? S.C[S.drow[mm]] : 0.f;
-      const float Rz =
-          residual ? __fdiv_rn(ff_f(S.Z[S.trow[mm]]), ff_f(S.Z[S.drow[mm]])) : 0.f;
+      const float Rz = residual ? ff_ratio(S.Z[S.trow[mm]], S.Z[S.drow[mm]]) : 0.f;
       const uint64_t s2 = pk2(s, s), ct2 = pk2(Ct, Ct);
-      const float cdr = residual ? Cd + __log2f(Rz) : 0.f;  // the draft weight scaled by R
-      const uint64_t cd2 = pk2(cdr, cdr);
+      const uint64_t cd2 = pk2(Cd, Cd), r2 = pk2(Rz, Rz);  // draft weights times R
       const int wr = (Rt.nvec + NW - 1) / NW;  // vectors per warp
       const int wq0 = min(warp * wr, Rt.nvec), wq1 = min(wq0 + wr, Rt.nvec);
       const int wsteps = (wq1 - wq0 + 2 * 32 - 1) / (2 * 32);
@@ -1560,7 +1574,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
                 dv = d_vec ? load_vec_slow<E>(*Rd, q, v0, v1) : tv;
               }
               if (residual && !d_vec) dv = load_vec_slow<E>(Rdt, q, v0, v1);
-              ms += vec_mass<E>(tv, dv, residual, s2, ct2, cd2);
+              ms += vec_mass<E>(tv, dv, residual, s2, ct2, cd2, r2);
             }
           }
           pmw[u * 32 + lane] = ms;
@@ -1688,7 +1702,7 @@ __global__ void __launch_bounds__(NT, 2) sd_seq_kernel(const __grid_constant__ P
               if (residual)
                 dvv = d_vec ? load_vec_direct<E>(*Rd, q, v0, v1) : load_vec_slow<E>(Rdt, q, v0, v1);
               float ww[NV];
-              pass_weights<E>(tvv, dvv, residual, s2, ct2, cd2, ww);
+              pass_weights<E>(tvv, dvv, residual, s2, ct2, cd2, r2, ww);
               float wi = 0.f;
 #pragma unroll
               for (int ii = 0; ii < NV; ++ii)

@@ -367,7 +367,8 @@ static __device__ void fin_outputs(const Params &P, const FinS &S, int b, bool t
 template <typename E>
 __device__ __noinline__ ff draw_pass(const RowInfo &Rt, const RowInfo &Rd, const RowInfo &Rdt,
                                      bool residual, bool d_vec, int wq0, int wq1, int v0, int v1,
-                                     uint64_t s2, uint64_t ct2, uint64_t cd2, float *pmw) {
+                                     uint64_t s2, uint64_t ct2, uint64_t cd2, uint64_t r2,
+                                     float *pmw) {
   const int lane = threadIdx.x & 31;
   const int nit = (wq1 - wq0 + 31) / 32;
   const uint32_t ni = Elt<E>::kNegInfWord;
@@ -379,7 +380,7 @@ __device__ __noinline__ ff draw_pass(const RowInfo &Rt, const RowInfo &Rd, const
       float ms = 0.f;
       if (q < wq1)
         ms = vec_mass<E>(load_vec_direct<E>(Rt, q, v0, v1), load_vec_slow<E>(Rdt, q, v0, v1), true,
-                         s2, ct2, cd2);
+                         s2, ct2, cd2, r2);
       pmw[it * 32 + lane] = ms;
       kahan_add(tsum, tcomp, ms);
     }
@@ -403,7 +404,7 @@ __device__ __noinline__ ff draw_pass(const RowInfo &Rt, const RowInfo &Rd, const
 #pragma unroll
     for (int c = 0; c < kFinCH; ++c) {
       if (it0 + c < nit) {
-        const float ms = vec_mass<E>(tv[c], dv[c], residual, s2, ct2, cd2);
+        const float ms = vec_mass<E>(tv[c], dv[c], residual, s2, ct2, cd2, r2);
         pmw[(it0 + c) * 32 + lane] = ms;
         kahan_add(tsum, tcomp, ms);
       }
@@ -418,7 +419,7 @@ __device__ __noinline__ ff draw_pass(const RowInfo &Rt, const RowInfo &Rd, const
     if (((q - wq0) & 31) == lane) {
       const uint4 tvv = load_vec_slow<E>(Rt, q, v0, v1);
       const uint4 dvv = residual ? load_vec_slow<E>(Rd, q, v0, v1) : tvv;
-      const float ms = vec_mass<E>(tvv, dvv, residual, s2, ct2, cd2);
+      const float ms = vec_mass<E>(tvv, dvv, residual, s2, ct2, cd2, r2);
       pmw[((q - wq0) >> 5) * 32 + lane] = ms;
       kahan_add(tsum, tcomp, ms);
     }
@@ -571,7 +572,7 @@ __global__ void __launch_bounds__(kFinNT, 2) sd_finish_kernel(const __grid_const
         const ff xd = ff_add_f(two_prod(ldr, s), S.C[rd]);
         const float zt = ff_f(S.Z[j]), zd = ff_f(S.Z[rd]);
         const float r = (ldr == -INFINITY) ? INFINITY  // q(d) = 0
-                                           : exp2_ff(ff_sub(xt, xd)) * __fdiv_rn(zd, zt);
+                                           : exp2_ff(ff_sub(xt, xd)) * ff_ratio(S.Z[rd], S.Z[j]);
         a = (S.u_acc[j] <= r) ? 1 : 0;
         if (rank == 0) {
           const int64_t pj = (int64_t)b * K + j;
@@ -682,15 +683,15 @@ __global__ void __launch_bounds__(kFinNT, 2) sd_finish_kernel(const __grid_const
     const RowInfo &Rdt = S.ddt;  // otherwise: element-wise on the target's grid
     const float Ct = S.C[mm];
     const float Cd = residual ? S.C[K + 1 + mm] : 0.f;
-    const float Rz = residual ? __fdiv_rn(ff_f(S.Z[mm]), ff_f(S.Z[K + 1 + mm])) : 0.f;
+    const float Rz = residual ? ff_ratio(S.Z[mm], S.Z[K + 1 + mm]) : 0.f;
     const uint64_t s2 = pk2(s, s), ct2 = pk2(Ct, Ct);
-    const float cdr = residual ? Cd + __log2f(Rz) : 0.f;  // the draft weight scaled by R
-    const uint64_t cd2 = pk2(cdr, cdr);
+    const uint64_t cd2 = pk2(Cd, Cd), r2 = pk2(Rz, Rz);  // draft weights times R
     const int nvec = Rt.nvec;
     const int wr = (nvec + NW - 1) / NW;  // vectors per warp
     const int wq0 = min(warp * wr, nvec), wq1 = min(wq0 + wr, nvec);
     float *pmw = pm + warp * P.pw * 32;  // [iteration][lane] masses of this warp
-    const ff lm = draw_pass<E>(Rt, S.dd, Rdt, residual, d_vec, wq0, wq1, v0, v1, s2, ct2, cd2, pmw);
+    const ff lm =
+        draw_pass<E>(Rt, S.dd, Rdt, residual, d_vec, wq0, wq1, v0, v1, s2, ct2, cd2, r2, pmw);
     const ff wm = ff_warp_sum(lm);
     if (lane == 0) S.wmass[warp] = wm;
     __syncthreads();
@@ -773,7 +774,7 @@ __global__ void __launch_bounds__(kFinNT, 2) sd_finish_kernel(const __grid_const
             if (residual)
               dvv = d_vec ? load_vec_direct<E>(S.dd, q, v0, v1) : load_vec_slow<E>(Rdt, q, v0, v1);
             float ww[NV];
-            pass_weights<E>(tvv, dvv, residual, s2, ct2, cd2, ww);
+            pass_weights<E>(tvv, dvv, residual, s2, ct2, cd2, r2, ww);
             float wi = 0.f;
 #pragma unroll
             for (int ii = 0; ii < NV; ++ii)
