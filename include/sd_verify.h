@@ -234,6 +234,65 @@ sd_status_t sd_outcome_predict(int32_t B, int32_t K, int32_t V, sd_dtype_t dtype
                                void *stream);
 
 /*
+ * Vocabulary-sharded verify ("Speculative Speculative Decoding" blog
+ * (jiwasawa.github.io), performance and hardware: the target runs on four
+ * GPUs, so its logits arrive split over the vocabulary).  S shards cover
+ * [0, V) in order; shard `shard` holds columns [v0, v0 + vs) of every logit
+ * row: target [B][K+1][vs], draft [B][K][vs], bonus draft [B][vs], each
+ * contiguous, on its own device (or all on one device).  The step runs in
+ * three calls per shard with an exchange between them:
+ *   sd_vshard_stats  -> stats block of this shard (sd_vshard_stats_bytes);
+ *                       all-gather the S blocks, in shard order, into
+ *                       stats_all;
+ *   sd_vshard_mass   -> this shard's mass block (sd_vshard_mass_bytes):
+ *                       every shard combines all rows' statistics and takes
+ *                       the same accept decisions, then measures its own
+ *                       columns' share of the draw; all-gather into mass_all;
+ *   sd_vshard_pick   -> outputs: the prefix over the shards' masses names the
+ *                       shard holding u * S, which alone scans its columns
+ *                       (a two-level inverse CDF) and writes the token and the
+ *                       hit flag of a sampled row; every shard writes the
+ *                       rest, which is the same everywhere.
+ * Pre-fill out_tokens with -1 and hit with 0: an element-wise maximum over
+ * the shards' outputs (an all-reduce, or on one device running the shards'
+ * picks on the same output arrays) completes them.  The results are those of
+ * sd_verify on the unsharded logits (num_accepted, out_tokens, tau, hit,
+ * keys_out with SD_FLAG_PREDICT), with the same uniforms.  Flags:
+ * SD_FLAG_PREDICT (fanout_host, draft_bonus_logits, keys_out),
+ * SD_FLAG_CHECK_FINITE.  1 <= S <= 32.  Buffers are caller-owned device
+ * memory, 16-byte aligned; nothing in them needs clearing.
+ */
+typedef struct sd_vshard_args {
+  int32_t B, K, V;             /* batch, drafts, full vocabulary              */
+  int32_t S, shard;            /* shard count, this shard                     */
+  int32_t v0, vs;              /* this shard's columns [v0, v0 + vs)           */
+  sd_dtype_t dtype;
+  uint32_t flags;
+  uint64_t seed;
+  int64_t row_base;
+  const void *target_logits;   /* [B][K+1][vs]                                */
+  const void *draft_logits;    /* [B][K][vs]                                  */
+  const int32_t *draft_tokens; /* [B][K], vocabulary ids                      */
+  const float *temperature;    /* [B]                                          */
+  const int32_t *fanout_host;  /* [K+1] (host), with SD_FLAG_PREDICT          */
+  const void *draft_bonus_logits; /* [B][vs] or NULL                          */
+  int32_t *keys_out;           /* [B][sum(fanout)][2] (pick)                  */
+  int32_t *num_accepted;       /* [B] (pick)                                  */
+  int32_t *out_tokens;         /* [B][K+1] (pick), pre-filled with -1        */
+  int32_t *tau;                /* [B] (pick)                                  */
+  uint8_t *hit;                /* [B] or NULL (pick), pre-filled with 0       */
+  int32_t *status;             /* one int32 or NULL                           */
+} sd_vshard_args;
+
+size_t sd_vshard_stats_bytes(int32_t B, int32_t K);
+size_t sd_vshard_mass_bytes(int32_t B);
+sd_status_t sd_vshard_stats(const sd_vshard_args *args, void *stats, void *stream);
+sd_status_t sd_vshard_mass(const sd_vshard_args *args, const void *stats_all, void *mass,
+                           void *stream);
+sd_status_t sd_vshard_pick(const sd_vshard_args *args, const void *stats_all,
+                           const void *mass_all, void *stream);
+
+/*
  * The drafter's next pass, packed from the outcome keys ("LLMの生成を5倍速く
  * する「D3D」を図で読む" (animemo.app), sections 答え:ありうる結果すべてに、
  * 先回りして下書きする and パック:24ブロックを1回の計算で).  A block is K+1

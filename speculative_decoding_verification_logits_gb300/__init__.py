@@ -49,6 +49,20 @@ class VerifyArgs(ctypes.Structure):
     ]
 
 
+class VShardArgs(ctypes.Structure):
+    """Mirror of ``sd_vshard_args`` in include/sd_verify.h."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("K", ctypes.c_int32), ("V", ctypes.c_int32),
+        ("S", ctypes.c_int32), ("shard", ctypes.c_int32), ("v0", ctypes.c_int32),
+        ("vs", ctypes.c_int32), ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32),
+        ("seed", ctypes.c_uint64), ("row_base", ctypes.c_int64),
+        ("target_logits", _P), ("draft_logits", _P), ("draft_tokens", _P),
+        ("temperature", _P), ("fanout_host", _P), ("draft_bonus_logits", _P),
+        ("keys_out", _P), ("num_accepted", _P), ("out_tokens", _P), ("tau", _P),
+        ("hit", _P), ("status", _P),
+    ]
+
+
 _lib = None
 _lib_lock = threading.Lock()
 
@@ -87,6 +101,16 @@ def lib():
             L.sd_kv_rollback.restype = ctypes.c_int
             L.sd_uniforms.argtypes = [u64, i32, _P, _P, _P, _P, _P]
             L.sd_uniforms.restype = ctypes.c_int
+            L.sd_vshard_stats_bytes.argtypes = [i32, i32]
+            L.sd_vshard_stats_bytes.restype = sz
+            L.sd_vshard_mass_bytes.argtypes = [i32]
+            L.sd_vshard_mass_bytes.restype = sz
+            L.sd_vshard_stats.argtypes = [ctypes.POINTER(VShardArgs), _P, _P]
+            L.sd_vshard_stats.restype = ctypes.c_int
+            L.sd_vshard_mass.argtypes = [ctypes.POINTER(VShardArgs), _P, _P, _P]
+            L.sd_vshard_mass.restype = ctypes.c_int
+            L.sd_vshard_pick.argtypes = [ctypes.POINTER(VShardArgs), _P, _P, _P]
+            L.sd_vshard_pick.restype = ctypes.c_int
             L.sd_verify_args_size.argtypes = []
             L.sd_verify_args_size.restype = sz
             if L.sd_verify_args_size() != ctypes.sizeof(VerifyArgs):
@@ -390,6 +414,185 @@ def uniforms(seed: int, row, pos, slot, *, stream=None) -> torch.Tensor:
     out = torch.empty(row.shape, dtype=torch.float64, device=dev)
     _check(lib().sd_uniforms(int(seed) & (2 ** 64 - 1), row.numel(), _ptr(row), _ptr(pos),
                              _ptr(slot), _ptr(out), _stream(dev, stream)), "sd_uniforms")
+    return out
+
+
+# ------------------------------------------------ vocabulary-sharded verify --
+def vshard_bounds(V: int, S: int):
+    """Even split of [0, V) into S shards in order: list of (v0, vs)."""
+    base, extra = divmod(V, S)
+    out, v0 = [], 0
+    for s in range(S):
+        vs = base + (1 if s < extra else 0)
+        out.append((v0, vs))
+        v0 += vs
+    return out
+
+
+def _vshard_args(target_s, draft_s, tokens, temperature, seed, *, S, shard, v0, V, row_base,
+                 fanout, draft_bonus_s, check_finite, out, status, fan_arr):
+    B, K1, vs = target_s.shape
+    K = K1 - 1
+    a = VShardArgs()
+    a.B, a.K, a.V, a.S, a.shard, a.v0, a.vs = B, K, V, S, shard, v0, vs
+    a.dtype = _dtype_code(target_s)
+    a.flags = (SD_FLAG_PREDICT if fanout is not None else 0) | (
+        SD_FLAG_CHECK_FINITE if check_finite else 0)
+    a.seed, a.row_base = int(seed) & (2 ** 64 - 1), int(row_base)
+    a.target_logits = target_s.data_ptr()
+    a.draft_logits = draft_s.data_ptr() if K > 0 else None
+    a.draft_tokens = tokens.data_ptr() if K > 0 else None
+    a.temperature = temperature.data_ptr()
+    if fan_arr is not None:
+        a.fanout_host = ctypes.cast(fan_arr, ctypes.c_void_p)
+        a.draft_bonus_logits = draft_bonus_s.data_ptr() if draft_bonus_s is not None else None
+    if out is not None:
+        a.keys_out = out.keys.data_ptr() if out.keys is not None else None
+        a.num_accepted, a.out_tokens, a.tau = (out.num_accepted.data_ptr(),
+                                              out.out_tokens.data_ptr(), out.tau.data_ptr())
+        a.hit = out.hit.data_ptr() if out.hit is not None else None
+    a.status = status.data_ptr() if status is not None else None
+    return a
+
+
+def vshard_stats(target_s, draft_s, tokens, temperature, seed, *, S, shard, v0, V, row_base=0,
+                 fanout=None, draft_bonus_s=None, check_finite=False, stats=None, stream=None):
+    """sd_vshard_stats: this shard's stats block (uint8 tensor)."""
+    _need(target_s, "target_s")
+    dev = target_s.device
+    B, K1, vs = target_s.shape
+    K = K1 - 1
+    if K > 0:
+        _need(draft_s, "draft_s", target_s.dtype, (B, K, vs), dev)
+        _need(tokens, "tokens", torch.int32, (B, K), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    fan_arr = None
+    if fanout is not None:
+        fan_arr = (ctypes.c_int32 * (K + 1))(*[int(f) for f in fanout])
+        if draft_bonus_s is not None:
+            _need(draft_bonus_s, "draft_bonus_s", target_s.dtype, (B, vs), dev)
+    n = int(lib().sd_vshard_stats_bytes(B, K))
+    if stats is None:
+        stats = torch.empty(n, dtype=torch.uint8, device=dev)
+    a = _vshard_args(target_s, draft_s, tokens, temperature, seed, S=S, shard=shard, v0=v0, V=V,
+                     row_base=row_base, fanout=fanout, draft_bonus_s=draft_bonus_s,
+                     check_finite=check_finite, out=None, status=None, fan_arr=fan_arr)
+    _check(lib().sd_vshard_stats(ctypes.byref(a), _ptr(stats), _stream(dev, stream)),
+           "sd_vshard_stats")
+    return stats
+
+
+def vshard_mass(target_s, draft_s, tokens, temperature, seed, stats_all, *, S, shard, v0, V,
+                row_base=0, fanout=None, draft_bonus_s=None, check_finite=False, mass=None,
+                stream=None):
+    """sd_vshard_mass: this shard's mass block (uint8 tensor) from all
+    shards' stats blocks (stats_all: S blocks in shard order)."""
+    dev = target_s.device
+    B, K1, _ = target_s.shape
+    K = K1 - 1
+    fan_arr = (ctypes.c_int32 * (K + 1))(*[int(f) for f in fanout]) if fanout is not None else None
+    if mass is None:
+        mass = torch.empty(int(lib().sd_vshard_mass_bytes(B)), dtype=torch.uint8, device=dev)
+    a = _vshard_args(target_s, draft_s, tokens, temperature, seed, S=S, shard=shard, v0=v0, V=V,
+                     row_base=row_base, fanout=fanout, draft_bonus_s=draft_bonus_s,
+                     check_finite=check_finite, out=None, status=None, fan_arr=fan_arr)
+    _check(lib().sd_vshard_mass(ctypes.byref(a), _ptr(stats_all), _ptr(mass),
+                                _stream(dev, stream)), "sd_vshard_mass")
+    return mass
+
+
+def vshard_pick(target_s, draft_s, tokens, temperature, seed, stats_all, mass_all, out, *, S,
+                shard, v0, V, row_base=0, fanout=None, draft_bonus_s=None, check_finite=False,
+                stream=None):
+    """sd_vshard_pick into `out` (a VerifyResult whose out_tokens start at -1
+    and hit at 0)."""
+    dev = target_s.device
+    K = target_s.shape[1] - 1
+    fan_arr = (ctypes.c_int32 * (K + 1))(*[int(f) for f in fanout]) if fanout is not None else None
+    a = _vshard_args(target_s, draft_s, tokens, temperature, seed, S=S, shard=shard, v0=v0, V=V,
+                     row_base=row_base, fanout=fanout, draft_bonus_s=draft_bonus_s,
+                     check_finite=check_finite, out=out, status=out.status, fan_arr=fan_arr)
+    _check(lib().sd_vshard_pick(ctypes.byref(a), _ptr(stats_all), _ptr(mass_all),
+                                _stream(dev, stream)), "sd_vshard_pick")
+    return out
+
+
+def _vshard_out(B, K, device, n_keys):
+    r = alloc_outputs(B, K, device, hit=True, n_keys=n_keys)
+    r.out_tokens.fill_(-1)
+    r.hit.fill_(0)
+    return r
+
+
+def verify_vsharded(targets, drafts, tokens, temperature, seed, *, V, fanout=None,
+                    draft_bonus=None, check_finite=False, row_base=0, stream=None):
+    """The sharded verify on one device: targets / drafts / draft_bonus are
+    lists of the S shards' column blocks ([B][K+1][vs_s] ...) in vocabulary
+    order.  The exchanges are the stats and mass blocks laid side by side,
+    and the shards' picks writing one set of outputs."""
+    S = len(targets)
+    B, K1, _ = targets[0].shape
+    K = K1 - 1
+    dev = targets[0].device
+    v0s = [0]
+    for t in targets[:-1]:
+        v0s.append(v0s[-1] + t.shape[2])
+    if v0s[-1] + targets[-1].shape[2] != V:
+        raise ValueError("the shards must cover [0, V) in order")
+    nst = int(lib().sd_vshard_stats_bytes(B, K))
+    nma = int(lib().sd_vshard_mass_bytes(B))
+    stats_all = torch.empty(S * nst, dtype=torch.uint8, device=dev)
+    mass_all = torch.empty(S * max(nma, 16), dtype=torch.uint8, device=dev)
+    bon = draft_bonus if draft_bonus is not None else [None] * S
+    kw = dict(V=V, row_base=row_base, fanout=fanout, check_finite=check_finite, stream=stream)
+    for s in range(S):
+        vshard_stats(targets[s], drafts[s], tokens, temperature, seed, S=S, shard=s, v0=v0s[s],
+                     draft_bonus_s=bon[s], stats=stats_all[s * nst:(s + 1) * nst], **kw)
+    for s in range(S):
+        vshard_mass(targets[s], drafts[s], tokens, temperature, seed, stats_all, S=S, shard=s,
+                    v0=v0s[s], draft_bonus_s=bon[s], mass=mass_all[s * nma:(s + 1) * nma], **kw)
+    out = _vshard_out(B, K, dev, sum(fanout) if fanout is not None else 0)
+    for s in range(S):
+        vshard_pick(targets[s], drafts[s], tokens, temperature, seed, stats_all, mass_all, out,
+                    S=S, shard=s, v0=v0s[s], draft_bonus_s=bon[s], **kw)
+    return out
+
+
+def verify_vsharded_dist(target_s, draft_s, tokens, temperature, seed, *, V, v0, group=None,
+                         fanout=None, draft_bonus_s=None, check_finite=False, row_base=0,
+                         phases=None):
+    """The sharded verify across the ranks of a torch.distributed group, one
+    shard per rank (rank order = vocabulary order; v0 = this rank's first
+    column).  Exchanges: all-gather of the stats blocks and of the mass
+    blocks, all-reduce (max) of the outputs.  `phases` (stats, mass, pick)
+    replaces the library calls (tests of the exchange logic)."""
+    import torch.distributed as dist
+    S = dist.get_world_size(group)
+    shard = dist.get_rank(group)
+    B, K1, _ = target_s.shape
+    K = K1 - 1
+    f_stats, f_mass, f_pick = phases or (vshard_stats, vshard_mass, vshard_pick)
+    kw = dict(S=S, shard=shard, v0=v0, V=V, row_base=row_base, fanout=fanout,
+              draft_bonus_s=draft_bonus_s, check_finite=check_finite)
+    def gather(x):   # the S blocks side by side, in rank order
+        parts = [torch.empty_like(x) for _ in range(S)]
+        dist.all_gather(parts, x, group=group)
+        return torch.cat(parts)
+
+    st = f_stats(target_s, draft_s, tokens, temperature, seed, **kw)
+    stats_all = gather(st)
+    ma = f_mass(target_s, draft_s, tokens, temperature, seed, stats_all, **kw)
+    mass_all = gather(ma)
+    out = _vshard_out(B, K, target_s.device, sum(fanout) if fanout is not None else 0)
+    f_pick(target_s, draft_s, tokens, temperature, seed, stats_all, mass_all, out, **kw)
+    for t in (out.out_tokens, out.hit):
+        if t is not None:
+            x = t.to(torch.int32) if t.dtype != torch.int32 else t
+            dist.all_reduce(x, op=dist.ReduceOp.MAX, group=group)
+            if x is not t:
+                t.copy_(x)
+    if out.status is not None:
+        dist.all_reduce(out.status, op=dist.ReduceOp.MAX, group=group)
     return out
 
 

@@ -987,6 +987,100 @@ __device__ __forceinline__ void row_end_gen(RowAcc<KF> &A, int fl, bool bad, int
   A.reset();
 }
 
+// The crossing point of a warp's values x (one per lane, in index order)
+// for target t: the first lane with positive mass whose inclusive prefix
+// exceeds t; if none (rounding put t at or past the total), the last lane
+// with positive mass (crossed = 0); l = -1 when no lane has mass.  `before`
+// is the prefix before lane l, `total` the warp's sum.  Whole warp.
+struct Cross {
+  int l, crossed;
+  ff before, total;
+};
+static __device__ __noinline__ Cross ff_cross(ff x, ff t) {
+  const ff incl = ff_warp_scan(x);
+  const unsigned cross = ballot(ff_pos(x) && ff_gt(incl, t));
+  const unsigned pos = ballot(ff_pos(x));
+  Cross c;
+  c.crossed = cross != 0u;
+  c.l = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : -1);
+  c.before = ff_shfl(ff_sub(incl, x), c.l < 0 ? 0 : c.l);
+  if (c.l < 0) c.before = ff{0.f, 0.f};
+  c.total = ff_shfl(incl, 31);
+  return c;
+}
+
+constexpr int kFinCH = 8;  // draw iterations whose loads a warp keeps in flight together
+
+// Weights pass of the draw over one warp's contiguous share [wq0, wq1) of
+// this CTA's slice vectors: iteration it covers vectors wq0 + 32 it + lane.
+// Writes the mass of each (iteration, lane) to pmw[it][lane] and returns the
+// lane's total (Kahan-summed) as a float-float pair.  Whole vectors are read
+// with all loads of a chunk in flight at once; the at most two ragged
+// vectors of the slice are assembled afterwards, and a draft row off the
+// target's vector grid takes the element-wise loop.
+template <typename E>
+__device__ __noinline__ ff draw_pass(const RowInfo &Rt, const RowInfo &Rd, const RowInfo &Rdt,
+                                     bool residual, bool d_vec, int wq0, int wq1, int v0, int v1,
+                                     uint64_t s2, uint64_t ct2, uint64_t cd2, uint64_t r2,
+                                     float *pmw) {
+  const int lane = threadIdx.x & 31;
+  const int nit = (wq1 - wq0 + 31) / 32;
+  const uint32_t ni = Elt<E>::kNegInfWord;
+  float tsum = 0.f, tcomp = 0.f;
+  if (residual && !d_vec) {
+#pragma unroll 1
+    for (int it = 0; it < nit; ++it) {
+      const int q = wq0 + it * 32 + lane;
+      float ms = 0.f;
+      if (q < wq1)
+        ms = vec_mass<E>(load_vec_direct<E>(Rt, q, v0, v1), load_vec_slow<E>(Rdt, q, v0, v1), true,
+                         s2, ct2, cd2, r2);
+      pmw[it * 32 + lane] = ms;
+      kahan_add(tsum, tcomp, ms);
+    }
+    return two_sum(tsum, -tcomp);
+  }
+  const uint8_t *const tg = Rt.gbase;
+  const uint8_t *const dg = residual ? Rd.gbase : Rt.gbase;
+  const int tlo = Rt.qlo, thi = Rt.qhi;
+#pragma unroll 1
+  for (int it0 = 0; it0 < nit; it0 += kFinCH) {
+    uint4 tv[kFinCH], dv[kFinCH];
+#pragma unroll
+    for (int c = 0; c < kFinCH; ++c) {
+      const int q = wq0 + (it0 + c) * 32 + lane;
+      tv[c] = dv[c] = make_uint4(ni, ni, ni, ni);
+      if (q < wq1 && q >= tlo && q < thi) {
+        tv[c] = __ldcg(reinterpret_cast<const uint4 *>(tg + 16 * q));
+        if (residual) dv[c] = __ldcg(reinterpret_cast<const uint4 *>(dg + 16 * q));
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kFinCH; ++c) {
+      if (it0 + c < nit) {
+        const float ms = vec_mass<E>(tv[c], dv[c], residual, s2, ct2, cd2, r2);
+        pmw[(it0 + c) * 32 + lane] = ms;
+        kahan_add(tsum, tcomp, ms);
+      }
+    }
+  }
+  // the ragged vectors, by the lanes that own them: vector 0 when the slice
+  // starts off the 16-byte grid (tlo = 1), the last when it ends off it
+#pragma unroll 1
+  for (int x = 0; x < 2; ++x) {
+    const int q = x == 0 ? (tlo > 0 ? 0 : -1) : (thi < Rt.nvec ? Rt.nvec - 1 : -1);
+    if (q < wq0 || q >= wq1 || (x == 1 && q == 0 && tlo > 0)) continue;
+    if (((q - wq0) & 31) == lane) {
+      const uint4 tvv = load_vec_slow<E>(Rt, q, v0, v1);
+      const uint4 dvv = residual ? load_vec_slow<E>(Rd, q, v0, v1) : tvv;
+      const float ms = vec_mass<E>(tvv, dvv, residual, s2, ct2, cd2, r2);
+      pmw[((q - wq0) >> 5) * 32 + lane] = ms;
+      kahan_add(tsum, tcomp, ms);
+    }
+  }
+  return two_sum(tsum, -tcomp);
+}
+
 // The CTA's best KF elements (value desc, index asc) of key row R from the
 // NW x KF vectors its warps kept, by one warp: the lanes expand the vectors
 // into elements (without the excluded token, -inf and anything outside the

@@ -106,6 +106,33 @@ def test_next_row_entry_points_refuse_bad_requests():
                             None) == sd.SD_OK
 
 
+def test_vshard_entry_points_refuse_bad_requests():
+    # host-side checks of the sharded verify: shard index and count, columns
+    # outside the vocabulary, flags, null or unaligned blocks; nothing launched
+    L = sd.lib()
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    assert L.sd_vshard_stats_bytes(4, 3) == 4 * 8 * 96 + 4 * 3 * 16
+    assert L.sd_vshard_stats_bytes(-1, 3) == 0 and L.sd_vshard_mass_bytes(4) == 4 * 32
+    good = dict(B=4, K=3, V=100, S=2, shard=1, v0=50, vs=50, dtype=sd.SD_BF16)
+    for bad in (dict(S=0), dict(S=33), dict(shard=2), dict(shard=-1), dict(v0=60),
+                dict(vs=0), dict(K=sd.SD_MAX_K + 1), dict(dtype=7), dict(flags=0x2)):
+        a = sd.VShardArgs(**{**good, **bad})
+        a.target_logits = a.draft_logits = a.draft_tokens = a.temperature = 1 << 20
+        assert L.sd_vshard_stats(ctypes.byref(a), fake, None) == sd.SD_ERR_INVALID_ARG, bad
+    a = sd.VShardArgs(**good)
+    assert L.sd_vshard_stats(ctypes.byref(a), fake, None) == sd.SD_ERR_INVALID_ARG  # null logits
+    a.target_logits = a.draft_logits = a.draft_tokens = a.temperature = 1 << 20
+    assert L.sd_vshard_stats(ctypes.byref(a), None, None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_vshard_stats(ctypes.byref(a), P((1 << 20) + 8), None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_vshard_mass(ctypes.byref(a), fake, None, None) == sd.SD_ERR_INVALID_ARG
+    assert L.sd_vshard_pick(ctypes.byref(a), fake, fake, None) == sd.SD_ERR_INVALID_ARG  # outputs
+    a.flags = sd.SD_FLAG_PREDICT   # keys without fanout
+    assert L.sd_vshard_stats(ctypes.byref(a), fake, None) == sd.SD_ERR_INVALID_ARG
+    a = sd.VShardArgs(**{**good, "B": 0})
+    assert L.sd_vshard_stats(ctypes.byref(a), None, None) == sd.SD_OK
+
+
 def test_python_binding_refuses_cpu_tensors():
     import torch
     t = torch.zeros(2, 3, 10)
