@@ -171,15 +171,12 @@ size_t sd_verify_workspace_size(int32_t B, int32_t K);
  * tokens.
  * Each logit row is streamed from memory once; the target and draft rows at
  * the first rejection (or target row K) are read a second time for the
- * draw, mostly from L2.  Two ways to run: a split launch (a streaming
- * launch over the rows of all sequences, then a finish launch as its
- * programmatic dependent; needs the workspace) and a single cluster kernel.
- * With a workspace the split launch is taken where the cluster kernel would
- * leave SMs without work (B times its cluster size below the SM count) or
- * would give each sequence one CTA; else, and without a workspace, the
- * single launch; plus,
- * with SD_FLAG_COMPACT, a one-CTA packing launch (a programmatic dependent
- * of the last, same stream).  Requests outside the split launch's limits
+ * draw, mostly from L2.  Two ways to run: with a workspace, a split launch
+ * (a streaming launch over the rows of all sequences, every SM moving the
+ * same bytes, then a finish launch as its programmatic dependent); without
+ * one, a single cluster kernel; plus, with SD_FLAG_COMPACT, a one-CTA
+ * packing launch (a programmatic dependent of the last, same stream).
+ * Requests outside the split launch's limits
  * (a streaming CTA's share touching more than 2 SD_MAX_K + 2 rows, or B too
  * large for its shared-memory list of sampled rows) take the single launch.
  */
