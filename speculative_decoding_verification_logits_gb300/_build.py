@@ -56,7 +56,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if any(rcs):
             raise subprocess.CalledProcessError(next(r for r in rcs if r), "nvcc -c")
         tmp = LIB + tag
-        link = [nvc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", *objs, "-o", tmp]
+        # -ldl: the NVTX ranges look up a profiler's injection library by dlopen
+        link = [nvc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", *objs, "-ldl",
+                "-o", tmp]
         if verbose:
             print(" ".join(link), flush=True)
         subprocess.run(link, check=True)

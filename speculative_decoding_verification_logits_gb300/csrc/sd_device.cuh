@@ -10,6 +10,7 @@
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -1848,6 +1849,17 @@ static int env_int(const char *name, int dflt) {
 
 // Host-side state is kept per device: a process may drive several GPUs, and
 // SM counts, kernel attributes and occupancy answers belong to one of them.
+// An NVTX range named after the C-ABI entry point, open while the call does
+// its host work and enqueues its launches (a profiler shows each call's
+// launches under its name).  Header-only NVTX: without a tool attached a
+// push or pop is a call through an empty slot.
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 constexpr int kMaxDevices = 64;
 
 static int current_device() {

@@ -106,6 +106,7 @@ extern "C" sd_status_t sd_ngram_draft(int32_t B, int32_t L, int32_t K, int32_t n
                                       int32_t n_min, const int32_t *history,
                                       const int32_t *lengths, int32_t *drafts, int32_t *count,
                                       int32_t *match_pos, int32_t *match_n, void *stream) {
+  sdv::NvtxRange nvtx_range("sd_ngram_draft");
   if (B < 0 || L < 0 || L >= (1 << kJBits) || K < 0 || K > SD_MAX_K) return SD_ERR_INVALID_ARG;
   if (n_min < 1 || n_max < n_min || n_max > kNgramMax) return SD_ERR_INVALID_ARG;
   if (B == 0) return SD_OK;

@@ -54,6 +54,7 @@ static sd_status_t static_scratch(void **out) {
 using namespace sdv;
 
 extern "C" sd_status_t sd_verify_noalloc(const sd_verify_args *args, void *stream) {
+  sdv::NvtxRange nvtx_range("sd_verify_noalloc");
   if (!args) return SD_ERR_INVALID_ARG;
   if (args->workspace || args->workspace_bytes)
     return SD_ERR_INVALID_ARG;  // the static scratch replaces the caller's

@@ -64,6 +64,7 @@ extern "C" sd_status_t sd_d3d_pack(int32_t B, int32_t K, int32_t n_keys, const i
                                    const int32_t *anchor_pos, int32_t mask_token,
                                    int32_t *tokens, int32_t *positions, int32_t *ctx,
                                    void *stream) {
+  sdv::NvtxRange nvtx_range("sd_d3d_pack");
   if (B < 0 || K < 0 || K > SD_MAX_K || n_keys < 0 || n_keys > (SD_MAX_K + 1) * SD_MAX_FANOUT)
     return SD_ERR_INVALID_ARG;
   if (B == 0) return SD_OK;

@@ -82,6 +82,7 @@ extern "C" sd_status_t sd_kv_rollback(int32_t B, int32_t page_size, int32_t max_
                                       const int32_t *tau, int32_t *block_table,
                                       int32_t *new_len, int32_t *freed, int32_t *free_offsets,
                                       void *stream) {
+  sdv::NvtxRange nvtx_range("sd_kv_rollback");
   if (B < 0 || page_size < 1 || max_pages < 0 || appended < 0 || !free_offsets)
     return SD_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;

@@ -148,6 +148,7 @@ size_t sd_verify_workspace_size(int32_t B, int32_t K) {
 }
 
 sd_status_t sd_verify(const sd_verify_args *a, void *stream) {
+  sdv::NvtxRange nvtx_range("sd_verify");
   if (!a) return SD_ERR_INVALID_ARG;
   if (a->B < 0 || a->K < 0 || a->K > SD_MAX_K || a->V < 1 || a->V > SD_MAX_V)
     return SD_ERR_INVALID_ARG;
@@ -229,6 +230,7 @@ sd_status_t sd_outcome_predict(int32_t B, int32_t K, int32_t V, sd_dtype_t dtype
                                const void *draft_bonus_logits, const int32_t *fanout_host,
                                int32_t *keys, int32_t *n_keys_out, int32_t *status,
                                void *stream) {
+  sdv::NvtxRange nvtx_range("sd_outcome_predict");
   if (B < 0 || K < 0 || K > SD_MAX_K || V < 1 || V > SD_MAX_V) return SD_ERR_INVALID_ARG;
   if (dtype != SD_F32 && dtype != SD_BF16) return SD_ERR_INVALID_ARG;
   if (!fanout_host) return SD_ERR_INVALID_ARG;
@@ -267,6 +269,7 @@ sd_status_t sd_outcome_predict(int32_t B, int32_t K, int32_t V, sd_dtype_t dtype
 
 sd_status_t sd_compact(int32_t B, int32_t K, const int32_t *out_tokens, const int32_t *tau,
                        int32_t *offsets, int32_t *packed, int32_t *status, void *stream) {
+  sdv::NvtxRange nvtx_range("sd_compact");
   if (B < 0 || K < 0 || K > SD_MAX_K || !offsets) return SD_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   if (B == 0) {
@@ -279,6 +282,7 @@ sd_status_t sd_compact(int32_t B, int32_t K, const int32_t *out_tokens, const in
 
 sd_status_t sd_uniforms(uint64_t seed, int32_t n, const int32_t *row, const int32_t *pos,
                         const int32_t *slot, double *out, void *stream) {
+  sdv::NvtxRange nvtx_range("sd_uniforms");
   if (n < 0) return SD_ERR_INVALID_ARG;
   if (n == 0) return SD_OK;
   if (!row || !pos || !slot || !out) return SD_ERR_INVALID_ARG;

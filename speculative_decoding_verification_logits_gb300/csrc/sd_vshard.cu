@@ -710,6 +710,7 @@ size_t sd_vshard_stats_bytes(int32_t B, int32_t K) {
 size_t sd_vshard_mass_bytes(int32_t B) { return B < 0 ? 0 : (size_t)B * kVsMass; }
 
 sd_status_t sd_vshard_stats(const sd_vshard_args *a, void *stats, void *stream) {
+  sdv::NvtxRange nvtx_range("sd_vshard_stats");
   VsParams P;
   const sd_status_t st = vs_params(a, P);
   if (st != SD_OK) return st;
@@ -724,6 +725,7 @@ sd_status_t sd_vshard_stats(const sd_vshard_args *a, void *stats, void *stream) 
 
 sd_status_t sd_vshard_mass(const sd_vshard_args *a, const void *stats_all, void *mass,
                            void *stream) {
+  sdv::NvtxRange nvtx_range("sd_vshard_mass");
   VsParams P;
   const sd_status_t st = vs_params(a, P);
   if (st != SD_OK) return st;
@@ -739,6 +741,7 @@ sd_status_t sd_vshard_mass(const sd_vshard_args *a, const void *stats_all, void 
 
 sd_status_t sd_vshard_pick(const sd_vshard_args *a, const void *stats_all, const void *mass_all,
                            void *stream) {
+  sdv::NvtxRange nvtx_range("sd_vshard_pick");
   VsParams P;
   const sd_status_t st = vs_params(a, P);
   if (st != SD_OK) return st;

@@ -402,6 +402,32 @@ def test_row_base_splits_batch_identically(dev, path):
     assert torch.equal(full.out_tokens, torch.cat([lo.out_tokens, hi.out_tokens]))
 
 
+def test_second_device_in_the_same_process(dev, path):
+    """The library's host state (SM count, kernel attributes, cluster
+    occupancy) is kept per device: one process calling on cuda:1 after
+    cuda:0, and on cuda:0 again, gets the same results on each."""
+    if torch.cuda.device_count() < 2:
+        pytest.skip("needs two visible devices")
+    B, K, V = 12, 5, 50021
+    inp = W.synth(B, K, V, "bf16", kind="normal", temperature=0.8, seed=77, device=dev)
+    fan = [2] * (K + 1)
+
+    def run(d):
+        with torch.cuda.device(d):
+            r = sd.verify(inp.target.to(d), inp.draft.to(d), inp.tokens.to(d),
+                          inp.temperature.to(d), inp.seed, fanout=fan, compact=True)
+            torch.cuda.synchronize(d)
+        return {k: getattr(r, k).cpu() for k in ("out_tokens", "tau", "keys", "packed",
+                                                  "status")}
+
+    first = run(torch.device("cuda:0"))
+    second = run(torch.device("cuda:1"))
+    again = run(torch.device("cuda:0"))
+    for k in first:
+        assert torch.equal(first[k], second[k]), k
+        assert torch.equal(first[k], again[k]), k
+
+
 def test_compact_standalone(dev):
     rng = np.random.default_rng(4)
     B, K = 3000, 5
