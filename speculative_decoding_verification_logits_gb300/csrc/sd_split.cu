@@ -164,7 +164,10 @@ __global__ void __launch_bounds__(NT, stream_ctas_per_sm<KF>())
       b = lo;
       isx = rank[b + 1] > rank[b] && i == b + rank[b];
     }
+    // both loads issued before either is used
+    const int fj = (isx && g > 0 && P.keys) ? P.fanout[j] : 0;
     const float T = P.temps[b];
+    const int tok = fj > 0 ? P.tokens[(int64_t)b * K + j] : -1;
     const bool sampled = T > 0.f && T <= 3.4e38f;
     RowInfo &R = S.rows[tid];
     R.kind = isx ? (g == 0 ? kBonus : kDraft) : kTarget;
@@ -177,11 +180,10 @@ __global__ void __launch_bounds__(NT, stream_ctas_per_sm<KF>())
       R.g = P.target + ((int64_t)b * (K + 1) + j) * P.V * sz;
       R.type = sampled ? (P.argmax_out ? kRowEA : kRowE) : kRowA;
     } else if (R.kind == kDraft) {
-      const int fj = P.keys ? P.fanout[j] : 0;
       R.g = P.draft + ((int64_t)b * K + j) * P.V * sz;
       R.type = sampled ? (fj > 0 ? kRowEK : kRowE) : kRowK;
       R.fan = fj;
-      if (fj > 0) R.excl = P.tokens[(int64_t)b * K + j];
+      if (fj > 0) R.excl = tok;
     } else {
       R.g = P.bonus + (int64_t)b * P.V * sz;
       R.type = kRowK;
@@ -233,33 +235,23 @@ __global__ void __launch_bounds__(NT, stream_ctas_per_sm<KF>())
   }
   __syncthreads();
 
-  // ---- one record per piece: the warps combined in a fixed order (a warp
-  // with a NaN sum, from the finiteness check, makes the piece's sum NaN)
-  if (tid < nrows) {
-    const int r = tid;
-    float M = -INFINITY;
-    bool poison = false;
+  // ---- one record per piece: a warp per row, lane w holding warp w's
+  // statistics, combined by warp-wide reductions (a warp with a NaN sum,
+  // from the finiteness check, makes the piece's sum NaN)
 #pragma unroll 1
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, wstat[r * NW + w].m);
-    int Ix = INT32_MAX;
-    float C = INFINITY;
-#pragma unroll 1
-    for (int w = 0; w < NW; ++w) {
-      const WStat x = wstat[r * NW + w];
-      if (x.m == M) Ix = min(Ix, x.idx);
-      if (x.z > 0.f) C = fminf(C, x.c);
-      poison |= x.z != x.z;
-    }
-    ff Z{0.f, 0.f};
-#pragma unroll 1
-    for (int w = 0; w < NW; ++w) {
-      const WStat x = wstat[r * NW + w];
-      if (x.z > 0.f) Z = ff_add(Z, two_prod(x.z, ex2(C - x.c)));
-    }
+  for (int r = warp; r < nrows; r += NW) {
+    const WStat x = lane < NW ? wstat[r * NW + lane] : WStat{-INFINITY, 0.f, INFINITY, INT32_MAX};
+    const float M = rmax_f(x.m);
+    const int Ix = rmin_i(x.m == M ? x.idx : INT32_MAX);
+    const float C = rmin_f(x.z > 0.f ? x.c : INFINITY);
+    const bool poison = ballot(x.z != x.z) != 0u;
+    ff Z = ff_warp_sum(x.z > 0.f ? two_prod(x.z, ex2(C - x.c)) : ff{0.f, 0.f});
     if (poison) Z.hi = __int_as_float(0x7fffffff);
-    float *rec = reinterpret_cast<float *>(P.ws + (int64_t)S.rows[r].rec * kRecBytes);
-    *reinterpret_cast<float4 *>(rec) = make_float4(M, __int_as_float(Ix), C, Z.hi);
-    rec[4] = Z.lo;
+    if (lane == 0) {
+      float *rec = reinterpret_cast<float *>(P.ws + (int64_t)S.rows[r].rec * kRecBytes);
+      *reinterpret_cast<float4 *>(rec) = make_float4(M, __int_as_float(Ix), C, Z.hi);
+      rec[4] = Z.lo;
+    }
   }
   if (KF > 0) {
 #pragma unroll 1
