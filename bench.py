@@ -241,6 +241,11 @@ def measure(name, steps, warmup, dev, rank, ws_n, e2e_steps=0):
             for _ in range(n_sets)]
     stream = torch.cuda.Stream(dev)
     wss = sd.workspace(B, K, dev, stream)
+    # The inputs and buffers above were made on the default stream; the
+    # rounds run on `stream`.  Wait for all of it first: a conversion still
+    # queued on the default stream could otherwise read a freed temporary
+    # that the allocator has already handed out as an output buffer.
+    torch.cuda.synchronize(dev)
     pack = "anchor" in one.meta   # the D3D workload also packs the drafter's next pass
     n_keys = sum(fan) if fan else 0
     packs = [(torch.empty((B, 1 + n_keys, K + 1), dtype=torch.int32, device=dev),
@@ -488,6 +493,7 @@ def run_ngram(args):
     e = lambda *sh: torch.empty(sh, dtype=torch.int32, device=dev)
     outs = [(e(B, K), e(B), e(B), e(B)) for _ in range(n_sets)]
     stream = torch.cuda.Stream(dev)
+    torch.cuda.synchronize(dev)   # the pool is made on the default stream
 
     def step(i):
         sd.ngram_draft(pool[i % n_sets], lens, K, s["n_max"], s["n_min"], out=outs[i % n_sets],

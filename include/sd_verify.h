@@ -171,7 +171,7 @@ size_t sd_verify_workspace_size(int32_t B, int32_t K);
  * tokens.
  * Each logit row is streamed from memory once; the target and draft rows at
  * the first rejection (or target row K) are read a second time for the
- * draw, mostly from L2.  Two ways to run: with a workspace, a split launch
+ * draw (from L2 when a round's logits fit there).  Two ways to run: with a workspace, a split launch
  * (a streaming launch over the rows of all sequences, every SM moving the
  * same bytes, then a finish launch as its programmatic dependent); without
  * one, a single cluster kernel; plus, with SD_FLAG_COMPACT, a one-CTA
@@ -202,9 +202,10 @@ sd_status_t sd_verify(const sd_verify_args *args, void *stream);
  * streams, other threads) race on it, so order them on one stream.  The
  * array keeps the last call's records; nothing in it needs clearing, as
  * every record is written before it is read within a call.  Like
- * sd_verify, it takes the split launch only where that is the faster one
- * (see sd_verify) and the single cluster kernel, which needs no scratch,
- * otherwise.
+ * sd_verify given scratch, it takes the split launch, and the single
+ * cluster kernel (which needs no scratch) outside the split launch's
+ * limits.  The looked-up address belongs to the device's primary context:
+ * it is not valid across cudaDeviceReset (reload the library after one).
  */
 sd_status_t sd_verify_noalloc(const sd_verify_args *args, void *stream);
 

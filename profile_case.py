@@ -44,6 +44,10 @@ def main():
             sd.kv_rollback(m["block_table"], m["kv_len"], r.tau, m["page_size"], p.K + 1)
     torch.cuda.synchronize()
     print("ok", r.tau.float().mean().item())
+    # logit bytes each input set's round must read (greedy rows skip their
+    # draft rows), for the profile summaries' ratio of DRAM to algorithmic bytes
+    print("alg_bytes", *[W.logit_bytes(p, algorithmic=True, with_bonus=fan is not None)
+                         for p in pool])
 
 
 if __name__ == "__main__":

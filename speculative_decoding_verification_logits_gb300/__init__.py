@@ -16,6 +16,7 @@ Entry points (same names as the C ABI):
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 from dataclasses import dataclass
@@ -141,6 +142,22 @@ def _stream(device, stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _on_stream(fn):
+    """Run a wrapper with `stream` (when given) as the current stream, so the
+    tensors it allocates belong to the stream its launches are queued on: the
+    caching allocator reuses a freed block in the order of the stream that
+    allocated it, and a block allocated on another stream could still be in
+    use by work queued there."""
+    @functools.wraps(fn)
+    def call(*args, **kwargs):
+        s = kwargs.get("stream")
+        if s is None:
+            return fn(*args, **kwargs)
+        with torch.cuda.stream(s):
+            return fn(*args, **kwargs)
+    return call
+
+
 def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.float32:
         return SD_F32
@@ -186,7 +203,8 @@ def workspace(B: int, K: int, device=None, stream=None):
     with _ws_lock:
         buf = _ws.get(key)
         if buf is None or buf.numel() < need:
-            buf = torch.zeros(need, dtype=torch.uint8, device=device)
+            with torch.cuda.stream(s):   # the block belongs to the stream it serves
+                buf = torch.zeros(need, dtype=torch.uint8, device=device)
             _ws[key] = buf
     return buf
 
@@ -227,6 +245,7 @@ def alloc_outputs(B, K, device, *, hit=False, compact=False, stats=False, n_keys
     return r
 
 
+@_on_stream
 def verify(target, draft, tokens, temperature, seed: int, *, row_base: int = 0,
            cache_keys=None, fanout=None, draft_bonus=None, compact: bool = False,
            stats: bool = False, check_finite: bool = False, out: VerifyResult | None = None,
@@ -300,6 +319,7 @@ def verify(target, draft, tokens, temperature, seed: int, *, row_base: int = 0,
     return r
 
 
+@_on_stream
 def outcome_predict(draft, tokens, fanout, draft_bonus=None, *, keys=None, status=None,
                     stream=None) -> torch.Tensor:
     """Speculation-cache keys [B][sum(fanout)][2] (position, token)."""
@@ -326,6 +346,7 @@ def outcome_predict(draft, tokens, fanout, draft_bonus=None, *, keys=None, statu
     return keys
 
 
+@_on_stream
 def d3d_pack(keys, draft_tokens, anchor, anchor_pos, mask_token: int, *, out=None,
              stream=None):
     """The drafter's packed next pass: (tokens, positions) [B][1+n_keys][K+1]
@@ -353,6 +374,7 @@ def d3d_pack(keys, draft_tokens, anchor, anchor_pos, mask_token: int, *, out=Non
     return t, p, c
 
 
+@_on_stream
 def ngram_draft(history, lengths, K: int, n_max: int, n_min: int, *, out=None, stream=None):
     """Prompt-lookup drafts (drafts [B][K], count, match_pos, match_n [B])
     from history [B][L] and lengths [B] (int32, CUDA)."""
@@ -370,6 +392,7 @@ def ngram_draft(history, lengths, K: int, n_max: int, n_min: int, *, out=None, s
     return d, c, p, n
 
 
+@_on_stream
 def kv_rollback(block_table, kv_len, tau, page_size: int, appended: int, *, out=None,
                 stream=None):
     """Roll row caches back after a round: block_table [B][max_pages] is
@@ -390,6 +413,7 @@ def kv_rollback(block_table, kv_len, tau, page_size: int, appended: int, *, out=
     return n, f, o
 
 
+@_on_stream
 def compact(out_tokens, tau, *, offsets=None, packed=None, status=None, stream=None):
     """(offsets [B+1], packed [B*(K+1)]) from out_tokens [B][K+1] and tau [B]."""
     _need(out_tokens, "out_tokens", torch.int32)
@@ -405,6 +429,7 @@ def compact(out_tokens, tau, *, offsets=None, packed=None, status=None, stream=N
     return offsets, packed
 
 
+@_on_stream
 def uniforms(seed: int, row, pos, slot, *, stream=None) -> torch.Tensor:
     """The verify step's uniforms u(seed, row, pos, slot) (float64)."""
     _need(row, "row", torch.int32)
@@ -455,6 +480,7 @@ def _vshard_args(target_s, draft_s, tokens, temperature, seed, *, S, shard, v0, 
     return a
 
 
+@_on_stream
 def vshard_stats(target_s, draft_s, tokens, temperature, seed, *, S, shard, v0, V, row_base=0,
                  fanout=None, draft_bonus_s=None, check_finite=False, stats=None, stream=None):
     """sd_vshard_stats: this shard's stats block (uint8 tensor)."""
@@ -482,6 +508,7 @@ def vshard_stats(target_s, draft_s, tokens, temperature, seed, *, S, shard, v0, 
     return stats
 
 
+@_on_stream
 def vshard_mass(target_s, draft_s, tokens, temperature, seed, stats_all, *, S, shard, v0, V,
                 row_base=0, fanout=None, draft_bonus_s=None, check_finite=False, mass=None,
                 stream=None):
@@ -501,6 +528,7 @@ def vshard_mass(target_s, draft_s, tokens, temperature, seed, stats_all, *, S, s
     return mass
 
 
+@_on_stream
 def vshard_pick(target_s, draft_s, tokens, temperature, seed, stats_all, mass_all, out, *, S,
                 shard, v0, V, row_base=0, fanout=None, draft_bonus_s=None, check_finite=False,
                 stream=None):
@@ -524,6 +552,7 @@ def _vshard_out(B, K, device, n_keys):
     return r
 
 
+@_on_stream
 def verify_vsharded(targets, drafts, tokens, temperature, seed, *, V, fanout=None,
                     draft_bonus=None, check_finite=False, row_base=0, stream=None):
     """The sharded verify on one device: targets / drafts / draft_bonus are
