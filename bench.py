@@ -726,6 +726,9 @@ def run_reference(args):
     import oracle
     oracle.build()
     name = args.workload
+    sharded = name == "vshard"   # the oracle computes the unsharded verify
+    if sharded:
+        name = HEADLINE
     cores = os.cpu_count() or 1
     if name == "ngram":   # the oracle's drafter over whole rounds, one thread
         h, lens, s = W.ngram_inputs(0)
@@ -767,11 +770,144 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws_n,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_of(name, ws_n, _l2_bytes()),
+            "data": "synthetic",
+            "config": (vshard_config(args.shards, ws_n, _l2_bytes()) if sharded
+                       else config_of(name, ws_n, _l2_bytes())),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "cpu": cpu_model(), "sample": sample,
                              "single_thread_ms_per_round": per_row * B * 1e3},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def vshard_config(S, ws_n, l2):
+    """The `config` object of the sharded workload's line (both arms)."""
+    c = config_of(HEADLINE, ws_n, l2)
+    c["workload"] += f"; logits cut into {S} vocabulary shards, all on one GPU"
+    c["shards"] = S
+    return c
+
+
+def run_vshard(args):
+    """The vocabulary-sharded verify with every shard on this GPU: the
+    headline workload's logits cut into S column blocks, each round the S
+    shards' statistics, mass and pick launches in turn, the exchanges being
+    the shards' blocks laid side by side.  Same timing rules as the other
+    workloads; the oracle sample checks the outputs of one round."""
+    import speculative_decoding_verification_logits_gb300 as sd
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sd.lib()
+    name, S = HEADLINE, args.shards
+    fan = W.WORKLOADS[name].get("fanout")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    one = W.workload(name, round_idx=0, device=dev)
+    set_bytes = W.logit_bytes(one, algorithmic=False, with_bonus=True)
+    n_sets = pool_size(set_bytes, l2)
+    bounds = sd.vshard_bounds(one.V, S)
+
+    def shards(x):
+        return [x[..., a:a + n].contiguous() for a, n in bounds] if x is not None else None
+
+    pool = []
+    for i in range(n_sets):
+        p = one if i == 0 else W.workload(name, round_idx=i, device=dev)
+        pool.append((shards(p.target), shards(p.draft), p.tokens, p.temperature, p.seed,
+                     shards(p.draft_bonus)))
+    B, K, V = one.B, one.K, one.V
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.synchronize(dev)   # the pool is made on the default stream
+    outs = [None] * n_sets
+
+    def step(i):
+        t, d, tok, temp, seed, bon = pool[i % n_sets]
+        outs[i % n_sets] = sd.verify_vsharded(t, d, tok, temp, seed + i // n_sets, V=V,
+                                              fanout=fan, draft_bonus=bon,
+                                              row_base=rank * B, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize(dev)
+    G = min(args.steps, max(n_sets, (64 // n_sets) * n_sets))
+    graphs = {}
+    full, rem = divmod(args.steps, G)
+    plan = [G] * full + ([rem] if rem else [])
+    for n in set(plan):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i)
+        graphs[n] = g
+    with torch.cuda.stream(stream):
+        for n in set(plan):
+            graphs[n].replay()
+    torch.cuda.synchronize(dev)
+
+    def timed(fn):
+        if ws_n > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1)
+        if ws_n > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    def replay_all():
+        with torch.cuda.stream(stream):
+            for n in plan:
+                graphs[n].replay()
+
+    with ClockSampler(local) as clk:
+        ms = timed(replay_all)
+    clocks = clk.summary()
+    # one round of set 0 with its first seed, for the oracle's comparison
+    t, d, tok, temp, seed, bon = pool[0]
+    with torch.cuda.stream(stream):
+        so = sd.verify_vsharded(t, d, tok, temp, seed, V=V, fanout=fan, draft_bonus=bon,
+                                row_base=one.meta.get("row_base", 0), stream=stream)
+    torch.cuda.synchronize(dev)
+    sample = {k: getattr(so, k).cpu().numpy() for k in ("num_accepted", "out_tokens", "tau",
+                                                        "hit", "keys")}
+    status = int(so.status.item()) if so.status is not None else None
+    if ws_n > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    alg = algorithmic_bytes(one)
+    achieved = alg / (ms / args.steps / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": ws_n * args.steps / (ms / 1e3), "unit": UNIT,
+        "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": one.meta["dtype"],
+        "data": "synthetic (seeded logits shaped like the workload; draft tokens drawn from q)",
+        "config": vshard_config(S, ws_n, l2),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                     "peak_source": pk_kind,
+                     "kernel": "sharded verify step: all launches of one round "
+                               "(duration = step time)",
+                     "algorithmic_bytes_per_launch": alg},
+        # per step: S statistics, S mass and S pick launches of this library
+        "gpu_launches": 3 * S * args.steps, "clocks": clocks,
+        "e2e": None, "status_bits": status,
+        "launch_plan": f"sharded x{S} (stats, mass, pick per shard)",
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"], line["parity_sample"] = cpu_baseline(name, args.cpu_seconds, sample)
+    return line
 
 
 def main():
@@ -779,7 +915,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=HEADLINE, choices=W.ORDER + ["ngram"])
+    ap.add_argument("--workload", default=HEADLINE, choices=W.ORDER + ["ngram", "vshard"])
+    ap.add_argument("--shards", type=int, default=4,
+                    help="vocabulary shards of the vshard workload (the headline's logits)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=400)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -796,6 +934,8 @@ def main():
         line = run_reference(args)
     elif args.workload == "ngram":
         line = run_ngram(args)
+    elif args.workload == "vshard":
+        line = run_vshard(args)
     else:
         line = run_gpu(args)
     if line is not None:
