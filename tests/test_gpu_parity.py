@@ -259,6 +259,44 @@ def test_largest_k_with_keys(dev, path, dt):
     _check(*compare_verify(r, o, temps))
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_maximum_sizes(dev, path, dt):
+    """The header's limits at once: SD_MAX_V, SD_MAX_K and SD_MAX_FANOUT keys
+    at every position plus the bonus row; every row against the oracle."""
+    B, K, V = 2, sd.SD_MAX_K, sd.SD_MAX_V
+    fan = [sd.SD_MAX_FANOUT] * (K + 1)
+    temps = [0.8, 0.0]
+    inp = W.synth(B, K, V, dt, kind="peaked", sigma=2.0, draft_sigma=0.5, peaks=20,
+                  temperature=temps, seed=262, device=dev, bonus_row=True)
+    keys_ref = oracle.outcome_predict(_np(inp.draft), inp.tokens.cpu().numpy(), fan,
+                                      _np(inp.draft_bonus))
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, fanout=fan,
+                  draft_bonus=inp.draft_bonus, stats=True, compact=True)
+    np.testing.assert_array_equal(r.keys.cpu().numpy(), keys_ref)
+    o = _oracle_for(inp, keys=keys_ref)
+    _check(*compare_verify(r, o, temps))
+    offs, packed = oracle.compact(r.out_tokens.cpu().numpy(), r.tau.cpu().numpy())
+    np.testing.assert_array_equal(r.packed.cpu().numpy()[: offs[-1]], packed)
+
+
+@pytest.mark.parametrize("B,K,V", [(4096, 2, 300), (1500, 4, 1024)])
+def test_large_batches_of_short_rows(dev, path, B, K, V):
+    """Many sequences of short rows: a streaming CTA covers dozens of rows,
+    the finish launches thousands of clusters; every row against the oracle."""
+    g = torch.Generator().manual_seed(B + K)
+    temps = torch.where(torch.rand(B, generator=g) < 0.7, torch.rand(B, generator=g) + 0.3,
+                        torch.zeros(B)).tolist()
+    inp = W.synth(B, K, V, "bf16", kind="normal", sigma=2.0, draft_sigma=0.7,
+                  temperature=temps, seed=B, device=dev)
+    r = sd.verify(inp.target, inp.draft, inp.tokens, inp.temperature, inp.seed, compact=True)
+    o = _oracle_for(inp)
+    stats, bad = compare_verify(r, o, temps, check_stats=False)
+    _check(stats, bad)
+    offs, packed = oracle.compact(r.out_tokens.cpu().numpy(), r.tau.cpu().numpy())
+    np.testing.assert_array_equal(r.offsets.cpu().numpy(), offs)
+    np.testing.assert_array_equal(r.packed.cpu().numpy()[: offs[-1]], packed)
+
+
 def test_d3d_key_counts(dev, path):
     B, K, V = 2, 15, 4096
     inp = W.synth(B, K, V, "bf16", kind="normal", temperature=0.0, seed=9, device=dev,
