@@ -35,6 +35,7 @@ namespace sdv {
 constexpr int kVsNT = 256;
 constexpr int kVsNW = kVsNT / 32;
 constexpr int kVsMass = 32;  // bytes per sequence in a mass block
+constexpr int kVsCH = 4;     // vectors per row a mass thread loads before using them
 
 struct VsParams {
   const uint8_t *target, *draft, *bonus;  // this shard's columns
@@ -359,15 +360,28 @@ __global__ void __launch_bounds__(kVsNT) sd_vshard_mass_kernel(const __grid_cons
     const uint64_t s2 = pk2(s, s), ct2 = pk2(Ct, Ct), cd2 = pk2(Cd, Cd), r2 = pk2(Rz, Rz);
     const bool d_vec = residual && S.dd.hp == S.dt.hp;
     float a = 0.f, ac = 0.f, p = 0.f, pc = 0.f;
+    // kVsCH vectors of each row per thread in flight at once, then their masses
+    const int nvec = S.dt.nvec;
 #pragma unroll 1
-    for (int q = tid; q < S.dt.nvec; q += NT) {
-      const uint4 tv = load_vec_direct<E>(S.dt, q, 0, P.vs);
-      if (residual) {
-        const uint4 dv = d_vec ? load_vec_direct<E>(S.dd, q, 0, P.vs)
-                               : load_vec_slow<E>(S.ddt, q, 0, P.vs);
-        kahan_add(a, ac, vec_mass<E>(tv, dv, true, s2, ct2, cd2, r2));
+    for (int q0 = tid; q0 < nvec; q0 += NT * kVsCH) {
+      uint4 tv[kVsCH], dv[kVsCH];
+#pragma unroll
+      for (int c = 0; c < kVsCH; ++c) {
+        const int q = q0 + c * NT;
+        if (q < nvec) {
+          tv[c] = load_vec_direct<E>(S.dt, q, 0, P.vs);
+          if (residual)
+            dv[c] = d_vec ? load_vec_direct<E>(S.dd, q, 0, P.vs)
+                          : load_vec_slow<E>(S.ddt, q, 0, P.vs);
+        }
       }
-      kahan_add(p, pc, vec_mass<E>(tv, tv, false, s2, ct2, cd2, r2));
+#pragma unroll
+      for (int c = 0; c < kVsCH; ++c) {
+        if (q0 + c * NT < nvec) {
+          if (residual) kahan_add(a, ac, vec_mass<E>(tv[c], dv[c], true, s2, ct2, cd2, r2));
+          kahan_add(p, pc, vec_mass<E>(tv[c], tv[c], false, s2, ct2, cd2, r2));
+        }
+      }
     }
     mres = ff_warp_sum(two_sum(a, -ac));
     mp = ff_warp_sum(two_sum(p, -pc));
