@@ -34,8 +34,17 @@ namespace sdv {
 
 constexpr int kVsNT = 256;
 constexpr int kVsNW = kVsNT / 32;
-constexpr int kVsMass = 32;  // bytes per sequence in a mass block
-constexpr int kVsCH = 4;     // vectors per row a mass thread loads before using them
+constexpr int kVsParts = 4;              // column parts of a shard (mass CTAs per sequence)
+constexpr int kVsMass = 16 * kVsParts;   // bytes per sequence in a mass block
+constexpr int kVsCH = 4;  // vectors per row a mass thread loads before using them
+
+// Columns [a, e) of part p of a shard of vs columns: kVsParts near-equal
+// ranges of whole 16-column groups, the last one taking the rest.
+__host__ __device__ inline void vs_part(int vs, int p, int &a, int &e) {
+  const int len = ((vs + kVsParts - 1) / kVsParts + 15) / 16 * 16;
+  a = p * len < vs ? p * len : vs;
+  e = a + len < vs ? a + len : vs;
+}
 
 struct VsParams {
   const uint8_t *target, *draft, *bonus;  // this shard's columns
@@ -211,7 +220,7 @@ struct VsS {
   RowInfo dt, dd, ddt;
   ff wmass[kVsNW];
   ff t_loc, t_w;
-  int m, kind, valid, dvalid, fvalid, tok, owner, wsel;
+  int m, kind, valid, dvalid, fvalid, tok, owner, wsel, part;
 };
 
 // Combine of every row over the shards (warp per row, lane p = shard p, the
@@ -312,19 +321,19 @@ __device__ void vs_decide(const VsParams &P, VsS &S, int b, float s, bool tvalid
   __syncthreads();
 }
 
-// The rows the draw reads, on this shard's columns.
+// The rows the draw reads, on columns [a, e) of this shard.
 template <typename E>
-__device__ void vs_draw_rows(const VsParams &P, VsS &S, int b) {
+__device__ void vs_draw_rows(const VsParams &P, VsS &S, int b, int a, int e) {
   constexpr int sz = Elt<E>::kSize;
   const int K = P.K, mm = S.m;
   if (threadIdx.x == 0 && S.kind != 0) {
     S.dt.g = P.target + ((int64_t)b * (K + 1) + mm) * P.vs * sz;
     S.dt.excl = -1;
-    row_geometry<kVsNT>(S.dt, 0, P.vs, sz);
+    row_geometry<kVsNT>(S.dt, a, e, sz);
     if (mm < K) {
       S.dd.g = P.draft + ((int64_t)b * K + mm) * P.vs * sz;
       S.dd.excl = -1;
-      row_geometry<kVsNT>(S.dd, 0, P.vs, sz);
+      row_geometry<kVsNT>(S.dd, a, e, sz);
       S.ddt = S.dt;  // the draft row read element-wise on the target's grid
       S.ddt.g = S.dd.g;
       S.ddt.qlo = 1;
@@ -335,21 +344,24 @@ __device__ void vs_draw_rows(const VsParams &P, VsS &S, int b) {
 }
 
 // ------------------------------------------------------------------- mass --
-// One CTA per sequence: the decision, then this shard's mass of the residual
-// at m and of p at m (the fallback for an identically zero residual).
+// One CTA per (sequence, part of the shard's columns): the decision, then
+// the part's mass of the residual at m and of p at m (the fallback for an
+// identically zero residual), one float-float pair each per part.
 template <typename E>
 __global__ void __launch_bounds__(kVsNT) sd_vshard_mass_kernel(const __grid_constant__ VsParams P) {
   constexpr int NT = kVsNT, NW = kVsNW;
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x, part = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ VsS S;
   __shared__ ff red[2][NW];
+  int pa, pe;  // this CTA's columns of the shard
+  vs_part(P.vs, part, pa, pe);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const float T = P.temps[b];
   const bool tvalid = (T >= 0.f) && (T <= 3.4e38f);
   const bool sampled = tvalid && T > 0.f;
   const float s = sampled ? log2e_over(T) : 0.f;
   vs_decide<E>(P, S, b, s, tvalid, sampled);
-  vs_draw_rows<E>(P, S, b);
+  vs_draw_rows<E>(P, S, b, pa, pe);
   ff mres{0.f, 0.f}, mp{0.f, 0.f};
   if (S.kind != 0) {
     const int mm = S.m;
@@ -369,10 +381,10 @@ __global__ void __launch_bounds__(kVsNT) sd_vshard_mass_kernel(const __grid_cons
       for (int c = 0; c < kVsCH; ++c) {
         const int q = q0 + c * NT;
         if (q < nvec) {
-          tv[c] = load_vec_direct<E>(S.dt, q, 0, P.vs);
+          tv[c] = load_vec_direct<E>(S.dt, q, pa, pe);
           if (residual)
-            dv[c] = d_vec ? load_vec_direct<E>(S.dd, q, 0, P.vs)
-                          : load_vec_slow<E>(S.ddt, q, 0, P.vs);
+            dv[c] = d_vec ? load_vec_direct<E>(S.dd, q, pa, pe)
+                          : load_vec_slow<E>(S.ddt, q, pa, pe);
         }
       }
 #pragma unroll
@@ -397,15 +409,16 @@ __global__ void __launch_bounds__(kVsNT) sd_vshard_mass_kernel(const __grid_cons
       x = ff_add(x, red[0][w]);
       y = ff_add(y, red[1][w]);
     }
-    *reinterpret_cast<float4 *>(P.mass + (int64_t)b * kVsMass) = make_float4(x.hi, x.lo, y.hi, y.lo);
+    *reinterpret_cast<float4 *>(P.mass + (int64_t)b * kVsMass + 16 * part) =
+        make_float4(x.hi, x.lo, y.hi, y.lo);
   }
 }
 
 // ------------------------------------------------------------------- pick --
 // One CTA per sequence: the decision again, the keys from all shards'
-// candidates, the shard holding u * S; that shard scans its columns (warp,
-// iteration, lane, element, as the split launch's finish does) and writes
-// the token.  Every shard writes the outputs that are the same everywhere.
+// candidates, the shard holding u * S and, in it, the part holding it; that
+// shard scans the part's columns (warp, iteration, lane, element, as the
+// split launch's finish does) and writes the token.  Every shard writes the outputs that are the same everywhere.
 template <typename E>
 __global__ void __launch_bounds__(kVsNT) sd_vshard_pick_kernel(const __grid_constant__ VsParams P) {
   constexpr int NW = kVsNW;
@@ -473,16 +486,19 @@ __global__ void __launch_bounds__(kVsNT) sd_vshard_pick_kernel(const __grid_cons
       }
     }
   }
-  vs_draw_rows<E>(P, S, b);
   if (S.kind != 0 && warp == 0) {
-    // the shard holding u * S: prefix over the shards' masses (lane p: shard p)
+    // the shard holding u * S: prefix over the shards' masses (lane p: shard
+    // p, the sum of its parts in order)
     const int mm = S.m;
     ff x{0.f, 0.f}, y{0.f, 0.f};
     if (lane < P.S) {
-      const float4 m4 = __ldcg(reinterpret_cast<const float4 *>(
-          P.mass_all + (int64_t)lane * P.B * kVsMass + (int64_t)b * kVsMass));
-      x = ff{m4.x, m4.y};
-      y = ff{m4.z, m4.w};
+#pragma unroll
+      for (int q = 0; q < kVsParts; ++q) {
+        const float4 m4 = __ldcg(reinterpret_cast<const float4 *>(
+            P.mass_all + (int64_t)lane * P.B * kVsMass + (int64_t)b * kVsMass + 16 * q));
+        x = ff_add(x, ff{m4.x, m4.y});
+        y = ff_add(y, ff{m4.z, m4.w});
+      }
     }
     const ff tres = ff_warp_sum(x);
     // a draw from p at the bonus position, or for an identically zero residual
@@ -499,6 +515,24 @@ __global__ void __launch_bounds__(kVsNT) sd_vshard_pick_kernel(const __grid_cons
   }
   __syncthreads();
   if (S.kind != 0 && S.owner == P.shard) {
+    // the part of this shard holding u * S (lane q: part q)
+    if (warp == 0) {
+      ff mq{0.f, 0.f};
+      if (lane < kVsParts) {
+        const float4 m4 = __ldcg(reinterpret_cast<const float4 *>(
+            P.mass_all + (int64_t)P.shard * P.B * kVsMass + (int64_t)b * kVsMass + 16 * lane));
+        mq = S.kind == 2 ? ff{m4.z, m4.w} : ff{m4.x, m4.y};
+      }
+      const Cross c = ff_cross(mq, S.t_loc);
+      if (lane == 0) {
+        S.part = c.l < 0 ? 0 : c.l;
+        S.t_loc = ff_sub(S.t_loc, c.before);
+      }
+    }
+    __syncthreads();
+    int pa, pe;  // the part's columns, which the draw scans
+    vs_part(P.vs, S.part, pa, pe);
+    vs_draw_rows<E>(P, S, b, pa, pe);
     const int mm = S.m;
     const bool residual = S.kind == 1;
     const RowInfo &Rt = S.dt;
@@ -511,7 +545,7 @@ __global__ void __launch_bounds__(kVsNT) sd_vshard_pick_kernel(const __grid_cons
     const int wr = (nvec + NW - 1) / NW;
     const int wq0 = min(warp * wr, nvec), wq1 = min(wq0 + wr, nvec);
     float *pmw = pm + warp * P.pw * 32;
-    const ff lm = draw_pass<E>(Rt, S.dd, S.ddt, residual, d_vec, wq0, wq1, 0, P.vs, s2, ct2, cd2,
+    const ff lm = draw_pass<E>(Rt, S.dd, S.ddt, residual, d_vec, wq0, wq1, pa, pe, s2, ct2, cd2,
                                r2, pmw);
     const ff wm = ff_warp_sum(lm);
     if (lane == 0) S.wmass[warp] = wm;
@@ -559,18 +593,18 @@ __global__ void __launch_bounds__(kVsNT) sd_vshard_pick_kernel(const __grid_cons
           const ff t_l = ff_sub(t_it, cl.before);
           const int q = wq0 + isel * 32 + cl.l;
           const int i = lane % NV;
-          const uint4 tvv = load_vec_direct<E>(Rt, q, 0, P.vs);
+          const uint4 tvv = load_vec_direct<E>(Rt, q, pa, pe);
           uint4 dvv = tvv;
           if (residual)
-            dvv = d_vec ? load_vec_direct<E>(S.dd, q, 0, P.vs) : load_vec_slow<E>(S.ddt, q, 0, P.vs);
+            dvv = d_vec ? load_vec_direct<E>(S.dd, q, pa, pe) : load_vec_slow<E>(S.ddt, q, pa, pe);
           float ww[NV];
           pass_weights<E>(tvv, dvv, residual, s2, ct2, cd2, r2, ww);
           float wi = 0.f;
 #pragma unroll
           for (int ii = 0; ii < NV; ++ii)
             if (ii == i) wi = ww[ii];
-          const int ei = elem_index(0, Rt.hp, q, i, sz);
-          const bool ok = lane < NV && ei >= 0 && ei < P.vs && wi > 0.f;
+          const int ei = elem_index(pa, Rt.hp, q, i, sz);
+          const bool ok = lane < NV && ei >= pa && ei < pe && wi > 0.f;
           const Cross ce = ff_cross(ff{ok ? wi : 0.f, 0.f}, t_l);
           tok = __shfl_sync(0xffffffffu, ei, ce.l < 0 ? 0 : ce.l);
           if (ce.l < 0) tok = -1;
@@ -750,7 +784,8 @@ sd_status_t sd_vshard_mass(const sd_vshard_args *a, const void *stats_all, void 
   P.mass = (uint8_t *)mass;
   const void *fn = a->dtype == SD_BF16 ? (const void *)sd_vshard_mass_kernel<__nv_bfloat16>
                                        : (const void *)sd_vshard_mass_kernel<float>;
-  return vs_launch(fn, dim3((unsigned)P.B, 1, 1), 0, P, (cudaStream_t)stream, "sd_vshard_mass");
+  return vs_launch(fn, dim3((unsigned)P.B, kVsParts, 1), 0, P, (cudaStream_t)stream,
+                   "sd_vshard_mass");
 }
 
 sd_status_t sd_vshard_pick(const sd_vshard_args *a, const void *stats_all, const void *mass_all,
@@ -767,7 +802,9 @@ sd_status_t sd_vshard_pick(const sd_vshard_args *a, const void *stats_all, const
   P.stats_all = (const uint8_t *)stats_all;
   P.mass_all = (const uint8_t *)mass_all;
   const int sz = a->dtype == SD_BF16 ? 2 : 4;
-  const int nvec = (int)(((int64_t)P.vs * sz + 31) / 16) + 1;
+  int pa, pe;  // the draw scans one part of the shard: part 0 is the largest
+  vs_part(P.vs, 0, pa, pe);
+  const int nvec = (int)(((int64_t)(pe - pa) * sz + 31) / 16) + 1;
   P.pw = ((nvec + kVsNW - 1) / kVsNW + 31) / 32;
   const int smem = 4 * kVsNW * P.pw * 32;
   if (smem > kVsSmemCap) return SD_ERR_UNSUPPORTED;
