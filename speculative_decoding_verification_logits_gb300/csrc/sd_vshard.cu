@@ -34,7 +34,7 @@ namespace sdv {
 
 constexpr int kVsNT = 256;
 constexpr int kVsNW = kVsNT / 32;
-constexpr int kVsParts = 4;              // column parts of a shard (mass CTAs per sequence)
+constexpr int kVsParts = 8;              // column parts of a shard (mass CTAs per sequence)
 constexpr int kVsMass = 16 * kVsParts;   // bytes per sequence in a mass block
 constexpr int kVsCH = 4;  // vectors per row a mass thread loads before using them
 
