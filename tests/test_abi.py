@@ -113,7 +113,7 @@ def test_vshard_entry_points_refuse_bad_requests():
     P = ctypes.c_void_p
     fake = P(1 << 20)
     assert L.sd_vshard_stats_bytes(4, 3) == 4 * 8 * 96 + 4 * 3 * 16
-    assert L.sd_vshard_stats_bytes(-1, 3) == 0 and L.sd_vshard_mass_bytes(4) == 4 * 32
+    assert L.sd_vshard_stats_bytes(-1, 3) == 0 and L.sd_vshard_mass_bytes(4) == 4 * 128
     good = dict(B=4, K=3, V=100, S=2, shard=1, v0=50, vs=50, dtype=sd.SD_BF16)
     for bad in (dict(S=0), dict(S=33), dict(shard=2), dict(shard=-1), dict(v0=60),
                 dict(vs=0), dict(K=sd.SD_MAX_K + 1), dict(dtype=7), dict(flags=0x2)):
