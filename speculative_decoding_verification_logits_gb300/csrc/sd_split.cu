@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(NT, stream_ctas_per_sm<KF>())
   if (u_hi <= u_lo) return;  // more CTAs than steps
   const int64_t r_first = u_lo / P.spr;
   const int nrows = (int)((u_hi - 1) / P.spr - r_first + 1);  // <= kMaxRows (host)
+  int rb = 0, rfj = 0;  // this thread's row: its sequence and fan-out
   if (tid < nrows) {
     // flat row r: group g (position j = K - g), place i in the group
     const int64_t r = r_first + tid;
@@ -164,35 +165,30 @@ __global__ void __launch_bounds__(NT, stream_ctas_per_sm<KF>())
       b = lo;
       isx = rank[b + 1] > rank[b] && i == b + rank[b];
     }
-    // both loads issued before either is used
+    // where the row is (all the first copies need); what it is streamed for
+    // depends on inputs and is filled in once those copies are under way
     const int fj = (isx && g > 0 && P.keys) ? P.fanout[j] : 0;
-    const float T = P.temps[b];
-    const int tok = fj > 0 ? P.tokens[(int64_t)b * K + j] : -1;
-    const bool sampled = T > 0.f && T <= 3.4e38f;
     RowInfo &R = S.rows[tid];
     R.kind = isx ? (g == 0 ? kBonus : kDraft) : kTarget;
     R.j = j;
-    R.s = sampled ? log2e_over(T) : 0.f;
     R.rec = blockIdx.x + (int)r;
     R.excl = -1;
     R.fan = 0;
     if (R.kind == kTarget) {
       R.g = P.target + ((int64_t)b * (K + 1) + j) * P.V * sz;
-      R.type = sampled ? (P.argmax_out ? kRowEA : kRowE) : kRowA;
     } else if (R.kind == kDraft) {
       R.g = P.draft + ((int64_t)b * K + j) * P.V * sz;
-      R.type = sampled ? (fj > 0 ? kRowEK : kRowE) : kRowK;
       R.fan = fj;
-      if (fj > 0) R.excl = tok;
     } else {
       R.g = P.bonus + (int64_t)b * P.V * sz;
-      R.type = kRowK;
       R.fan = P.fanout[K];
     }
     const int64_t r0 = r * P.spr;
     const int64_t a = (u_lo > r0 ? u_lo : r0) - r0;
     const int64_t e = (u_hi < r0 + P.spr ? u_hi : r0 + P.spr) - r0;
     row_geometry<NT>(R, (int)(a * ue), (int)(e * ue < P.V ? e * ue : (int64_t)P.V), sz);
+    rb = b;
+    rfj = fj;
   }
   __syncthreads();
 
@@ -204,6 +200,30 @@ __global__ void __launch_bounds__(NT, stream_ctas_per_sm<KF>())
     issuer_row<NT>(I, S, nrows);
 #pragma unroll
     for (int d = 0; d < kDepth - 1; ++d) issue_fill<E, NT>(I, S, nrows, ring_t);
+    // with the first copies in flight: the row's scale and statistics (from
+    // the sequence's temperature) and the drafted token the keys exclude
+    if (tid < nrows) {
+      RowInfo &R = S.rows[tid];
+      const float T = P.temps[rb];  // both loads issued before either is used
+      const int tok = rfj > 0 ? P.tokens[(int64_t)rb * K + R.j] : -1;
+      const bool sampled = T > 0.f && T <= 3.4e38f;
+      R.s = sampled ? log2e_over(T) : 0.f;
+      if (R.kind == kTarget) {
+        R.type = sampled ? (P.argmax_out ? kRowEA : kRowE) : kRowA;
+      } else if (R.kind == kDraft) {
+        R.type = sampled ? (rfj > 0 ? kRowEK : kRowE) : kRowK;
+        if (rfj > 0) {
+          R.excl = tok;
+          if (tok >= R.v0 && tok < R.v1) {  // the piece's vector holding it
+            R.qd = ((tok - R.v0) * sz + R.hp) / 16;
+            R.qd_step = R.qd / (NT * kU);
+          }
+        }
+      } else {
+        R.type = kRowK;
+      }
+    }
+    __syncthreads();
     uint32_t c_off = tid * 16;
     RowAcc<KF> A;
     A.reset();
