@@ -595,9 +595,18 @@ static __device__ void compact_block(int B, int K, const int32_t *out_tokens, co
                               int *red) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int carry = 0;
+  constexpr int kPre = 16;  // rows this short are read along with their tau
+  const bool pre_on = K + 1 <= kPre;
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
     int t = 0;
+    int pre[kPre];
+    if (b < B && pre_on) {
+      const int32_t *src = out_tokens + (int64_t)b * (K + 1);
+#pragma unroll
+      for (int i = 0; i < kPre; ++i)
+        if (i <= K) pre[i] = cg_loads ? __ldcg(src + i) : src[i];
+    }
     if (b < B) {
       t = cg_loads ? __ldcg(tau + b) : tau[b];
       if (t < 0 || t > K + 1) {
@@ -628,8 +637,14 @@ static __device__ void compact_block(int B, int K, const int32_t *out_tokens, co
     const int excl = carry + (w > 0 ? red[w - 1] : 0) + x - t;
     if (b < B) {
       offsets[b] = excl;
-      const int32_t *src = out_tokens + (int64_t)b * (K + 1);
-      for (int i = 0; i < t; ++i) packed[excl + i] = cg_loads ? __ldcg(src + i) : src[i];
+      if (pre_on) {
+#pragma unroll
+        for (int i = 0; i < kPre; ++i)
+          if (i < t) packed[excl + i] = pre[i];
+      } else {
+        const int32_t *src = out_tokens + (int64_t)b * (K + 1);
+        for (int i = 0; i < t; ++i) packed[excl + i] = cg_loads ? __ldcg(src + i) : src[i];
+      }
     }
     carry += red[nw - 1];
     __syncthreads();
