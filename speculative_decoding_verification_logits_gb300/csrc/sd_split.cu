@@ -306,6 +306,7 @@ struct FinS {
   int2 keys[(SD_MAX_K + 1) * SD_MAX_FANOUT];
   RowInfo dt, dd;  // draw: target and draft row at m on this CTA's slice
   RowInfo ddt;     // the draft row read element-wise on the target's vector grid
+  RowInfo geo[2 * SD_MAX_K + 1];  // every row the draw may read: target j, then draft j
   ff wmass[kFinNW];
   ff cmass[2][kMaxCS];  // per-CTA masses of the draw, entry c pushed by CTA c
   ff t_loc, t_w;
@@ -423,6 +424,17 @@ __global__ void __launch_bounds__(kFinNT, 2) sd_finish_kernel(const __grid_const
     S.pc0[tid] = c0;
     S.npc[tid] = c1 - c0 + 1;
   }
+  // the geometry of every row the draw may read on this CTA's slice (the
+  // first rejection picks two of them)
+  const int v0 = min(rank * P.slice, P.V);
+  const int v1 = min(v0 + P.slice, P.V);
+  if (sampled && tid < 2 * K + 1) {
+    RowInfo &R = S.geo[tid];
+    R.g = tid <= K ? P.target + ((int64_t)b * (K + 1) + tid) * P.V * sz
+                   : P.draft + ((int64_t)b * K + (tid - K - 1)) * P.V * sz;
+    R.excl = -1;
+    row_geometry<NT>(R, v0, v1, sz);
+  }
   __syncthreads();
 
   // ---- the streaming grid has finished and its records are visible
@@ -471,8 +483,6 @@ __global__ void __launch_bounds__(kFinNT, 2) sd_finish_kernel(const __grid_const
   }
   __syncthreads();
 
-  const int v0 = min(rank * P.slice, P.V);
-  const int v1 = min(v0 + P.slice, P.V);
   if (warp == 0) {
     // ---- accept tests, one lane per position (K <= 32)
     const int j = lane;
@@ -505,13 +515,8 @@ __global__ void __launch_bounds__(kFinNT, 2) sd_finish_kernel(const __grid_const
     const unsigned rejects = ballot(rej);
     const int mm = rejects ? __ffs(rejects) - 1 : K;
     const bool valid = tvalid && dvalid && S.fvalid != 0;
-    if (sampled && valid && lane < 2 && (lane == 0 || mm < K)) {  // the rows the draw reads
-      RowInfo &R = lane == 0 ? S.dt : S.dd;
-      R.g = lane == 0 ? P.target + ((int64_t)b * (K + 1) + mm) * P.V * sz
-                      : P.draft + ((int64_t)b * K + mm) * P.V * sz;
-      R.excl = -1;
-      row_geometry<NT>(R, v0, v1, sz);
-    }
+    if (sampled && valid && lane < 2 && (lane == 0 || mm < K))  // the rows the draw reads
+      (lane == 0 ? S.dt : S.dd) = S.geo[lane == 0 ? mm : K + 1 + mm];
     __syncwarp();
     if (sampled && valid && lane == 0 && mm < K && S.dd.hp != S.dt.hp) {
       S.ddt = S.dt;
