@@ -200,7 +200,7 @@ def algorithmic_bytes(inp: W.Inputs) -> int:
 
 
 # ---------------------------------------------------------------- GPU arm ---
-# BASELINE configs 1..5, in order: the per-config object of the default run
+# the five benchmark workloads, in order (configs 1..5): the per-config object of the default run
 CONFIGS = ["small", "peaked", "zipf", "saguaro", "mix"]
 
 
@@ -419,7 +419,7 @@ def run_gpu(args):
     name = args.workload
     m = measure(name, args.steps, args.warmup, dev, rank, ws_n,
                 e2e_steps=0 if args.no_e2e else min(args.steps, args.e2e_steps))
-    # every BASELINE config measured in the same run (the default run only)
+    # every benchmark workload measured in the same run (the default run only)
     per = {}
     if name == HEADLINE and not args.no_per_config:
         for c in CONFIGS:
