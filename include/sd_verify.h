@@ -245,10 +245,12 @@ sd_status_t sd_outcome_predict(int32_t B, int32_t K, int32_t V, sd_dtype_t dtype
  *   sd_vshard_mass   -> this shard's mass block (sd_vshard_mass_bytes):
  *                       every shard combines all rows' statistics and takes
  *                       the same accept decisions, then measures its own
- *                       columns' share of the draw; all-gather into mass_all;
+ *                       columns' share of the draw, part by part (eight
+ *                       column parts per shard); all-gather into mass_all;
  *   sd_vshard_pick   -> outputs: the prefix over the shards' masses names the
- *                       shard holding u * S, which alone scans its columns
- *                       (a two-level inverse CDF) and writes the token and the
+ *                       shard holding u * S and the prefix over its parts the
+ *                       part; that shard alone scans the part's columns (an
+ *                       inverse CDF in levels) and writes the token and the
  *                       hit flag of a sampled row; every shard writes the
  *                       rest, which is the same everywhere.
  * Pre-fill out_tokens with -1 and hit with 0: an element-wise maximum over
