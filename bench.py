@@ -356,7 +356,14 @@ def measure(name, steps, warmup, dev, rank, ws_n, e2e_steps=0):
                 hp["anchor"] = p.meta["anchor"].cpu().pin_memory()
                 hp["anchor_pos"] = p.meta["anchor_pos"].cpu().pin_memory()
             host.append(hp)
-        dbuf = {k: torch.empty_like(v, device=dev) for k, v in host[0].items()}
+        # two device copies of the inputs: step i's are copied on copy_stream
+        # while step i - 1 verifies on `stream`
+        dbufs = [{k: torch.empty_like(v, device=dev) for k, v in host[0].items()}
+                 for _ in range(2)]
+        copy_stream = torch.cuda.Stream(dev)
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        used = [torch.cuda.Event(), torch.cuda.Event()]
+        torch.cuda.synchronize(dev)
         r_host = {"out_tokens": torch.empty((B, K + 1), dtype=torch.int32).pin_memory(),
                   "tau": torch.empty(B, dtype=torch.int32).pin_memory(),
                   "hit": torch.empty(B, dtype=torch.uint8).pin_memory(),
@@ -368,10 +375,16 @@ def measure(name, steps, warmup, dev, rank, ws_n, e2e_steps=0):
         n_e2e = max(1, e2e_steps)
 
         def e2e_run():
+            copy_stream.wait_stream(stream)
             for i in range(n_e2e):
-                hp = host[i % 2]
-                for k, t in hp.items():
-                    dbuf[k].copy_(t, non_blocking=True)
+                hp, dbuf = host[i % 2], dbufs[i % 2]
+                with torch.cuda.stream(copy_stream):
+                    if i >= 2:   # step i - 2 has finished reading this buffer
+                        copy_stream.wait_event(used[i % 2])
+                    for k, t in hp.items():
+                        dbuf[k].copy_(t, non_blocking=True)
+                    copied[i % 2].record(copy_stream)
+                stream.wait_event(copied[i % 2])
                 sd.verify(dbuf["target"], dbuf["draft"], dbuf["tokens"], dbuf["temperature"],
                           pool[0].seed + i, row_base=rank * B, fanout=fan,
                           draft_bonus=dbuf.get("draft_bonus"), compact=True, out=out0, ws=wss,
@@ -379,8 +392,10 @@ def measure(name, steps, warmup, dev, rank, ws_n, e2e_steps=0):
                 if pack:
                     sd.d3d_pack(out0.keys, dbuf["tokens"], dbuf["anchor"], dbuf["anchor_pos"],
                                 pool[0].meta["mask_token"], out=packs[0], stream=stream)
+                used[i % 2].record(stream)
                 for k, t in r_host.items():
                     t.copy_(getattr(out0, k), non_blocking=True)
+            stream.wait_stream(copy_stream)
 
         with torch.cuda.stream(stream):
             e2e_run()
