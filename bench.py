@@ -374,17 +374,25 @@ def measure(name, steps, warmup, dev, rank, ws_n, e2e_steps=0):
         out0 = outs[0]
         n_e2e = max(1, e2e_steps)
 
+        # overlapped copies pay off once the link is the bound; for a few MB
+        # per step the extra stream and event calls cost more host time
+        overlap = h2d >= (8 << 20)
+
         def e2e_run():
             copy_stream.wait_stream(stream)
             for i in range(n_e2e):
-                hp, dbuf = host[i % 2], dbufs[i % 2]
-                with torch.cuda.stream(copy_stream):
-                    if i >= 2:   # step i - 2 has finished reading this buffer
-                        copy_stream.wait_event(used[i % 2])
+                hp, dbuf = host[i % 2], dbufs[i % 2 if overlap else 0]
+                if overlap:
+                    with torch.cuda.stream(copy_stream):
+                        if i >= 2:   # step i - 2 has finished reading this buffer
+                            copy_stream.wait_event(used[i % 2])
+                        for k, t in hp.items():
+                            dbuf[k].copy_(t, non_blocking=True)
+                        copied[i % 2].record(copy_stream)
+                    stream.wait_event(copied[i % 2])
+                else:
                     for k, t in hp.items():
                         dbuf[k].copy_(t, non_blocking=True)
-                    copied[i % 2].record(copy_stream)
-                stream.wait_event(copied[i % 2])
                 sd.verify(dbuf["target"], dbuf["draft"], dbuf["tokens"], dbuf["temperature"],
                           pool[0].seed + i, row_base=rank * B, fanout=fan,
                           draft_bonus=dbuf.get("draft_bonus"), compact=True, out=out0, ws=wss,
@@ -392,7 +400,8 @@ def measure(name, steps, warmup, dev, rank, ws_n, e2e_steps=0):
                 if pack:
                     sd.d3d_pack(out0.keys, dbuf["tokens"], dbuf["anchor"], dbuf["anchor_pos"],
                                 pool[0].meta["mask_token"], out=packs[0], stream=stream)
-                used[i % 2].record(stream)
+                if overlap:
+                    used[i % 2].record(stream)
                 for k, t in r_host.items():
                     t.copy_(getattr(out0, k), non_blocking=True)
             stream.wait_stream(copy_stream)
@@ -401,7 +410,9 @@ def measure(name, steps, warmup, dev, rank, ws_n, e2e_steps=0):
             e2e_run()
             ms_e2e = timed(e2e_run)
         e2e = {"value": ws_n * n_e2e / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": n_e2e}
+               "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "copies": "overlapped with the previous step's verify" if overlap
+                         else "in order with the verify"}
 
     # one round of set 0 with its first seed: the CPU baseline's oracle sample
     # runs on the same inputs, and its outputs are compared with these
