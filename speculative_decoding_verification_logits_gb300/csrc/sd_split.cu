@@ -8,8 +8,10 @@
 // row for j = K) when the sequence needs it, then target row j; draft rows
 // with keys and target rows alternate, so every CTA sees the same mix of
 // row kinds.  The rows of the first positions, where a rejection is
-// likeliest, come last and are still in L2 when the finish re-reads them.
-// One row loop serves every kind of row (the statistics a row needs --
+// likeliest, come last, so that the finish finds them in L2 when a round's
+// logits fit there.  A CTA issues its first copies as soon as it knows where
+// its rows are, before it loads the temperatures and drafted tokens that say
+// what each row is streamed for.  One row loop serves every kind of row (the statistics a row needs --
 // offset exp-sum, argmax, key vectors, the finiteness check -- are switched
 // per row), and ragged vectors are assembled into the copy ring where they
 // are issued, so the loop always consumes whole steps.  Per row piece the
@@ -19,7 +21,8 @@
 // Finish.  One thread-block cluster per sequence, launched as a
 // programmatic dependent of the streaming grid: its prologue (drafted
 // tokens, their logits, the uniforms, the sequence's place in the flat
-// order) reads only inputs and overlaps the stream's tail.  Then every CTA
+// order, the geometry of every row the draw may read) reads only inputs and
+// overlaps the stream's tail.  Then every CTA
 // combines the records of each row in the same order, so all CTAs take the
 // same accept decisions; warp 0 runs the accept scan while the other warps
 // merge the key candidates.  The draw (residual max(0, p - q) at the first
